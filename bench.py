@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Benchmark of compressed-KV-cache attention on GB300.
+
+One step = the whole hot path over one synthetic prompt of the workload:
+prefill compression of every layer (scoring, pooling, top-k, gather +
+quantize + pack, window init), then every decode step over all layers (append
+with group flushes, split-K decode attention). Inputs are resident in HBM before
+the timed region; L2 is flushed (256 MiB memset, outside the measured kernel
+intervals) before every decode step, as the rest of a model would between two
+tokens; the prefill inputs (4.3 GB for the default workload) exceed L2.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "compressed-KV decode tokens/s, cache GB/s vs HBM peak; compress ms/layer"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--decode-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def rank_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def workload_desc(spec, S):
+    sched = (f"pyramid avg {spec.avg_budget} depth {spec.pyramid_depth}"
+             if spec.schedule == "pyramid" else
+             (f"uniform {spec.avg_budget}" if spec.schedule == "uniform" else "no eviction"))
+    return (f"{spec.name}: {spec.n_layers} layers, {spec.n_q_heads}/{spec.n_kv_heads} heads, "
+            f"d{spec.head_dim}, batch {spec.batch}, prompt {spec.prompt_len}, {sched}, "
+            f"obs {spec.obs_window}, pool {spec.pool_kernel}, {spec.bits}-bit g{spec.group_size}, "
+            f"bf16 window {spec.window_len}, {S} decode steps")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, enabled=True):
+        self.proc = None
+        self.path = f"/tmp/kvc_clocks_{os.getpid()}.csv"
+        if enabled:
+            try:
+                self.f = open(self.path, "w")
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(index), f"--query-gpu={self.QUERY}",
+                     "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=self.f, stderr=subprocess.DEVNULL)
+            except Exception:
+                self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        if not sm:
+            return None
+        loaded = [s for s in sm if mx and s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+def oracle_sample(spec, n_layers_sample=2, n_steps=8):
+    """Time the CPU oracle on a bounded sample of the workload.
+
+    Returns (compress seconds per layer, decode seconds per token per layer, text).
+    """
+    import numpy as np
+    import synth
+    from oracle import OracleCache
+    budgets = _budgets_host(spec)
+    t_comp, t_dec, layers = 0.0, 0.0, list(range(n_layers_sample))
+    for layer in layers:
+        x = synth.layer_inputs(spec, layer, device="cpu")
+        k = x["k"].float().double().numpy()
+        v = x["v"].float().double().numpy()
+        q = x["q_obs"].float().double().numpy() if "q_obs" in x else None
+        oc = OracleCache(spec.batch, spec.n_q_heads, spec.n_kv_heads, spec.head_dim, spec.bits,
+                         spec.group_size, spec.window_len)
+        ns = spec.prompt_len - spec.obs_window
+        t0 = time.perf_counter()
+        oc.prefill(k, v, spec.obs_window, budget=budgets[layer] if budgets[layer] < ns else None,
+                   q_obs=q, pool_kernel=spec.pool_kernel)
+        t_comp += time.perf_counter() - t0
+        for t in range(n_steps):
+            dx = synth.decode_inputs(spec, layer, t, device="cpu")
+            args = [dx[n].float().double().numpy() for n in ("q", "k_new", "v_new")]
+            t0 = time.perf_counter()
+            oc.step(*args)
+            t_dec += time.perf_counter() - t0
+    text = (f"oracle on layers 0..{n_layers_sample - 1} (full prompt, all heads) + "
+            f"{n_steps} decode steps each; extrapolated linearly to {spec.n_layers} layers")
+    return t_comp / len(layers), t_dec / (len(layers) * n_steps), text
+
+
+def _budgets_host(spec):
+    from oracle import plan_budgets
+    ns = spec.prompt_len - spec.obs_window
+    if spec.schedule == "none":
+        return [ns] * spec.n_layers
+    return plan_budgets(spec.n_layers, spec.schedule, spec.avg_budget, spec.pyramid_depth,
+                        spec.group_size, max_budget=ns)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    import synth
+    spec = synth.workload(args.workload)
+    S = args.decode_steps or spec.steps
+    vals, comp, per_tok = [], [], []
+    text = ""
+    for i in range(args.warmup + args.steps):
+        c, d, text = oracle_sample(spec, n_layers_sample=1, n_steps=4)
+        if i >= args.warmup:
+            per_token = d * spec.n_layers
+            vals.append(spec.batch / per_token)
+            comp.append(c * 1e3)
+            per_tok.append(per_token)
+    value = statistics.mean(vals)
+    step_s = statistics.mean(comp) / 1e3 * spec.n_layers + statistics.mean(per_tok) * S
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (quantizer f32)", "data": "synthetic",
+        "config": {"workload": workload_desc(spec, S)},
+        "compress_ms_per_layer": statistics.mean(comp),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": text},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def kernel_hash(name):
+    p = os.path.join(ROOT, "kv_cache_compression_snapkv_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_file):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source
+    is unchanged since the capture (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t[kernel_file]
+        if e["source_sha256_16"] != kernel_hash(kernel_file):
+            return None
+        return e
+    except Exception:
+        return None
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    rank, world, local = rank_info()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import synth
+    import kv_cache_compression_snapkv_gb300 as K
+
+    spec = synth.workload(args.workload)
+    S = args.decode_steps or spec.steps
+    L, B, Hq, Hk, D = spec.n_layers, spec.batch, spec.n_q_heads, spec.n_kv_heads, spec.head_dim
+    dims = K.dims_from_spec(spec, max_new_tokens=S)
+    budgets = K.kvc_plan_budgets(dims, spec.schedule, spec.avg_budget, spec.pyramid_depth)
+    dev = torch.device("cuda", local)
+
+    # ---- inputs resident in HBM
+    prompt = [synth.layer_inputs(spec, l, device=dev) for l in range(L)]
+    qs, kns, vns = [], [], []
+    for t in range(S):
+        dx = synth.decode_inputs_layers(spec, t, range(L), device=dev)
+        qs.append(dx["q"]); kns.append(dx["k_new"]); vns.append(dx["v_new"])
+    out = torch.empty(L, B, Hq, D, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cache = K.kvc_cache_create(dims, budgets)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    c0, c1 = ev(), ev()
+    dev_ev = [(ev(), ev(), ev()) for _ in range(S)]
+    block_bytes = 8 * D * (spec.bits + 1)
+
+    dec_bytes = []   # algorithmic bytes of each decode-attention launch
+
+    def one_step(record_bytes=False):
+        K.kvc_cache_reset(cache)
+        c0.record(stream)
+        for l in range(L):
+            x = prompt[l]
+            K.kvc_prefill_compress(dims, budgets, l, x.get("q_obs"), x["k"], x["v"], cache=cache)
+        c1.record(stream)
+        for t in range(S):
+            flush.zero_()
+            e0, e1, e2 = dev_ev[t]
+            e0.record(stream)
+            K.kvc_append_layers(cache, 0, L, kns[t], vns[t])
+            e1.record(stream)
+            K.kvc_decode_attn(cache, 0, L, qs[t], out)
+            e2.record(stream)
+            if record_bytes:
+                tot = 0
+                for l in range(L):
+                    info = K.kvc_layer_info_get(cache, l)
+                    tot += B * Hk * (info["packed_tokens"] // 32 * block_bytes
+                                     + info["window_tokens"] * D * 4)
+                tot += L * B * Hq * D * (2 + 4)
+                dec_bytes.append(tot)
+
+    def collect():
+        torch.cuda.synchronize()
+        comp = c0.elapsed_time(c1)
+        app = [dev_ev[t][0].elapsed_time(dev_ev[t][1]) for t in range(S)]
+        att = [dev_ev[t][1].elapsed_time(dev_ev[t][2]) for t in range(S)]
+        return comp, app, att
+
+    one_step(record_bytes=True)
+    collect()
+    for _ in range(max(0, args.warmup - 1)):
+        one_step()
+        collect()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    n0 = K.kvc_launch_count()
+    t_wall0 = time.perf_counter()
+    comps, apps, atts = [], [], []
+    for _ in range(args.steps):
+        one_step()
+        comp, app, att = collect()
+        comps.append(comp); apps.append(app); atts.append(att)
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - t_wall0) / args.steps
+    launches = K.kvc_launch_count() - n0
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+
+    comp_ms = statistics.mean(comps)
+    dec_ms = statistics.mean([sum(a) + sum(b) for a, b in zip(apps, atts)])
+    att_ms_all = [x for a in atts for x in a]
+    att_ms = statistics.mean(att_ms_all)
+    step_ms = comp_ms + dec_ms
+    if world > 1:
+        t = torch.tensor([step_ms, dec_ms, comp_ms, att_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, dec_ms, comp_ms, att_ms = [float(v) for v in t.tolist()]
+
+    hbm, tc, peak_kind = peaks()
+    tokens = B * S * world
+    value = tokens / (dec_ms / 1e3)
+    # decode attention: algorithmic bytes per launch / mean launch duration
+    mean_bytes = statistics.mean(dec_bytes)
+    dec_gbs = mean_bytes / (att_ms / 1e3) / 1e9
+    # compression: algorithmic bytes and flops per layer
+    ns = spec.prompt_len - spec.obs_window
+    comp_bytes = comp_flops = 0
+    for l in range(L):
+        kept = min(budgets[l], ns)
+        scored = kept < ns
+        comp_bytes += (B * Hk * spec.prompt_len * D * 2 * (1 if scored else 2)
+                       + (B * Hk * kept * D * 2 * 2 if scored else 0)
+                       + B * Hk * (kept // 32) * block_bytes
+                       + (B * Hq * spec.obs_window * D * 2 if scored else 0))
+        comp_flops += 2 * B * Hq * spec.obs_window * spec.prompt_len * D if scored else 0
+    t_roof = max(comp_bytes / (hbm * 1e9), comp_flops / (tc * 1e12))
+    comp_frac = t_roof / (comp_ms / 1e3)
+
+    traffic = profiled_traffic("decode.cu")
+    roofline = {"kernel": "decode_kernel (split-K decode attention, all layers per launch)",
+                "bound": "hbm", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": dec_gbs / hbm, "peak_source": peak_kind + " (burst copy)",
+                "bytes_per_launch": mean_bytes,
+                "traffic": traffic["dram_bytes_per_launch"] if traffic else None}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int2 codes + bf16 window (fp16/bf16 mma, fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(spec, S),
+                   "l2": "flushed (256 MiB) before every decode step; prefill inputs exceed L2",
+                   "decode_launch": f"one append + one attention launch per token for all {L} layers",
+                   "parallelism": f"replicas x{world}"},
+        "decode_tokens_per_s": value,
+        "cache_gbs": dec_gbs, "cache_frac_of_hbm": dec_gbs / hbm,
+        "decode_attn_us_per_launch": att_ms * 1e3,
+        "append_us_per_launch": statistics.mean([x for a in apps for x in a]) * 1e3,
+        "compress_ms_per_layer": comp_ms / L,
+        "compress_roofline": {"bytes": comp_bytes, "flops": comp_flops, "t_roof_ms": t_roof * 1e3,
+                              "frac": comp_frac},
+        "wall_ms_per_step": wall * 1e3,
+        "roofline": roofline,
+        "gpu_launches": launches,
+        "gpu_launches_per_step": launches / args.steps,
+    }
+    if clk:
+        line["clocks"] = clk
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_measure(K, spec, dims, budgets, cache, prompt, qs, kns, vns, S, dev)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        c, d, text = oracle_sample(spec)
+        per_token = d * L
+        line["cpu_baseline"] = {"value": B / per_token, "unit": UNIT, "cores": cpu_cores(),
+                                "kind": "oracle", "sample": text,
+                                "compress_ms_per_layer": c * 1e3}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    cache.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def e2e_measure(K, spec, dims, budgets, cache, prompt, qs, kns, vns, S, dev, steps=2):
+    """Same metric through the C ABI with host buffers: every step copies the
+    prompt (pinned host -> device) before compressing it, and each decode step's
+    inputs in and its output back."""
+    import torch
+    L = spec.n_layers
+    hp = [{k: v.cpu().pin_memory() for k, v in x.items()
+           if isinstance(v, torch.Tensor) and k in ("q_obs", "k", "v")} for x in prompt]
+    hq = torch.stack(qs).cpu().pin_memory()
+    hk = torch.stack(kns).cpu().pin_memory()
+    hv = torch.stack(vns).cpu().pin_memory()
+    hout = torch.empty(S, *qs[0].shape, dtype=torch.float32).pin_memory()
+    dp = {k: torch.empty_like(v, device=dev) for k, v in hp[0].items()}
+    dq, dk, dv = (torch.empty_like(qs[0]), torch.empty_like(kns[0]), torch.empty_like(vns[0]))
+    dout = torch.empty(qs[0].shape, dtype=torch.float32, device=dev)
+    h2d = sum(v.numel() * v.element_size() for x in hp for v in x.values()) + \
+        (hq.numel() * hq.element_size() + hk.numel() * hk.element_size() +
+         hv.numel() * hv.element_size())
+    d2h = hout.numel() * 4
+
+    def step():
+        K.kvc_cache_reset(cache)
+        for l in range(L):
+            for k in dp:
+                dp[k].copy_(hp[l][k], non_blocking=True)
+            K.kvc_prefill_compress(dims, budgets, l, dp.get("q_obs"), dp["k"], dp["v"],
+                                   cache=cache)
+        for t in range(S):
+            dq.copy_(hq[t], non_blocking=True)
+            dk.copy_(hk[t], non_blocking=True)
+            dv.copy_(hv[t], non_blocking=True)
+            K.kvc_decode_step(cache, 0, L, dq, dk, dv, dout)
+            hout[t].copy_(dout, non_blocking=True)
+        torch.cuda.synchronize()
+
+    step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": spec.batch * S / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3,
+            "note": "includes the prompt's host->device copy and prefill compression"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

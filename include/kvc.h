@@ -1,0 +1,265 @@
+/*
+ * kvc.h -- compressed-KV-cache attention on one GB300 (sm_103a): the C ABI.
+ *
+ * Two halves of one serving path:
+ *   prefill   score every prompt key by the attention a trailing observation
+ *             window of queries pays it, max-pool the scores, keep a per-head
+ *             top-k under a per-layer budget, and store the survivors as 2- or
+ *             4-bit group-quantized codes (keys per channel, values per token,
+ *             groups of 32, fp16 scale + zero-point per group);
+ *   decode    append each new key/value to a bf16 recent window that is
+ *             quantized group by group as it fills, and attend one query per
+ *             head (GQA-aware) over packed codes + window in one softmax.
+ *
+ * Sources of the method (page title, section):
+ *   PyramidKV: Dynamic KV Cache Compression based on Pyramidal Information
+ *     Funneling -- §4.2 (per-layer budgets, arithmetic sequence, bottom layers
+ *     get more), §4.2.2 KV Cache Selection (instruction-token scores, pooling,
+ *     per-head top-k, the last alpha tokens always kept).
+ *   MiniKV: Pushing the Limits of LLM Inference via 2-Bit Layer-Discriminative
+ *     KV Cache -- §2 eq. (1) and Definition 2.1 (the co-compression problem:
+ *     layers, heads, head dim, budget, bits), §4.1 (selection frozen after
+ *     prefill), §4.2 (uniform / pyramid budgets), §4.4 and Algorithm 1
+ *     (quantize the selected tokens, pack codes into INT32 words with FP16 scale
+ *     and zero-point, streaming 16-bit buffer, one softmax over packed + buffer).
+ *   KV Cache Compression: Eviction and Quantization (blog) -- "Quantization:
+ *     keep each token in fewer bits" and "Measured on a real model" (zero-point
+ *     = group min, scale = (max - min)/(2^b - 1), keys per channel, values per
+ *     token, exact recent window).
+ *
+ * Conventions for every call
+ *   - Device pointers are caller-owned (e.g. PyTorch tensors). They are only
+ *     borrowed until the work enqueued on `stream` completes; the library never
+ *     frees them. `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   - All work is stream-ordered. One cache must be used from one stream at a
+ *     time; calls on one cache must not overlap.
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     failing call returns a status and enqueues nothing (or, for a launch
+ *     failure, KVC_E_CUDA). Calls never abort, exit or trap.
+ *   - Tensors are dense, row-major, bf16 unless stated; outputs are fp32.
+ */
+#ifndef KVC_H_
+#define KVC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvc_status {
+  KVC_OK = 0,
+  KVC_E_ARG = 1,          /* null pointer or argument value out of range        */
+  KVC_E_SHAPE = 2,        /* dimensions unsupported or inconsistent             */
+  KVC_E_OOM = 3,          /* device allocation failed                           */
+  KVC_E_CUDA = 4,         /* a CUDA runtime call or kernel launch failed        */
+  KVC_E_STATE = 5,        /* call out of order (e.g. decode before prefill)     */
+  KVC_E_CAPACITY = 6,     /* more appended tokens than max_new_tokens allows    */
+  KVC_E_TIMEOUT = 7,      /* a bounded device-side wait gave up                 */
+  KVC_E_DEVICE_CHECK = 8  /* a device-side check recorded an error              */
+} kvc_status;
+
+/* Per-layer budget schedules (PyramidKV §4.2; MiniKV §4.2). */
+typedef enum kvc_schedule {
+  KVC_SCHED_NONE = 0,     /* keep every prompt token (quantize-only cache)      */
+  KVC_SCHED_UNIFORM = 1,  /* every layer keeps avg_budget tokens per head       */
+  KVC_SCHED_PYRAMID = 2   /* linear: layer 0 gets 2x - x/d, the top layer x/d   */
+} kvc_schedule;
+
+/* Optional allocator hooks (e.g. a framework's caching allocator). When
+ * `alloc` is NULL the library uses cudaMalloc / cudaFree. */
+typedef void* (*kvc_alloc_fn)(size_t bytes, void* stream, void* ctx);
+typedef void (*kvc_free_fn)(void* ptr, void* stream, void* ctx);
+
+/* The problem statement (MiniKV Definition 2.1 plus the selection and window
+ * parameters of PyramidKV §4.2.2 and MiniKV §4.4). */
+typedef struct kvc_dims {
+  int32_t n_layers;       /* transformer layers (1..256)                           */
+  int32_t batch;          /* independent sequences                                 */
+  int32_t n_q_heads;      /* query heads; a multiple of n_kv_heads                 */
+  int32_t n_kv_heads;     /* key/value heads (GQA group g = n_q_heads/n_kv_heads,  */
+                          /*   g in {1, 2, 4, 8})                                  */
+  int32_t head_dim;       /* 64 or 128                                             */
+  int32_t prompt_len;     /* n, tokens in the prompt                               */
+  int32_t obs_window;     /* alpha, trailing observation/instruction tokens;       */
+                          /*   0 only with KVC_SCHED_NONE budgets (no scoring)     */
+  int32_t pool_kernel;    /* w, odd max-pool width (1 = no pooling)                */
+  int32_t bits;           /* 2 or 4                                                */
+  int32_t group_size;     /* G, quantization group; must be 32                     */
+  int32_t window_len;     /* R, bf16 recent window; a multiple of G, 32..1024      */
+  int32_t max_new_tokens; /* decode steps the cache is sized for                   */
+  kvc_alloc_fn alloc;     /* optional; NULL = cudaMalloc                           */
+  kvc_free_fn free;       /* optional; must be set when alloc is                   */
+  void* alloc_ctx;        /* passed to alloc/free                                  */
+} kvc_dims;
+
+typedef struct kvc_cache kvc_cache;   /* opaque; owns its device storage */
+
+/* ---------------------------------------------------------------------------
+ * kvc_plan_budgets -- per-layer token budgets (host only, no device work).
+ *   PyramidKV §4.2 / MiniKV §4.2. For KVC_SCHED_PYRAMID the budgets run linearly
+ *   from 2x - x/d (layer 0) down to x/d (top layer), x = avg_budget and
+ *   d = pyramid_depth, in whole groups of G tokens: unit budgets are floored and
+ *   the leftover units go to the largest remainders (ties to the lower layer),
+ *   so they sum to exactly n_layers * avg_budget. UNIFORM gives avg_budget to
+ *   every layer; NONE gives prompt_len (keep all). Every budget is finally
+ *   clipped to prompt_len - obs_window.
+ *   budgets_out: host array of n_layers int32 (written).
+ *   Errors: KVC_E_ARG (null pointer, avg_budget not a positive multiple of G,
+ *   pyramid_depth < 1), KVC_E_SHAPE (invalid dims).
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_plan_budgets(const kvc_dims* dims, kvc_schedule schedule,
+                            int32_t avg_budget, int32_t pyramid_depth,
+                            int32_t* budgets_out);
+
+/* ---------------------------------------------------------------------------
+ * kvc_prefill_compress -- compress one layer's prompt into the cache.
+ *   PyramidKV §4.2.2; MiniKV §4.1, §4.4 and Algorithm 1 (prefill part).
+ *   If *cache is NULL a cache is created for `dims` and `budgets` (host,
+ *   n_layers int32, as from kvc_plan_budgets) and returned in *cache; later
+ *   calls must pass the same dims. Each layer is compressed once.
+ *   q_obs: device bf16 [batch][n_q_heads][obs_window][head_dim], the queries of
+ *          the last obs_window prompt positions (may be NULL when the layer's
+ *          budget keeps every token).
+ *   k, v:  device bf16 [batch][n_kv_heads][prompt_len][head_dim] (post-RoPE keys).
+ *   Computes, per (sequence, kv head): causal softmax of q_obs.k^T/sqrt(d) per
+ *   observation row, summed over rows and over the g query heads of the group,
+ *   for keys [0, n - alpha); a max-pool of width pool_kernel; the
+ *   min(budget, n - alpha) largest pooled scores (ties to the lower index);
+ *   whole groups of 32 kept tokens (ascending position) are quantized into the
+ *   packed store; the remaining kept tokens and then the alpha observation
+ *   tokens start the bf16 window.
+ *   Errors: KVC_E_ARG, KVC_E_SHAPE (e.g. initial window not shorter than R),
+ *   KVC_E_STATE (layer already compressed), KVC_E_OOM, KVC_E_CUDA.
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets,
+                                int32_t layer, const void* q_obs, const void* k,
+                                const void* v, kvc_cache** cache, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * kvc_prefill_selected -- like kvc_prefill_compress, but with the kept
+ *   positions supplied by the caller instead of scored (any selection policy:
+ *   e.g. attention sinks + recent tokens, StreamingLLM-style).
+ *   kept: device int32 [batch][n_kv_heads][n_kept], strictly ascending, each in
+ *   [0, prompt_len - obs_window); n_kept <= the layer's budget. The cache must
+ *   exist (created by kvc_prefill_compress or kvc_cache_create).
+ *   Errors: as kvc_prefill_compress; KVC_E_CAPACITY if n_kept > budget. Index
+ *   order/range is the caller's contract (not checked on the device).
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_prefill_selected(kvc_cache* cache, int32_t layer, const int32_t* kept,
+                                int32_t n_kept, const void* k, const void* v,
+                                void* stream);
+
+/* kvc_cache_create -- create an empty cache for dims/budgets (what
+ * kvc_prefill_compress does when *cache is NULL). */
+kvc_status kvc_cache_create(const kvc_dims* dims, const int32_t* budgets,
+                            kvc_cache** cache);
+
+/* ---------------------------------------------------------------------------
+ * kvc_append -- append one token per (sequence, kv head) to one layer.
+ *   MiniKV Algorithm 1 (decoding: concatenate into the 16-bit buffer; quantize
+ *   when it fills). k_new, v_new: device bf16 [batch][n_kv_heads][head_dim].
+ *   When the window reaches window_len tokens its oldest 32 are quantized as
+ *   one key group (per channel) and 32 value rows (per token) and leave it.
+ *   Errors: KVC_E_STATE (layer not prefilled), KVC_E_CAPACITY (more than
+ *   max_new_tokens appends), KVC_E_ARG, KVC_E_CUDA.
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_append(kvc_cache* cache, int32_t layer, const void* k_new,
+                      const void* v_new, void* stream);
+
+/* kvc_append_layers -- kvc_append over layers [layer_begin, +layer_count) in
+ * one launch; k_new, v_new: device bf16 [layer_count][batch][n_kv_heads][head_dim]. */
+kvc_status kvc_append_layers(kvc_cache* cache, int32_t layer_begin, int32_t layer_count,
+                             const void* k_new, const void* v_new, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * kvc_decode_attn -- decode attention of one query per head.
+ *   MiniKV §2 eq. (1), Algorithm 1 (one softmax over dequantized packed keys
+ *   and the window's keys; output = A_quant.dequant(V) + A_window.V_window);
+ *   blog "Measured on a real model" (exact window, rounded rest).
+ *   q:   device bf16 [layer_count][batch][n_q_heads][head_dim].
+ *   out: device fp32 [layer_count][batch][n_q_heads][head_dim] (written).
+ *   Query head j reads kv head j / g. Split-K over the packed store and the
+ *   window, merged with a log-sum-exp combine inside the same launch.
+ *   Errors: KVC_E_STATE (a layer not prefilled), KVC_E_ARG, KVC_E_CUDA.
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_decode_attn(kvc_cache* cache, int32_t layer_begin, int32_t layer_count,
+                           const void* q, float* out, void* stream);
+
+/* kvc_decode_step -- kvc_append_layers then kvc_decode_attn on the same layers
+ * (one decode step of Algorithm 1). */
+kvc_status kvc_decode_step(kvc_cache* cache, int32_t layer_begin, int32_t layer_count,
+                           const void* q, const void* k_new, const void* v_new,
+                           float* out, void* stream);
+
+/* kvc_free -- release the cache and all device storage it owns. The caller
+ * must ensure no enqueued work still uses it (synchronize the stream first).
+ * NULL is accepted. */
+kvc_status kvc_free(kvc_cache* cache);
+
+/* ---------------------------------------------------------------------------
+ * Inspection (tests, tools).
+ * ------------------------------------------------------------------------- */
+typedef struct kvc_layer_info {
+  int32_t prefilled;      /* 1 once the layer is compressed                      */
+  int32_t budget;         /* clipped budget (tokens per head)                     */
+  int32_t n_kept;         /* prompt tokens selected (excluding the obs window)   */
+  int32_t packed_tokens;  /* tokens in the packed store (multiple of 32)         */
+  int32_t capacity_tokens;/* packed capacity (tokens per head)                   */
+  int32_t window_tokens;  /* tokens in the bf16 window                           */
+  int32_t appended;       /* tokens appended since prefill                       */
+  int64_t packed_bytes;   /* device bytes of this layer's packed store           */
+} kvc_layer_info;
+
+kvc_status kvc_layer_info_get(const kvc_cache* cache, int32_t layer, kvc_layer_info* out);
+
+/* kvc_export_layer -- unpack one layer into plain device arrays (caller-owned;
+ * any pointer may be NULL to skip that array). T = packed_tokens, W =
+ * window_tokens, K = n_kept, B = batch, H = n_kv_heads, d = head_dim.
+ *   kept    int32  [B][H][K]       selected prompt positions (ascending)
+ *   k_codes uint8  [B][H][T][d]    key codes (token-major)
+ *   k_scale, k_zero  fp16 [B][H][T/32][d]   per-channel key groups
+ *   v_codes uint8  [B][H][T][d]
+ *   v_scale, v_zero  fp16 [B][H][T][d/32]   per-token value groups
+ *   win_k, win_v     bf16 [B][H][W][d]      window, oldest first
+ * The packed layout itself is internal; this is the only way to read it. */
+typedef struct kvc_export {
+  int32_t* kept;
+  uint8_t* k_codes;
+  void* k_scale;
+  void* k_zero;
+  uint8_t* v_codes;
+  void* v_scale;
+  void* v_zero;
+  void* win_k;
+  void* win_v;
+} kvc_export;
+
+kvc_status kvc_export_layer(kvc_cache* cache, int32_t layer, const kvc_export* dst,
+                            void* stream);
+
+/* kvc_scores_layer -- copy the last scored layer's selection scores (fp32,
+ * device [B][H][prompt_len - obs_window]) and pooled scores (same shape);
+ * either pointer may be NULL. Only valid right after kvc_prefill_compress of a
+ * scoring layer (the scratch is reused by the next one). */
+kvc_status kvc_scores_layer(kvc_cache* cache, float* scores, float* pooled, void* stream);
+
+/* kvc_cache_reset -- forget every layer's contents (host-side state only; the
+ * device storage is kept) so the cache can take the next prompt with the same
+ * dims and budgets. Enqueued work must have completed or be stream-ordered
+ * before the next call on the cache. */
+kvc_status kvc_cache_reset(kvc_cache* cache);
+
+/* kvc_launch_count -- number of kernels this library has launched in the
+ * process so far (all caches, all threads). */
+uint64_t kvc_launch_count(void);
+
+/* kvc_status_string -- static description of a status code. */
+const char* kvc_status_string(kvc_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H_ */

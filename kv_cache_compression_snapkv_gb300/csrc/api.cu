@@ -1,0 +1,457 @@
+// api.cu -- the C ABI (include/kvc.h): argument validation, cache creation and
+// sizing, host-side tracking of each layer's packed/window state, and the
+// orchestration of the device kernels. No device arithmetic happens here.
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <new>
+
+#include "kvc_internal.cuh"
+
+using kvc::LayerState;
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+kvc_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return KVC_OK;
+  if (e == cudaErrorMemoryAllocation) return KVC_E_OOM;
+  return KVC_E_CUDA;
+}
+
+// Keeps the caller's current device and switches to the cache's device.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+kvc_status check_dims(const kvc_dims* d) {
+  if (!d) return KVC_E_ARG;
+  if (d->n_layers < 1 || d->n_layers > 256) return KVC_E_SHAPE;
+  if (d->batch < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1) return KVC_E_SHAPE;
+  if (d->n_q_heads % d->n_kv_heads) return KVC_E_SHAPE;
+  const int g = d->n_q_heads / d->n_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return KVC_E_SHAPE;
+  if (d->head_dim != 64 && d->head_dim != 128) return KVC_E_SHAPE;
+  if (d->prompt_len < 1) return KVC_E_SHAPE;
+  if (d->obs_window < 0 || d->obs_window >= d->prompt_len) return KVC_E_SHAPE;
+  if (d->pool_kernel < 1 || d->pool_kernel % 2 == 0) return KVC_E_ARG;
+  if (d->bits != 2 && d->bits != 4) return KVC_E_ARG;
+  if (d->group_size != KVC_GROUP) return KVC_E_ARG;
+  if (d->window_len < KVC_GROUP || d->window_len > 1024 || d->window_len % KVC_GROUP)
+    return KVC_E_SHAPE;
+  if (d->max_new_tokens < 0) return KVC_E_ARG;
+  if (d->obs_window >= d->window_len) return KVC_E_SHAPE;
+  if ((d->alloc == nullptr) != (d->free == nullptr)) return KVC_E_ARG;
+  return KVC_OK;
+}
+
+bool same_dims(const kvc_dims& a, const kvc_dims& b) {
+  return a.n_layers == b.n_layers && a.batch == b.batch && a.n_q_heads == b.n_q_heads &&
+         a.n_kv_heads == b.n_kv_heads && a.head_dim == b.head_dim &&
+         a.prompt_len == b.prompt_len && a.obs_window == b.obs_window &&
+         a.pool_kernel == b.pool_kernel && a.bits == b.bits && a.group_size == b.group_size &&
+         a.window_len == b.window_len && a.max_new_tokens == b.max_new_tokens;
+}
+
+void* dev_alloc(kvc_cache* c, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  void* p = nullptr;
+  if (c->dims.alloc) {
+    p = c->dims.alloc(bytes, nullptr, c->dims.alloc_ctx);
+  } else if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    p = nullptr;
+  }
+  if (p) c->allocations.push_back(p);
+  return p;
+}
+
+void release_all(kvc_cache* c) {
+  for (void* p : c->allocations) {
+    if (c->dims.free) c->dims.free(p, nullptr, c->dims.alloc_ctx);
+    else cudaFree(p);
+  }
+  c->allocations.clear();
+}
+
+int kept_cap(const kvc_dims& d, int budget) {
+  const int ns = d.prompt_len - d.obs_window;
+  return budget < ns ? budget : ns;
+}
+
+kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out) {
+  kvc_status st = check_dims(dims);
+  if (st != KVC_OK) return st;
+  if (!budgets || !out) return KVC_E_ARG;
+  const kvc_dims& d = *dims;
+  const int units = d.batch * d.n_kv_heads;
+  const int g = d.n_q_heads / d.n_kv_heads;
+  const int ns = d.prompt_len - d.obs_window;
+  bool scoring = false;
+  for (int l = 0; l < d.n_layers; ++l) {
+    if (budgets[l] < 0) return KVC_E_ARG;
+    const int nk = kept_cap(d, budgets[l]);
+    if (nk % KVC_GROUP + d.obs_window >= d.window_len) return KVC_E_SHAPE;
+    if (nk < ns) scoring = true;
+  }
+  if (scoring && (d.obs_window < 1 || g * d.obs_window > 256)) return KVC_E_SHAPE;
+
+  kvc_cache* c = new (std::nothrow) kvc_cache();
+  if (!c) return KVC_E_OOM;
+  c->dims = d;
+  c->g = g;
+  c->block_bytes = kvc::block_bytes(d.head_dim, d.bits);
+  if (cudaGetDevice(&c->device) != cudaSuccess) { delete c; return KVC_E_CUDA; }
+  c->L.resize(d.n_layers);
+  size_t packed = 0, part_ctas = 0;
+  for (int l = 0; l < d.n_layers; ++l) {
+    LayerState& ls = c->L[l];
+    ls.budget = kept_cap(d, budgets[l]);
+    ls.cap_groups = ls.budget / KVC_GROUP +
+                    (KVC_GROUP - 1 + d.obs_window + d.max_new_tokens + KVC_GROUP - 1) / KVC_GROUP + 1;
+    ls.packed_off = packed;
+    packed += (size_t)units * ls.cap_groups * c->block_bytes;
+    const int ctas = kvc::packed_ctas(ls.cap_groups) + kvc::window_ctas(d.window_len);
+    part_ctas += (size_t)units * ctas;
+  }
+  c->packed_bytes = packed;
+  c->win_elems = (size_t)d.n_layers * units * d.window_len * d.head_dim;
+  c->dec_part_elems = part_ctas * g * (d.head_dim + 2);
+  c->n_tickets = (size_t)d.n_layers * units;
+
+  c->packed = static_cast<uint8_t*>(dev_alloc(c, packed));
+  c->win_k = static_cast<__nv_bfloat16*>(dev_alloc(c, c->win_elems * 2));
+  c->win_v = static_cast<__nv_bfloat16*>(dev_alloc(c, c->win_elems * 2));
+  c->dec_part = static_cast<float*>(dev_alloc(c, c->dec_part_elems * 4));
+  c->tickets = static_cast<unsigned*>(dev_alloc(c, c->n_tickets * 4));
+  bool ok = c->packed && c->win_k && c->win_v && c->dec_part && c->tickets;
+  if (ok && scoring) {
+    const int M = g * d.obs_window;
+    const int nch = (d.prompt_len + kvc::kScoreChunk - 1) / kvc::kScoreChunk;
+    c->stats_elems = (size_t)units * nch * M;
+    c->rowstat_elems = (size_t)units * M;
+    c->score_elems = (size_t)units * ns;
+    c->stats = static_cast<float2*>(dev_alloc(c, c->stats_elems * 8));
+    c->rowstat = static_cast<float2*>(dev_alloc(c, c->rowstat_elems * 8));
+    c->scores = static_cast<float*>(dev_alloc(c, c->score_elems * 4));
+    c->pooled = static_cast<float*>(dev_alloc(c, c->score_elems * 4));
+    ok = c->stats && c->rowstat && c->scores && c->pooled;
+  }
+  // kept positions are stored for selective layers (keep-all layers are the identity)
+  if (ok) {
+    size_t off = 0;
+    for (int l = 0; l < d.n_layers; ++l) {
+      c->L[l].kept_off = off;
+      if (c->L[l].budget < ns) off += (size_t)units * c->L[l].budget;
+    }
+    c->kept_elems = off;
+    c->kept = static_cast<int32_t*>(dev_alloc(c, off * 4));
+    ok = c->kept != nullptr;
+    for (int l = 0; ok && l < d.n_layers; ++l)
+      if (c->L[l].budget < ns) c->L[l].kept_ptr = c->kept + c->L[l].kept_off;
+  }
+  if (ok) {
+    // the window is zero-initialised: masked slots must hold finite values
+    ok = cudaMemset(c->win_k, 0, c->win_elems * 2) == cudaSuccess &&
+         cudaMemset(c->win_v, 0, c->win_elems * 2) == cudaSuccess &&
+         cudaMemset(c->tickets, 0, c->n_tickets * 4) == cudaSuccess &&
+         cudaDeviceSynchronize() == cudaSuccess;
+  }
+  if (!ok) {
+    cudaGetLastError();
+    release_all(c);
+    delete c;
+    return KVC_E_OOM;
+  }
+  *out = c;
+  return KVC_OK;
+}
+
+kvc_status finish_prefill(kvc_cache* c, int layer, int n_kept, const int32_t* kept,
+                          const void* k, const void* v, cudaStream_t stream) {
+  const auto* K = static_cast<const __nv_bfloat16*>(k);
+  const auto* V = static_cast<const __nv_bfloat16*>(v);
+  cudaError_t e = kvc::launch_gather_quant(c, layer, kept, n_kept, K, V, stream);
+  if (e == cudaSuccess) e = kvc::launch_window_init(c, layer, kept, n_kept, K, V, stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  LayerState& ls = c->L[layer];
+  ls.n_kept = n_kept;
+  ls.n_groups = n_kept / KVC_GROUP;
+  ls.win_start = 0;
+  ls.win_len = n_kept % KVC_GROUP + c->dims.obs_window;
+  ls.appended = 0;
+  ls.prefilled = 1;
+  return KVC_OK;
+}
+
+}  // namespace
+
+void kvc::count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+extern "C" {
+
+uint64_t kvc_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+kvc_status kvc_cache_reset(kvc_cache* c) {
+  if (!c) return KVC_E_ARG;
+  for (LayerState& ls : c->L) {
+    ls.prefilled = 0;
+    ls.n_kept = 0;
+    ls.n_groups = 0;
+    ls.win_start = 0;
+    ls.win_len = 0;
+    ls.appended = 0;
+    if (ls.budget >= c->dims.prompt_len - c->dims.obs_window) ls.scored = 0;
+  }
+  c->last_scored_layer = -1;
+  return KVC_OK;
+}
+
+const char* kvc_status_string(kvc_status s) {
+  switch (s) {
+    case KVC_OK: return "ok";
+    case KVC_E_ARG: return "invalid argument";
+    case KVC_E_SHAPE: return "unsupported or inconsistent dimensions";
+    case KVC_E_OOM: return "device allocation failed";
+    case KVC_E_CUDA: return "CUDA error";
+    case KVC_E_STATE: return "call out of order";
+    case KVC_E_CAPACITY: return "capacity exceeded";
+    case KVC_E_TIMEOUT: return "device-side wait timed out";
+    case KVC_E_DEVICE_CHECK: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+kvc_status kvc_plan_budgets(const kvc_dims* dims, kvc_schedule schedule, int32_t avg_budget,
+                            int32_t pyramid_depth, int32_t* budgets_out) {
+  kvc_status st = check_dims(dims);
+  if (st != KVC_OK) return st;
+  if (!budgets_out) return KVC_E_ARG;
+  const int L = dims->n_layers, G = dims->group_size;
+  const int ns = dims->prompt_len - dims->obs_window;
+  std::vector<long long> units(L);
+  if (schedule == KVC_SCHED_NONE) {
+    for (int l = 0; l < L; ++l) budgets_out[l] = dims->prompt_len;
+  } else {
+    if (avg_budget <= 0 || avg_budget % G) return KVC_E_ARG;
+    const long long xu = avg_budget / G;
+    if (schedule == KVC_SCHED_UNIFORM) {
+      for (int l = 0; l < L; ++l) units[l] = xu;
+    } else if (schedule == KVC_SCHED_PYRAMID) {
+      if (pyramid_depth < 1) return KVC_E_ARG;
+      const long long top = xu / pyramid_depth, bottom = 2 * xu - top;
+      if (L == 1) {
+        units[0] = xu;
+      } else {
+        // r_l = (bottom*(L-1) - (bottom-top)*l) / (L-1): floor, then the leftover
+        // units to the largest remainders (ties to the lower layer)
+        const long long den = L - 1;
+        std::vector<long long> rem(L);
+        long long used = 0;
+        for (int l = 0; l < L; ++l) {
+          const long long num = bottom * den - (bottom - top) * l;
+          units[l] = num / den;
+          rem[l] = num % den;
+          used += units[l];
+        }
+        long long left = (long long)L * xu - used;
+        std::vector<int> order(L);
+        for (int l = 0; l < L; ++l) order[l] = l;
+        std::stable_sort(order.begin(), order.end(),
+                         [&](int a, int b) { return rem[a] > rem[b]; });
+        for (int i = 0; i < left && i < L; ++i) units[order[i]] += 1;
+      }
+    } else {
+      return KVC_E_ARG;
+    }
+    for (int l = 0; l < L; ++l) budgets_out[l] = (int32_t)(units[l] * G);
+  }
+  for (int l = 0; l < L; ++l) budgets_out[l] = std::min<int32_t>(budgets_out[l], ns);
+  return KVC_OK;
+}
+
+kvc_status kvc_cache_create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** cache) {
+  if (!cache) return KVC_E_ARG;
+  *cache = nullptr;
+  return create(dims, budgets, cache);
+}
+
+kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets, int32_t layer,
+                                const void* q_obs, const void* k, const void* v,
+                                kvc_cache** cache, void* stream) {
+  if (!cache || !dims) return KVC_E_ARG;
+  if (*cache == nullptr) {
+    kvc_status st = create(dims, budgets, cache);
+    if (st != KVC_OK) return st;
+  } else if (!same_dims((*cache)->dims, *dims)) {
+    return KVC_E_SHAPE;
+  }
+  kvc_cache* c = *cache;
+  if (layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
+  if (!k || !v) return KVC_E_ARG;
+  LayerState& ls = c->L[layer];
+  if (ls.prefilled) return KVC_E_STATE;
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int ns = c->dims.prompt_len - c->dims.obs_window;
+  const int n_kept = ls.budget;
+  const int32_t* kept = nullptr;
+  if (n_kept < ns) {
+    if (!q_obs) return KVC_E_ARG;
+    int32_t* kp = ls.kept_ptr;
+    cudaError_t e = kvc::launch_score(c, layer, static_cast<const __nv_bfloat16*>(q_obs),
+                                      static_cast<const __nv_bfloat16*>(k), s);
+    if (e == cudaSuccess) e = kvc::launch_pool_topk(c, layer, kp, n_kept, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    kept = kp;
+    ls.scored = 1;
+    c->last_scored_layer = layer;
+  } else {
+    ls.scored = 0;
+  }
+  return finish_prefill(c, layer, n_kept, kept, k, v, s);
+}
+
+kvc_status kvc_prefill_selected(kvc_cache* c, int32_t layer, const int32_t* kept, int32_t n_kept,
+                                const void* k, const void* v, void* stream) {
+  if (!c || !kept || !k || !v) return KVC_E_ARG;
+  if (layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
+  LayerState& ls = c->L[layer];
+  if (ls.prefilled) return KVC_E_STATE;
+  const int ns = c->dims.prompt_len - c->dims.obs_window;
+  if (n_kept < 0 || n_kept > ns) return KVC_E_ARG;
+  if (n_kept > ls.budget) return KVC_E_CAPACITY;
+  if (n_kept % KVC_GROUP + c->dims.obs_window >= c->dims.window_len) return KVC_E_SHAPE;
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int units = c->dims.batch * c->dims.n_kv_heads;
+  ls.scored = 0;
+  if (n_kept > 0) {
+    // keep a copy of the selection (row stride n_kept) for export
+    if (!ls.kept_ptr) {
+      ls.kept_ptr = static_cast<int32_t*>(dev_alloc(c, (size_t)units * n_kept * 4));
+      if (!ls.kept_ptr) return KVC_E_OOM;
+    }
+    cudaError_t e = cudaMemcpyAsync(ls.kept_ptr, kept, (size_t)units * n_kept * 4,
+                                    cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    ls.scored = 1;
+  }
+  return finish_prefill(c, layer, n_kept, ls.kept_ptr, k, v, s);
+}
+
+kvc_status kvc_append_layers(kvc_cache* c, int32_t layer_begin, int32_t layer_count,
+                             const void* k_new, const void* v_new, void* stream) {
+  if (!c || !k_new || !v_new) return KVC_E_ARG;
+  if (layer_count < 1 || layer_begin < 0 || layer_begin + layer_count > c->dims.n_layers)
+    return KVC_E_ARG;
+  for (int l = layer_begin; l < layer_begin + layer_count; ++l) {
+    if (!c->L[l].prefilled) return KVC_E_STATE;
+    if (c->L[l].appended >= c->dims.max_new_tokens) return KVC_E_CAPACITY;
+  }
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  const int R = c->dims.window_len;
+  std::vector<int> flush(layer_count);
+  for (int i = 0; i < layer_count; ++i) flush[i] = (c->L[layer_begin + i].win_len + 1 == R);
+  cudaError_t e = kvc::launch_append(c, layer_begin, layer_count,
+                                     static_cast<const __nv_bfloat16*>(k_new),
+                                     static_cast<const __nv_bfloat16*>(v_new), flush.data(),
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return from_cuda(e);
+  for (int i = 0; i < layer_count; ++i) {
+    LayerState& ls = c->L[layer_begin + i];
+    ls.win_len += 1;
+    ls.appended += 1;
+    if (flush[i]) {
+      ls.n_groups += 1;
+      ls.win_start = (ls.win_start + KVC_GROUP) % R;
+      ls.win_len -= KVC_GROUP;
+    }
+  }
+  return KVC_OK;
+}
+
+kvc_status kvc_append(kvc_cache* c, int32_t layer, const void* k_new, const void* v_new,
+                      void* stream) {
+  return kvc_append_layers(c, layer, 1, k_new, v_new, stream);
+}
+
+kvc_status kvc_decode_attn(kvc_cache* c, int32_t layer_begin, int32_t layer_count, const void* q,
+                           float* out, void* stream) {
+  if (!c || !q || !out) return KVC_E_ARG;
+  if (layer_count < 1 || layer_begin < 0 || layer_begin + layer_count > c->dims.n_layers)
+    return KVC_E_ARG;
+  for (int l = layer_begin; l < layer_begin + layer_count; ++l)
+    if (!c->L[l].prefilled) return KVC_E_STATE;
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  return from_cuda(kvc::launch_decode(c, layer_begin, layer_count,
+                                      static_cast<const __nv_bfloat16*>(q), out,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+kvc_status kvc_decode_step(kvc_cache* c, int32_t layer_begin, int32_t layer_count, const void* q,
+                           const void* k_new, const void* v_new, float* out, void* stream) {
+  kvc_status st = kvc_append_layers(c, layer_begin, layer_count, k_new, v_new, stream);
+  if (st != KVC_OK) return st;
+  return kvc_decode_attn(c, layer_begin, layer_count, q, out, stream);
+}
+
+kvc_status kvc_free(kvc_cache* c) {
+  if (!c) return KVC_OK;
+  DeviceGuard dg(c->device);
+  release_all(c);
+  delete c;
+  return KVC_OK;
+}
+
+kvc_status kvc_layer_info_get(const kvc_cache* c, int32_t layer, kvc_layer_info* out) {
+  if (!c || !out || layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
+  const LayerState& ls = c->L[layer];
+  out->prefilled = ls.prefilled;
+  out->budget = ls.budget;
+  out->n_kept = ls.n_kept;
+  out->packed_tokens = ls.n_groups * KVC_GROUP;
+  out->capacity_tokens = ls.cap_groups * KVC_GROUP;
+  out->window_tokens = ls.win_len;
+  out->appended = ls.appended;
+  out->packed_bytes = (int64_t)c->dims.batch * c->dims.n_kv_heads * ls.cap_groups * c->block_bytes;
+  return KVC_OK;
+}
+
+kvc_status kvc_export_layer(kvc_cache* c, int32_t layer, const kvc_export* dst, void* stream) {
+  if (!c || !dst || layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
+  if (!c->L[layer].prefilled) return KVC_E_STATE;
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  return from_cuda(kvc::launch_export(c, layer, dst, static_cast<cudaStream_t>(stream)));
+}
+
+kvc_status kvc_scores_layer(kvc_cache* c, float* scores, float* pooled, void* stream) {
+  if (!c) return KVC_E_ARG;
+  if (c->last_scored_layer < 0 || !c->scores) return KVC_E_STATE;
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = c->score_elems * 4;
+  cudaError_t e = cudaSuccess;
+  if (scores) e = cudaMemcpyAsync(scores, c->scores, bytes, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && pooled)
+    e = cudaMemcpyAsync(pooled, c->pooled, bytes, cudaMemcpyDeviceToDevice, s);
+  return from_cuda(e);
+}
+
+}  // extern "C"

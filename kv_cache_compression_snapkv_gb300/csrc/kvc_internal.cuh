@@ -1,0 +1,186 @@
+// kvc_internal.cuh -- shared definitions of the compressed-KV-cache library.
+//
+// Storage layout (all of it device memory owned by the cache):
+//
+//   packed store  one 32-token "group block" after another, per (layer, b, kv head):
+//     [K codes  D*4*BITS bytes][V codes  D*4*BITS bytes]
+//     [K scale  D fp16][K zero  D fp16]          per-channel key groups
+//     [V scale  32*(D/32) fp16][V zero  ...]     per-token value groups, [pair][gc][2]
+//   The code words are laid out so that lane l of a warp reading words
+//   (wi/4)*128 + l*4 + wi%4 holds exactly the B-operand fragments of the
+//   m16n8k16 tensor-core products the decode kernel issues (keys: k = channel,
+//   n = token; values: k = token, n = channel), two codes per 16-bit half pair.
+//   Key scales/zeros are stored in the order the A-operand lanes consume them.
+//
+//   window        bf16 ring of R slots per (layer, b, kv head):
+//     keys   [R][D]     channels permuted (kperm) into fragment order
+//     values [R/2][D][2] token pairs interleaved, channels permuted (vperm)
+//
+// Every layout map below is used by the writer (quantize / append), the reader
+// (decode) and the exporter, so they cannot drift apart.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+#include <vector>
+
+#include "kvc.h"
+
+#define KVC_GROUP 32
+#define KVC_MAX_LAUNCH_LAYERS 64
+
+namespace kvc {
+
+// ----------------------------------------------------------------- layout maps
+// Position of key channel c inside a permuted 16-bit row (window keys, key
+// scales/zeros): the 4 values a lane needs per k-step (channels 16ks + 2tid +
+// {0, 1, 8, 9}) are adjacent, and a lane's k-steps are contiguous.
+__host__ __device__ inline int kperm(int c, int D) {
+  int ks = c >> 4, r = c & 15;
+  int tid = (r & 7) >> 1;
+  int e = (r & 1) + 2 * (r >> 3);
+  return (tid * (D >> 4) + ks) * 4 + e;
+}
+// Position of value channel c inside a permuted window value pair-row.
+__host__ __device__ inline int vperm(int c, int D) {
+  return (c & 7) * (D >> 3) + (c >> 3);
+}
+
+// Index (in fp16 units) of the value scale/zero of (token t, channel group gc)
+// inside its section: token pairs interleaved, so (t, t+1) of one gc form a half2.
+__host__ __device__ inline int vsz_index(int t, int gc, int ngc) {
+  return ((t >> 1) * ngc + gc) * 2 + (t & 1);
+}
+
+// Bytes of one 32-token group block.
+__host__ __device__ inline int block_bytes(int D, int bits) { return 8 * D * (bits + 1); }
+__host__ __device__ inline int code_bytes(int D, int bits) { return 4 * D * bits; }
+
+struct CodePos {
+  int word;   // 32-bit word index inside the K-code (or V-code) section
+  int bit;    // bit offset of the code inside the word
+};
+
+// Words of one section a lane owns (D*BITS/32) and pairs per word (16/BITS).
+__host__ __device__ inline int words_per_lane(int D, int bits) { return D * bits / 32; }
+
+__host__ __device__ inline CodePos word_pos(int lane, int pi, int bits) {
+  int ppw = 16 / bits;
+  int wi = pi / ppw, p = pi % ppw;
+  CodePos cp;
+  cp.word = (wi >> 2) * 128 + lane * 4 + (wi & 3);
+  cp.bit = bits * p;
+  return cp;
+}
+
+// Key code of (token t in the group, channel c).
+__host__ __device__ inline CodePos kcode_pos(int t, int c, int D, int bits) {
+  int nt = t >> 3, gid = t & 7;
+  int ks = c >> 4, r = c & 15;
+  int tid = (r & 7) >> 1, odd = r & 1, half = r >> 3;
+  int lane = gid * 4 + tid;
+  int pi = (nt * (D >> 4) + ks) * 2 + half;
+  CodePos cp = word_pos(lane, pi, bits);
+  cp.bit += odd ? 16 : 0;
+  return cp;
+}
+
+// Value code of (token t in the group, channel c).
+__host__ __device__ inline CodePos vcode_pos(int t, int c, int D, int bits) {
+  int ks = t >> 4, r = t & 15;
+  int tid = (r & 7) >> 1, odd = r & 1, half = r >> 3;
+  int nt = c >> 3, gid = c & 7;
+  int lane = gid * 4 + tid;
+  int pi = (ks * (D >> 3) + nt) * 2 + half;
+  CodePos cp = word_pos(lane, pi, bits);
+  cp.bit += odd ? 16 : 0;
+  return cp;
+}
+
+// Section offsets inside a block (bytes).
+__host__ __device__ inline int off_kcodes(int, int) { return 0; }
+__host__ __device__ inline int off_vcodes(int D, int bits) { return code_bytes(D, bits); }
+__host__ __device__ inline int off_kscale(int D, int bits) { return 2 * code_bytes(D, bits); }
+__host__ __device__ inline int off_kzero(int D, int bits) { return 2 * code_bytes(D, bits) + 2 * D; }
+__host__ __device__ inline int off_vscale(int D, int bits) { return 2 * code_bytes(D, bits) + 4 * D; }
+__host__ __device__ inline int off_vzero(int D, int bits) { return 2 * code_bytes(D, bits) + 6 * D; }
+
+// ------------------------------------------------------------------ cache state
+struct LayerState {
+  int prefilled = 0;
+  int budget = 0;        // clipped budget (tokens per head)
+  int n_kept = 0;        // selected prompt tokens per head
+  int scored = 0;        // 1 if the selection is stored in kept_ptr (else identity)
+  int32_t* kept_ptr = nullptr;  // stored selection [units][n_kept]
+  int cap_groups = 0;    // packed capacity per (b, h) in groups
+  int n_groups = 0;      // packed groups per (b, h)
+  int win_start = 0;     // ring start slot
+  int win_len = 0;       // tokens in the window
+  int appended = 0;
+  size_t packed_off = 0; // byte offset of the layer inside the packed store
+  size_t kept_off = 0;   // element offset of the layer inside kept[]
+};
+
+}  // namespace kvc
+
+struct kvc_cache {
+  kvc_dims dims{};
+  int device = 0;
+  int g = 1;                    // GQA group
+  int block_bytes = 0;
+  std::vector<kvc::LayerState> L;
+  // storage
+  uint8_t* packed = nullptr;  size_t packed_bytes = 0;
+  __nv_bfloat16* win_k = nullptr;
+  __nv_bfloat16* win_v = nullptr; size_t win_elems = 0;
+  int32_t* kept = nullptr;    size_t kept_elems = 0;
+  // scratch
+  float2* stats = nullptr;    size_t stats_elems = 0;  // scoring partial row stats
+  float2* rowstat = nullptr;  size_t rowstat_elems = 0;
+  float* scores = nullptr;
+  float* pooled = nullptr;    size_t score_elems = 0;
+  float* dec_part = nullptr;  size_t dec_part_elems = 0;
+  unsigned* tickets = nullptr; size_t n_tickets = 0;
+  int max_ctas_per_unit = 0;
+  int last_scored_layer = -1;
+  std::vector<void*> allocations;
+};
+
+namespace kvc {
+
+// Process-wide count of kernels launched by this library (kvc_launch_count).
+void count_launches(int n);
+
+// --------------------------------------------------------------- launch helpers
+// (defined in the .cu files; all enqueue on `stream` and return a CUDA error)
+cudaError_t launch_score(const kvc_cache* c, int layer, const __nv_bfloat16* q_obs,
+                         const __nv_bfloat16* k, cudaStream_t stream);
+cudaError_t launch_pool_topk(const kvc_cache* c, int layer, int32_t* kept_out, int k_sel,
+                             cudaStream_t stream);
+cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* kept, int n_kept,
+                                const __nv_bfloat16* k, const __nv_bfloat16* v,
+                                cudaStream_t stream);
+cudaError_t launch_window_init(const kvc_cache* c, int layer, const int32_t* kept, int n_kept,
+                               const __nv_bfloat16* k, const __nv_bfloat16* v,
+                               cudaStream_t stream);
+cudaError_t launch_append(const kvc_cache* c, int layer_begin, int layer_count,
+                          const __nv_bfloat16* k_new, const __nv_bfloat16* v_new,
+                          const int* flush_flags, cudaStream_t stream);
+cudaError_t launch_decode(const kvc_cache* c, int layer_begin, int layer_count,
+                          const __nv_bfloat16* q, float* out, cudaStream_t stream);
+cudaError_t launch_export(const kvc_cache* c, int layer, const kvc_export* dst,
+                          cudaStream_t stream);
+
+// Decode work decomposition shared by the host (sizing) and the kernel.
+constexpr int kDecWarps = 4;
+constexpr int kGroupsPerCta = 64;      // packed groups per decode CTA (16 per warp)
+constexpr int kWinSlotsPerCta = 128;   // window slots per decode CTA (32 per warp)
+inline int packed_ctas(int n_groups) { return (n_groups + kGroupsPerCta - 1) / kGroupsPerCta; }
+inline int window_ctas(int win_len) { return (win_len + kWinSlotsPerCta - 1) / kWinSlotsPerCta; }
+
+// Scoring decomposition.
+constexpr int kScoreChunk = 128;       // keys per scoring CTA
+
+}  // namespace kvc

@@ -1,0 +1,54 @@
+"""CUDA path vs oracle on workloads the oracle finishes in seconds (several key
+tiles, ragged tails, every GQA group size, 2- and 4-bit, flushes during decode)."""
+import pytest
+
+import synth
+from _parity import run_small
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # the toy workload at full size: MHA, d=64, window == group (flush at step 16)
+    "toy": (synth.workload(1), 20, "score"),
+    # GQA g=4, d=128, pyramid over 3 layers (top layer budget 0), ragged n
+    "gqa4_pyramid": (synth.small_spec(2, n_layers=3, batch=2, n_q_heads=8, n_kv_heads=2,
+                                      prompt_len=1000, obs_window=32, avg_budget=96,
+                                      window_len=64), 40, "score"),
+    # quantize-only, MHA, 4-bit, prompt not a multiple of the group
+    "quant_only_4bit": (synth.small_spec(3, n_layers=2, batch=2, n_q_heads=4, n_kv_heads=4,
+                                         prompt_len=300, window_len=64), 60, "score"),
+    # g=8 with d=64, uniform budget
+    "gqa8_d64": (synth.small_spec(4, n_layers=1, batch=1, n_q_heads=16, n_kv_heads=2,
+                                  head_dim=64, prompt_len=700, obs_window=16,
+                                  avg_budget=160, window_len=64), 70, "score"),
+    # g=2, 4-bit with eviction
+    "gqa2_4bit": (synth.small_spec(2, n_layers=2, batch=1, n_q_heads=4, n_kv_heads=2,
+                                   prompt_len=777, obs_window=16, avg_budget=128,
+                                   schedule="uniform", bits=4, window_len=96), 50, "score"),
+    # long-context flavour: M = 256 scoring rows, needles, window 128
+    "long_needles": (synth.small_spec(5, n_layers=2, batch=1, n_q_heads=8, n_kv_heads=2,
+                                      prompt_len=4096, obs_window=64, avg_budget=256,
+                                      window_len=128), 130, "score"),
+    # the GPU given the oracle's selection (storage + decode parity alone)
+    "oracle_selection": (synth.small_spec(2, n_layers=2, batch=2, n_q_heads=8, n_kv_heads=2,
+                                          prompt_len=1500, obs_window=32, avg_budget=160,
+                                          window_len=64), 35, "oracle"),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_parity(name):
+    spec, steps, selection = CASES[name]
+    rep = run_small(spec, steps, selection=selection)
+    print(f"{name}: excused={rep.excused} kept_sets={rep.kept_compared} "
+          f"codes={rep.codes_compared} decode_err={rep.decode_err:.2e} "
+          f"score_err={rep.score_err:.2e}")
+    assert rep.decode_checked > 0
+
+
+def test_per_layer_calls_match():
+    """Single-layer append/decode calls give the same results as one multi-layer launch."""
+    spec = synth.small_spec(2, n_layers=2, batch=1, n_q_heads=4, n_kv_heads=1,
+                            prompt_len=600, obs_window=16, avg_budget=64, window_len=32)
+    rep = run_small(spec, 12, selection="score", multi_layer_decode=False)
+    assert rep.decode_err <= 2e-3
