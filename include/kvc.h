@@ -142,7 +142,8 @@ kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets,
  *   positions supplied by the caller instead of scored (any selection policy:
  *   e.g. attention sinks + recent tokens, StreamingLLM-style).
  *   kept: device int32 [batch][n_kv_heads][n_kept], strictly ascending, each in
- *   [0, prompt_len - obs_window); n_kept <= the layer's budget. The cache must
+ *   [0, prompt_len - obs_window) (may be NULL when n_kept == 0: only the
+ *   observation window is kept); n_kept <= the layer's budget. The cache must
  *   exist (created by kvc_prefill_compress or kvc_cache_create).
  *   Errors: as kvc_prefill_compress; KVC_E_CAPACITY if n_kept > budget. Index
  *   order/range is the caller's contract (not checked on the device).

@@ -325,7 +325,7 @@ kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets, in
 
 kvc_status kvc_prefill_selected(kvc_cache* c, int32_t layer, const int32_t* kept, int32_t n_kept,
                                 const void* k, const void* v, void* stream) {
-  if (!c || !kept || !k || !v) return KVC_E_ARG;
+  if (!c || !k || !v || (!kept && n_kept > 0)) return KVC_E_ARG;
   if (layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
   LayerState& ls = c->L[layer];
   if (ls.prefilled) return KVC_E_STATE;
