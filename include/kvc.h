@@ -246,6 +246,33 @@ kvc_status kvc_export_layer(kvc_cache* cache, int32_t layer, const kvc_export* d
  * scoring layer (the scratch is reused by the next one). */
 kvc_status kvc_scores_layer(kvc_cache* cache, float* scores, float* pooled, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * kvc_select_noalloc -- the prefill selection of one layer (observation-window
+ *   scores, max-pool, per-head top-k; the same kernels and results as
+ *   kvc_prefill_compress) for callers that cannot allocate device memory, e.g.
+ *   runtimes that carve all GPU memory into their own arena, or latency-critical
+ *   loops where a cudaMalloc is not allowed. The pages have no counterpart: this
+ *   is an interface variant, not a step of the method.
+ *   Allocates nothing: intermediates live in one static device array of
+ *   KVC_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading this library holds
+ *   until exit. All calls share it (it keeps the last call's contents; every
+ *   value a call reads is written by that call first), so calls that overlap on
+ *   the GPU race: serialize them. The first call on a device looks up the
+ *   array's device address; make it before any stream capture.
+ *   Scratch needed: B*H*ceil(n/128)*g*alpha*8 + B*H*g*alpha*4 + B*H*(n-alpha)*4
+ *   bytes (+ the same again for scores when `scores` is NULL), each part
+ *   rounded up to 256 bytes.
+ *   q_obs: device bf16 [B][Hq][alpha][d]; k: device bf16 [B][H][n][d];
+ *   kept:  device int32 [B][H][min(budget, n - alpha)] (written, ascending);
+ *   scores: optional device fp32 [B][H][n - alpha] (written when not NULL).
+ *   Only the fields n_layers..pool_kernel of dims are read.
+ *   Errors: KVC_E_ARG, KVC_E_SHAPE, KVC_E_CAPACITY (the sizes need more than
+ *   the static scratch; nothing is enqueued), KVC_E_CUDA.
+ * ------------------------------------------------------------------------- */
+#define KVC_NOALLOC_SCRATCH_BYTES (32u << 20)
+kvc_status kvc_select_noalloc(const kvc_dims* dims, int32_t budget, const void* q_obs,
+                              const void* k, int32_t* kept, float* scores, void* stream);
+
 /* kvc_cache_reset -- forget every layer's contents (host-side state only; the
  * device storage is kept) so the cache can take the next prompt with the same
  * dims and budgets. Enqueued work must have completed or be stream-ordered

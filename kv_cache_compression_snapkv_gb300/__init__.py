@@ -73,6 +73,7 @@ _SIGS = {
     "kvc_export_layer": [_P, _I, ctypes.POINTER(KvcExport), _P],
     "kvc_scores_layer": [_P, _P, _P, _P],
     "kvc_cache_reset": [_P],
+    "kvc_select_noalloc": [ctypes.POINTER(KvcDims), _I, _P, _P, _P, _P, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -240,6 +241,13 @@ def kvc_scores_layer(cache: Cache, scores=None, pooled=None, stream=None):
 
 def kvc_cache_reset(cache: Cache):
     _check(_lib.kvc_cache_reset(cache.handle), "kvc_cache_reset")
+
+
+def kvc_select_noalloc(dims: KvcDims, budget: int, q_obs, k, kept, scores=None, stream=None):
+    """Selection of one layer into `kept` (and `scores`) without any device
+    allocation; intermediates use the library's static 32 MiB device scratch."""
+    _check(_lib.kvc_select_noalloc(ctypes.byref(dims), budget, _ptr(q_obs), _ptr(k), _ptr(kept),
+                                   _ptr(scores), _stream(stream)), "kvc_select_noalloc")
 
 
 def kvc_launch_count() -> int:

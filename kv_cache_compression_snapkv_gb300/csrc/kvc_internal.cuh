@@ -172,6 +172,12 @@ cudaError_t launch_decode(const kvc_cache* c, int layer_begin, int layer_count,
                           const __nv_bfloat16* q, float* out, cudaStream_t stream);
 cudaError_t launch_export(const kvc_cache* c, int layer, const kvc_export* dst,
                           cudaStream_t stream);
+// Selection launches with explicit scratch (allocation-free entry point).
+cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
+                              const __nv_bfloat16* k, float2* stats, float* rowbias,
+                              float* scores, cudaStream_t stream);
+cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float* pooled,
+                                  int32_t* kept_out, int k_sel, cudaStream_t stream);
 
 // Decode work decomposition shared by the host (sizing) and the kernel.
 constexpr int kDecWarps = 4;

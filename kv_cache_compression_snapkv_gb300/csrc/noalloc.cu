@@ -1,0 +1,99 @@
+// noalloc.cu -- selection (scores -> max-pool -> per-head top-k) for callers that
+// cannot allocate device memory.
+//
+// Some callers own every byte of device memory themselves: serving runtimes that
+// carve all GPU memory into their own arena up front and keep exact accounting,
+// or latency-critical loops where a cudaMalloc (which may synchronize the device
+// and can fail under fragmentation) is not acceptable. kvc_select_noalloc gives
+// them the prefill selection without any allocation: the caller passes inputs
+// and outputs, and the intermediate buffers (per-chunk row statistics, per-row
+// normalisers, scores, pooled scores) live in one file-scope static device array
+// of fixed size, KVC_NOALLOC_SCRATCH_BYTES.
+//
+// Properties of that array:
+//   * every GPU that loads this library holds it until the process exits;
+//   * all calls share it and it keeps the previous call's contents; every
+//     element a call reads is first written by that same call, so nothing has
+//     to be cleared;
+//   * calls whose work overlaps on the GPU (different streams, or devices
+//     sharing a context) race on it: serialize them.
+// In host code the array's name is only a host-side stand-in, not a device
+// address, so its device address is looked up once per device
+// (cudaGetSymbolAddress, with that device current) on the first call made on
+// that device; make that first call before any stream capture.
+#include <mutex>
+
+#include "kvc_internal.cuh"
+
+namespace {
+
+constexpr size_t kScratchBytes = KVC_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_select_scratch[kScratchBytes];
+
+std::mutex g_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+kvc_status scratch_for_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_E_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return KVC_E_CUDA;
+    }
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return KVC_OK;
+}
+
+}  // namespace
+
+extern "C" kvc_status kvc_select_noalloc(const kvc_dims* dims, int32_t budget, const void* q_obs,
+                                         const void* k, int32_t* kept, float* scores,
+                                         void* stream) {
+  if (!dims || !q_obs || !k || !kept || budget < 0) return KVC_E_ARG;
+  const kvc_dims& d = *dims;
+  if (d.batch < 1 || d.n_q_heads < 1 || d.n_kv_heads < 1 || d.n_q_heads % d.n_kv_heads)
+    return KVC_E_SHAPE;
+  const int g = d.n_q_heads / d.n_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return KVC_E_SHAPE;
+  if (d.head_dim != 64 && d.head_dim != 128) return KVC_E_SHAPE;
+  if (d.prompt_len < 2 || d.obs_window < 1 || d.obs_window >= d.prompt_len) return KVC_E_SHAPE;
+  if (g * d.obs_window > 256) return KVC_E_SHAPE;
+  if (d.pool_kernel < 1 || d.pool_kernel % 2 == 0) return KVC_E_ARG;
+
+  const size_t units = (size_t)d.batch * d.n_kv_heads;
+  const size_t M = (size_t)g * d.obs_window;
+  const size_t ns = (size_t)d.prompt_len - d.obs_window;
+  const size_t nch = ((size_t)d.prompt_len + kvc::kScoreChunk - 1) / kvc::kScoreChunk;
+  const size_t stats_b = align256(units * nch * M * sizeof(float2));
+  const size_t bias_b = align256(units * M * sizeof(float));
+  const size_t score_b = align256(units * ns * sizeof(float));
+  const size_t need = stats_b + bias_b + (scores ? 0 : score_b) + score_b;
+  if (need > kScratchBytes) return KVC_E_CAPACITY;   // larger than the static scratch
+
+  void* base = nullptr;
+  kvc_status st = scratch_for_current_device(&base);
+  if (st != KVC_OK) return st;
+  unsigned char* p = static_cast<unsigned char*>(base);
+  float2* stats = reinterpret_cast<float2*>(p);
+  float* rowbias = reinterpret_cast<float*>(p + stats_b);
+  float* pooled = reinterpret_cast<float*>(p + stats_b + bias_b);
+  float* sc = scores ? scores : reinterpret_cast<float*>(p + stats_b + bias_b + score_b);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int k_sel = (size_t)budget < ns ? budget : (int)ns;
+  cudaError_t e = kvc::launch_score_into(d, static_cast<const __nv_bfloat16*>(q_obs),
+                                         static_cast<const __nv_bfloat16*>(k), stats, rowbias,
+                                         sc, s);
+  if (e == cudaSuccess) e = kvc::launch_pool_topk_into(d, sc, pooled, kept, k_sel, s);
+  if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? KVC_E_OOM : KVC_E_CUDA;
+  return KVC_OK;
+}

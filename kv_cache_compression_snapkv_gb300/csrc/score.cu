@@ -247,4 +247,50 @@ cudaError_t launch_score(const kvc_cache* c, int layer, const __nv_bfloat16* q_o
   return cudaGetLastError();
 }
 
+// The same three scoring launches with the scratch buffers given explicitly
+// (used by the allocation-free selection entry point).
+cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
+                              const __nv_bfloat16* k, float2* stats, float* rowbias,
+                              float* scores, cudaStream_t stream) {
+  const int units = d.batch * d.n_kv_heads;
+  const int n = d.prompt_len, alpha = d.obs_window;
+  const int M = (d.n_q_heads / d.n_kv_heads) * alpha;
+  const int warps = (M + 15) / 16;
+  const int nch1 = (n + kChunk - 1) / kChunk;
+  const int nch2 = (n - alpha + kChunk - 1) / kChunk;
+  const float sl2 = 1.4426950408889634f / sqrtf((float)d.head_dim);
+  cudaError_t e;
+  if (d.head_dim == 128) {
+    size_t sm = sizeof(ScoreSmem<128>);
+    if ((e = cudaFuncSetAttribute(score_stats_kernel<128>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)))
+      return e;
+    if ((e = cudaFuncSetAttribute(score_cols_kernel<128>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)))
+      return e;
+    score_stats_kernel<128><<<dim3(nch1, units), warps * 32, sm, stream>>>(q_obs, k, n, alpha, M,
+                                                                          sl2, stats);
+    score_combine_kernel<<<units, 256, 0, stream>>>(stats, nch1, M, rowbias);
+    score_cols_kernel<128><<<dim3(nch2, units), warps * 32, sm, stream>>>(q_obs, k, n, alpha, M,
+                                                                         sl2, rowbias, scores);
+  } else if (d.head_dim == 64) {
+    size_t sm = sizeof(ScoreSmem<64>);
+    if ((e = cudaFuncSetAttribute(score_stats_kernel<64>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)))
+      return e;
+    if ((e = cudaFuncSetAttribute(score_cols_kernel<64>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)))
+      return e;
+    score_stats_kernel<64><<<dim3(nch1, units), warps * 32, sm, stream>>>(q_obs, k, n, alpha, M,
+                                                                         sl2, stats);
+    score_combine_kernel<<<units, 256, 0, stream>>>(stats, nch1, M, rowbias);
+    score_cols_kernel<64><<<dim3(nch2, units), warps * 32, sm, stream>>>(q_obs, k, n, alpha, M,
+                                                                        sl2, rowbias, scores);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  count_launches(3);
+  return cudaGetLastError();
+}
+
 }  // namespace kvc

@@ -161,4 +161,16 @@ cudaError_t launch_pool_topk(const kvc_cache* c, int layer, int32_t* kept_out, i
   return cudaGetLastError();
 }
 
+// The same launch with the score and pooled buffers given explicitly (used by
+// the allocation-free selection entry point).
+cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float* pooled,
+                                  int32_t* kept_out, int k_sel, cudaStream_t stream) {
+  const int units = d.batch * d.n_kv_heads;
+  const int ns = d.prompt_len - d.obs_window;
+  pool_topk_kernel<<<units, kTopkThreads, 0, stream>>>(scores, pooled, ns, d.pool_kernel, k_sel,
+                                                        kept_out);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace kvc
