@@ -38,6 +38,8 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--decode-steps", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="use only the first N layers (small cases for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -233,9 +235,14 @@ def run_gpu(args):
 
     spec = synth.workload(args.workload)
     S = args.decode_steps or spec.steps
+    full_dims = K.dims_from_spec(spec, max_new_tokens=S)
+    budgets = K.kvc_plan_budgets(full_dims, spec.schedule, spec.avg_budget, spec.pyramid_depth)
+    if args.layers:     # the first N layers of the full model (with their budgets)
+        import dataclasses
+        spec = dataclasses.replace(spec, n_layers=min(args.layers, spec.n_layers))
+        budgets = budgets[:spec.n_layers]
     L, B, Hq, Hk, D = spec.n_layers, spec.batch, spec.n_q_heads, spec.n_kv_heads, spec.head_dim
     dims = K.dims_from_spec(spec, max_new_tokens=S)
-    budgets = K.kvc_plan_budgets(dims, spec.schedule, spec.avg_budget, spec.pyramid_depth)
     dev = torch.device("cuda", local)
 
     # ---- inputs resident in HBM
@@ -266,9 +273,8 @@ def run_gpu(args):
             flush.zero_()
             e0, e1, e2 = dev_ev[t]
             e0.record(stream)
-            K.kvc_append_layers(cache, 0, L, kns[t], vns[t])
             e1.record(stream)
-            K.kvc_decode_attn(cache, 0, L, qs[t], out)
+            K.kvc_decode_step(cache, 0, L, qs[t], kns[t], vns[t], out)
             e2.record(stream)
             if record_bytes:
                 tot = 0
@@ -276,7 +282,7 @@ def run_gpu(args):
                     info = K.kvc_layer_info_get(cache, l)
                     tot += B * Hk * (info["packed_tokens"] // 32 * block_bytes
                                      + info["window_tokens"] * D * 4)
-                tot += L * B * Hq * D * (2 + 4)
+                tot += L * B * Hq * D * (2 + 4) + L * B * Hk * D * 2 * 2
                 dec_bytes.append(tot)
 
     def collect():
@@ -340,7 +346,8 @@ def run_gpu(args):
     comp_frac = t_roof / (comp_ms / 1e3)
 
     traffic = profiled_traffic("decode.cu")
-    roofline = {"kernel": "decode_kernel (split-K decode attention, all layers per launch)",
+    roofline = {"kernel": "decode_kernel (fused append + split-K decode attention, all layers "
+                          "per launch)",
                 "bound": "hbm", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
                 "frac": dec_gbs / hbm, "peak_source": peak_kind + " (burst copy)",
                 "bytes_per_launch": mean_bytes,
@@ -354,12 +361,12 @@ def run_gpu(args):
         "data": "synthetic",
         "config": {"workload": workload_desc(spec, S),
                    "l2": "flushed (256 MiB) before every decode step; prefill inputs exceed L2",
-                   "decode_launch": f"one append + one attention launch per token for all {L} layers",
+                   "decode_launch": (f"one fused launch per token (append + group flush + "
+                                     f"split-K attention) for all {L} layers"),
                    "parallelism": f"replicas x{world}"},
         "decode_tokens_per_s": value,
         "cache_gbs": dec_gbs, "cache_frac_of_hbm": dec_gbs / hbm,
         "decode_attn_us_per_launch": att_ms * 1e3,
-        "append_us_per_launch": statistics.mean([x for a in apps for x in a]) * 1e3,
         "compress_ms_per_layer": comp_ms / L,
         "compress_roofline": {"bytes": comp_bytes, "flops": comp_flops, "t_roof_ms": t_roof * 1e3,
                               "frac": comp_frac},

@@ -188,11 +188,19 @@ kvc_status kvc_append_layers(kvc_cache* cache, int32_t layer_begin, int32_t laye
 kvc_status kvc_decode_attn(kvc_cache* cache, int32_t layer_begin, int32_t layer_count,
                            const void* q, float* out, void* stream);
 
-/* kvc_decode_step -- kvc_append_layers then kvc_decode_attn on the same layers
- * (one decode step of Algorithm 1). */
+/* kvc_decode_step -- one decode step of Algorithm 1 on layers [layer_begin,
+ * +layer_count) in ONE launch: append k_new/v_new (as kvc_append_layers, with
+ * the group flush when the window reaches R) and attend q (as kvc_decode_attn);
+ * the results equal those two calls made in sequence. Shapes as in those calls. */
 kvc_status kvc_decode_step(kvc_cache* cache, int32_t layer_begin, int32_t layer_count,
                            const void* q, const void* k_new, const void* v_new,
                            float* out, void* stream);
+
+/* kvc_check_device -- synchronize `stream` and report device-side failures
+ * recorded since the last check: KVC_E_TIMEOUT if a bounded wait inside a
+ * kernel gave up (that kernel then skipped the affected work), KVC_OK otherwise.
+ * The error word is cleared. */
+kvc_status kvc_check_device(kvc_cache* cache, void* stream);
 
 /* kvc_free -- release the cache and all device storage it owns. The caller
  * must ensure no enqueued work still uses it (synchronize the stream first).

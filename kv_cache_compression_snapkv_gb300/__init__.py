@@ -74,6 +74,7 @@ _SIGS = {
     "kvc_scores_layer": [_P, _P, _P, _P],
     "kvc_cache_reset": [_P],
     "kvc_select_noalloc": [ctypes.POINTER(KvcDims), _I, _P, _P, _P, _P, _P],
+    "kvc_check_device": [_P, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -250,6 +251,11 @@ def kvc_select_noalloc(dims: KvcDims, budget: int, q_obs, k, kept, scores=None, 
                                    _ptr(scores), _stream(stream)), "kvc_select_noalloc")
 
 
+def kvc_check_device(cache: Cache, stream=None):
+    """Synchronize and raise KvcError(KVC_E_TIMEOUT) if a bounded device wait gave up."""
+    _check(_lib.kvc_check_device(cache.handle, _stream(stream)), "kvc_check_device")
+
+
 def kvc_launch_count() -> int:
     return int(_lib.kvc_launch_count())
 
@@ -263,5 +269,5 @@ __all__ = ["KvcDims", "KvcError", "Cache", "make_dims", "dims_from_spec", "kvc_p
            "kvc_cache_create", "kvc_prefill_compress", "kvc_prefill_selected", "kvc_append",
            "kvc_append_layers", "kvc_decode_attn", "kvc_decode_step", "kvc_free",
            "kvc_layer_info_get", "kvc_export_layer", "kvc_scores_layer", "kvc_cache_reset",
-           "kvc_launch_count", "LIB_PATH",
+           "kvc_launch_count", "kvc_check_device", "kvc_select_noalloc", "LIB_PATH",
            "exported_symbols"]

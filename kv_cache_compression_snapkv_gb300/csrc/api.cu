@@ -134,7 +134,8 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
   c->win_v = static_cast<__nv_bfloat16*>(dev_alloc(c, c->win_elems * 2));
   c->dec_part = static_cast<float*>(dev_alloc(c, c->dec_part_elems * 4));
   c->tickets = static_cast<unsigned*>(dev_alloc(c, c->n_tickets * 4));
-  bool ok = c->packed && c->win_k && c->win_v && c->dec_part && c->tickets;
+  c->err = static_cast<unsigned*>(dev_alloc(c, 16));
+  bool ok = c->packed && c->win_k && c->win_v && c->dec_part && c->tickets && c->err;
   if (ok && scoring) {
     const int M = g * d.obs_window;
     const int nch = (d.prompt_len + kvc::kScoreChunk - 1) / kvc::kScoreChunk;
@@ -165,6 +166,7 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
     ok = cudaMemset(c->win_k, 0, c->win_elems * 2) == cudaSuccess &&
          cudaMemset(c->win_v, 0, c->win_elems * 2) == cudaSuccess &&
          cudaMemset(c->tickets, 0, c->n_tickets * 4) == cudaSuccess &&
+         cudaMemset(c->err, 0, 16) == cudaSuccess &&
          cudaDeviceSynchronize() == cudaSuccess;
   }
   if (!ok) {
@@ -181,8 +183,8 @@ kvc_status finish_prefill(kvc_cache* c, int layer, int n_kept, const int32_t* ke
                           const void* k, const void* v, cudaStream_t stream) {
   const auto* K = static_cast<const __nv_bfloat16*>(k);
   const auto* V = static_cast<const __nv_bfloat16*>(v);
+  // one launch: whole groups into the packed store plus the initial window
   cudaError_t e = kvc::launch_gather_quant(c, layer, kept, n_kept, K, V, stream);
-  if (e == cudaSuccess) e = kvc::launch_window_init(c, layer, kept, n_kept, K, V, stream);
   if (e != cudaSuccess) return from_cuda(e);
   LayerState& ls = c->L[layer];
   ls.n_kept = n_kept;
@@ -405,9 +407,50 @@ kvc_status kvc_decode_attn(kvc_cache* c, int32_t layer_begin, int32_t layer_coun
 
 kvc_status kvc_decode_step(kvc_cache* c, int32_t layer_begin, int32_t layer_count, const void* q,
                            const void* k_new, const void* v_new, float* out, void* stream) {
-  kvc_status st = kvc_append_layers(c, layer_begin, layer_count, k_new, v_new, stream);
-  if (st != KVC_OK) return st;
-  return kvc_decode_attn(c, layer_begin, layer_count, q, out, stream);
+  if (!c || !q || !out || !k_new || !v_new) return KVC_E_ARG;
+  if (layer_count < 1 || layer_begin < 0 || layer_begin + layer_count > c->dims.n_layers)
+    return KVC_E_ARG;
+  for (int l = layer_begin; l < layer_begin + layer_count; ++l) {
+    if (!c->L[l].prefilled) return KVC_E_STATE;
+    if (c->L[l].appended >= c->dims.max_new_tokens) return KVC_E_CAPACITY;
+  }
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  const int R = c->dims.window_len;
+  std::vector<int> flush(layer_count);
+  for (int i = 0; i < layer_count; ++i) flush[i] = (c->L[layer_begin + i].win_len + 1 == R);
+  // one launch: append (+ flush of the oldest group) and attention for every layer
+  cudaError_t e = kvc::launch_decode_step(c, layer_begin, layer_count,
+                                          static_cast<const __nv_bfloat16*>(q),
+                                          static_cast<const __nv_bfloat16*>(k_new),
+                                          static_cast<const __nv_bfloat16*>(v_new), flush.data(),
+                                          out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return from_cuda(e);
+  for (int i = 0; i < layer_count; ++i) {
+    LayerState& ls = c->L[layer_begin + i];
+    ls.win_len += 1;
+    ls.appended += 1;
+    if (flush[i]) {
+      ls.n_groups += 1;
+      ls.win_start = (ls.win_start + KVC_GROUP) % R;
+      ls.win_len -= KVC_GROUP;
+    }
+  }
+  return KVC_OK;
+}
+
+kvc_status kvc_check_device(kvc_cache* c, void* stream) {
+  if (!c) return KVC_E_ARG;
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KVC_E_CUDA;
+  if (cudaMemcpy(&word, c->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KVC_E_CUDA;
+  if (word == 0) return KVC_OK;
+  if (cudaMemset(c->err, 0, sizeof(word)) != cudaSuccess) return KVC_E_CUDA;
+  return KVC_E_TIMEOUT;
 }
 
 kvc_status kvc_free(kvc_cache* c) {

@@ -37,26 +37,26 @@ namespace kvc {
 // Position of key channel c inside a permuted 16-bit row (window keys, key
 // scales/zeros): the 4 values a lane needs per k-step (channels 16ks + 2tid +
 // {0, 1, 8, 9}) are adjacent, and a lane's k-steps are contiguous.
-__host__ __device__ inline int kperm(int c, int D) {
+__host__ __device__ constexpr int kperm(int c, int D) {
   int ks = c >> 4, r = c & 15;
   int tid = (r & 7) >> 1;
   int e = (r & 1) + 2 * (r >> 3);
   return (tid * (D >> 4) + ks) * 4 + e;
 }
 // Position of value channel c inside a permuted window value pair-row.
-__host__ __device__ inline int vperm(int c, int D) {
+__host__ __device__ constexpr int vperm(int c, int D) {
   return (c & 7) * (D >> 3) + (c >> 3);
 }
 
 // Index (in fp16 units) of the value scale/zero of (token t, channel group gc)
 // inside its section: token pairs interleaved, so (t, t+1) of one gc form a half2.
-__host__ __device__ inline int vsz_index(int t, int gc, int ngc) {
+__host__ __device__ constexpr int vsz_index(int t, int gc, int ngc) {
   return ((t >> 1) * ngc + gc) * 2 + (t & 1);
 }
 
 // Bytes of one 32-token group block.
-__host__ __device__ inline int block_bytes(int D, int bits) { return 8 * D * (bits + 1); }
-__host__ __device__ inline int code_bytes(int D, int bits) { return 4 * D * bits; }
+__host__ __device__ constexpr int block_bytes(int D, int bits) { return 8 * D * (bits + 1); }
+__host__ __device__ constexpr int code_bytes(int D, int bits) { return 4 * D * bits; }
 
 struct CodePos {
   int word;   // 32-bit word index inside the K-code (or V-code) section
@@ -64,7 +64,7 @@ struct CodePos {
 };
 
 // Words of one section a lane owns (D*BITS/32) and pairs per word (16/BITS).
-__host__ __device__ inline int words_per_lane(int D, int bits) { return D * bits / 32; }
+__host__ __device__ constexpr int words_per_lane(int D, int bits) { return D * bits / 32; }
 
 __host__ __device__ inline CodePos word_pos(int lane, int pi, int bits) {
   int ppw = 16 / bits;
@@ -100,12 +100,12 @@ __host__ __device__ inline CodePos vcode_pos(int t, int c, int D, int bits) {
 }
 
 // Section offsets inside a block (bytes).
-__host__ __device__ inline int off_kcodes(int, int) { return 0; }
-__host__ __device__ inline int off_vcodes(int D, int bits) { return code_bytes(D, bits); }
-__host__ __device__ inline int off_kscale(int D, int bits) { return 2 * code_bytes(D, bits); }
-__host__ __device__ inline int off_kzero(int D, int bits) { return 2 * code_bytes(D, bits) + 2 * D; }
-__host__ __device__ inline int off_vscale(int D, int bits) { return 2 * code_bytes(D, bits) + 4 * D; }
-__host__ __device__ inline int off_vzero(int D, int bits) { return 2 * code_bytes(D, bits) + 6 * D; }
+__host__ __device__ constexpr int off_kcodes(int, int) { return 0; }
+__host__ __device__ constexpr int off_vcodes(int D, int bits) { return code_bytes(D, bits); }
+__host__ __device__ constexpr int off_kscale(int D, int bits) { return 2 * code_bytes(D, bits); }
+__host__ __device__ constexpr int off_kzero(int D, int bits) { return 2 * code_bytes(D, bits) + 2 * D; }
+__host__ __device__ constexpr int off_vscale(int D, int bits) { return 2 * code_bytes(D, bits) + 4 * D; }
+__host__ __device__ constexpr int off_vzero(int D, int bits) { return 2 * code_bytes(D, bits) + 6 * D; }
 
 // ------------------------------------------------------------------ cache state
 struct LayerState {
@@ -143,6 +143,7 @@ struct kvc_cache {
   float* pooled = nullptr;    size_t score_elems = 0;
   float* dec_part = nullptr;  size_t dec_part_elems = 0;
   unsigned* tickets = nullptr; size_t n_tickets = 0;
+  unsigned* err = nullptr;     // device error word (bounded waits that gave up)
   int max_ctas_per_unit = 0;
   int last_scored_layer = -1;
   std::vector<void*> allocations;
@@ -162,12 +163,13 @@ cudaError_t launch_pool_topk(const kvc_cache* c, int layer, int32_t* kept_out, i
 cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* kept, int n_kept,
                                 const __nv_bfloat16* k, const __nv_bfloat16* v,
                                 cudaStream_t stream);
-cudaError_t launch_window_init(const kvc_cache* c, int layer, const int32_t* kept, int n_kept,
-                               const __nv_bfloat16* k, const __nv_bfloat16* v,
-                               cudaStream_t stream);
 cudaError_t launch_append(const kvc_cache* c, int layer_begin, int layer_count,
                           const __nv_bfloat16* k_new, const __nv_bfloat16* v_new,
                           const int* flush_flags, cudaStream_t stream);
+cudaError_t launch_decode_step(const kvc_cache* c, int layer_begin, int layer_count,
+                               const __nv_bfloat16* q, const __nv_bfloat16* k_new,
+                               const __nv_bfloat16* v_new, const int* flush_flags, float* out,
+                               cudaStream_t stream);
 cudaError_t launch_decode(const kvc_cache* c, int layer_begin, int layer_count,
                           const __nv_bfloat16* q, float* out, cudaStream_t stream);
 cudaError_t launch_export(const kvc_cache* c, int layer, const kvc_export* dst,
@@ -181,7 +183,7 @@ cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float*
 
 // Decode work decomposition shared by the host (sizing) and the kernel.
 constexpr int kDecWarps = 4;
-constexpr int kGroupsPerCta = 64;      // packed groups per decode CTA (16 per warp)
+constexpr int kGroupsPerCta = 16;      // packed groups per decode CTA (4 per warp)
 constexpr int kWinSlotsPerCta = 128;   // window slots per decode CTA (32 per warp)
 inline int packed_ctas(int n_groups) { return (n_groups + kGroupsPerCta - 1) / kGroupsPerCta; }
 inline int window_ctas(int win_len) { return (win_len + kWinSlotsPerCta - 1) / kWinSlotsPerCta; }

@@ -10,181 +10,59 @@
 // S == 0 gives code 0. MiniKV Algorithm 1 (decoding): new tokens go to a 16-bit
 // buffer that is quantized as it fills; here the oldest 32 tokens are quantized
 // as one group whenever the window reaches R tokens.
-#include "kvc_internal.cuh"
+#include "quant_device.cuh"
 
 namespace kvc {
 namespace {
 
-constexpr int kThreads = 128;
-
-__device__ __forceinline__ void group_params(float lo, float hi, int bits, __half& S, __half& Z,
-                                             float& Sf, float& Zf) {
-  float rng = __fsub_rn(hi, lo);
-  float s32 = __fdiv_rn(rng, (float)((1 << bits) - 1));
-  S = __float2half_rn(s32);
-  Z = __float2half_rn(lo);
-  Sf = __half2float(S);
-  Zf = __half2float(Z);
-}
-
-__device__ __forceinline__ int quant_code(float x, float Zf, float Sf, int bits) {
-  if (Sf == 0.f) return 0;
-  float q = __fdiv_rn(__fsub_rn(x, Zf), Sf);
-  int c = __float2int_rn(q);
-  int top = (1 << bits) - 1;
-  return c < 0 ? 0 : (c > top ? top : c);
-}
-
-// Shared-memory staging of one group: 32 key rows and 32 value rows (fp32,
-// natural channel order) plus their codes.
-template <int D>
-struct GroupSmem {
-  float k[KVC_GROUP][D + 1];
-  float v[KVC_GROUP][D + 1];
-  uint8_t kc[KVC_GROUP][D];
-  uint8_t vc[KVC_GROUP][D];
-};
-
-// Quantize the staged group and write one block. All kThreads threads call it.
-template <int D, int BITS>
-__device__ void quantize_block(GroupSmem<D>& s, uint8_t* __restrict__ blk) {
-  __half* kS = reinterpret_cast<__half*>(blk + off_kscale(D, BITS));
-  __half* kZ = reinterpret_cast<__half*>(blk + off_kzero(D, BITS));
-  __half* vS = reinterpret_cast<__half*>(blk + off_vscale(D, BITS));
-  __half* vZ = reinterpret_cast<__half*>(blk + off_vzero(D, BITS));
-  // keys: one group per channel over the 32 tokens
-  for (int c = threadIdx.x; c < D; c += kThreads) {
-    float lo = s.k[0][c], hi = lo;
-#pragma unroll 8
-    for (int t = 1; t < KVC_GROUP; ++t) { lo = fminf(lo, s.k[t][c]); hi = fmaxf(hi, s.k[t][c]); }
-    __half S, Z; float Sf, Zf;
-    group_params(lo, hi, BITS, S, Z, Sf, Zf);
-    for (int t = 0; t < KVC_GROUP; ++t) s.kc[t][c] = (uint8_t)quant_code(s.k[t][c], Zf, Sf, BITS);
-    kS[kperm(c, D)] = S;
-    kZ[kperm(c, D)] = Z;
-  }
-  // values: one group per (token, 32 channels)
-  constexpr int NGC = D / KVC_GROUP;
-  for (int i = threadIdx.x; i < KVC_GROUP * NGC; i += kThreads) {
-    int t = i / NGC, gc = i % NGC;
-    const float* row = &s.v[t][gc * KVC_GROUP];
-    float lo = row[0], hi = lo;
-#pragma unroll 8
-    for (int j = 1; j < KVC_GROUP; ++j) { lo = fminf(lo, row[j]); hi = fmaxf(hi, row[j]); }
-    __half S, Z; float Sf, Zf;
-    group_params(lo, hi, BITS, S, Z, Sf, Zf);
-    for (int j = 0; j < KVC_GROUP; ++j)
-      s.vc[t][gc * KVC_GROUP + j] = (uint8_t)quant_code(row[j], Zf, Sf, BITS);
-    vS[vsz_index(t, gc, NGC)] = S;
-    vZ[vsz_index(t, gc, NGC)] = Z;
-  }
-  __syncthreads();
-  // pack code words in fragment order
-  constexpr int WPL = D * BITS / 32;
-  constexpr int PPW = 16 / BITS;
-  constexpr int NW = 32 * WPL;
-  uint32_t* kw = reinterpret_cast<uint32_t*>(blk + off_kcodes(D, BITS));
-  uint32_t* vw = reinterpret_cast<uint32_t*>(blk + off_vcodes(D, BITS));
-  for (int widx = threadIdx.x; widx < 2 * NW; widx += kThreads) {
-    bool is_v = widx >= NW;
-    int w = is_v ? widx - NW : widx;
-    int lane = (w & 127) >> 2;
-    int wi = (w >> 7) * 4 + (w & 3);
-    int gid = lane >> 2, tid = lane & 3;
-    uint32_t word = 0;
-#pragma unroll
-    for (int p = 0; p < PPW; ++p) {
-      int pi = wi * PPW + p;
-      int half = pi & 1, q = pi >> 1;
-      uint32_t ce, co;
-      if (!is_v) {
-        int nt = q / (D / 16), ks = q % (D / 16);
-        int t = nt * 8 + gid, c = 16 * ks + 2 * tid + 8 * half;
-        ce = s.kc[t][c]; co = s.kc[t][c + 1];
-      } else {
-        int ks = q / (D / 8), nt = q % (D / 8);
-        int t = 16 * ks + 2 * tid + 8 * half, c = 8 * nt + gid;
-        ce = s.vc[t][c]; co = s.vc[t + 1][c];
-      }
-      word |= ce << (BITS * p);
-      word |= co << (16 + BITS * p);
-    }
-    (is_v ? vw : kw)[w] = word;
-  }
-}
-
-__device__ __forceinline__ void load_row_bf16_to_smem(float* dst, const __nv_bfloat16* src, int D,
-                                                      int lane16, int n16) {
-  // one thread copies 8 channels (16 bytes)
-  (void)n16;
-  uint4 u = *reinterpret_cast<const uint4*>(src + lane16 * 8);
-  const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) dst[lane16 * 8 + j] = __bfloat162float(h[j]);
-  (void)D;
-}
+constexpr int kThreads = 256;
 
 // --------------------------------------------------------------------- kernels
-// grid.x = group index j within the unit, grid.y = unit (b * H + h)
+// grid.x = group index j within the unit (j == n_groups: the initial window),
+// grid.y = unit (b * H + h)
 template <int D, int BITS>
 __global__ void __launch_bounds__(kThreads)
 gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-                    const int32_t* __restrict__ kept, int n_kept, int n, uint8_t* __restrict__ packed,
-                    int cap_groups, int block_bytes) {
+                    const int32_t* __restrict__ kept, int n_kept, int n, int alpha,
+                    uint8_t* __restrict__ packed, int cap_groups, int block_bytes, int R,
+                    __nv_bfloat16* __restrict__ win_k, __nv_bfloat16* __restrict__ win_v) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  GroupSmem<D>& s = *reinterpret_cast<GroupSmem<D>*>(smem_raw);
   const int j = blockIdx.x, unit = blockIdx.y;
+  const int n_groups = n_kept / KVC_GROUP;
   const __nv_bfloat16* K = k + (size_t)unit * n * D;
   const __nv_bfloat16* V = v + (size_t)unit * n * D;
   const int32_t* kp = kept ? kept + (size_t)unit * n_kept : nullptr;
+  if (j == n_groups) {
+    // initial window: the kept tokens past the last whole group, then the
+    // alpha observation tokens, in ring slots 0 .. W-1
+    const int n_full = n_groups * KVC_GROUP, tail = n_kept - n_full, W = tail + alpha;
+    __nv_bfloat16* wk = win_k + (size_t)unit * R * D;
+    __nv_bfloat16* wv = win_v + (size_t)unit * R * D;
+    for (int i = threadIdx.x; i < W * D; i += kThreads) {
+      const int w = i / D, c = i % D;
+      const int idx = w < tail ? (kp ? kp[n_full + w] : n_full + w) : n - alpha + (w - tail);
+      window_store(wk, wv, w, c, D, K[(size_t)idx * D + c], V[(size_t)idx * D + c]);
+    }
+    return;
+  }
+  GroupSmem<D, kThreads>& s = *reinterpret_cast<GroupSmem<D, kThreads>*>(smem_raw);
   constexpr int CH = D / 8;   // 16-byte chunks per row
   for (int i = threadIdx.x; i < KVC_GROUP * CH; i += kThreads) {
-    int t = i / CH, ch = i % CH;
-    int idx = kp ? kp[j * KVC_GROUP + t] : j * KVC_GROUP + t;
-    load_row_bf16_to_smem(s.k[t], K + (size_t)idx * D, D, ch, CH);
-    load_row_bf16_to_smem(s.v[t], V + (size_t)idx * D, D, ch, CH);
+    const int t = i / CH, ch = i % CH;
+    const int idx = kp ? kp[j * KVC_GROUP + t] : j * KVC_GROUP + t;
+    const uint4 uk = __ldg(reinterpret_cast<const uint4*>(K + (size_t)idx * D) + ch);
+    const uint4 uv = __ldg(reinterpret_cast<const uint4*>(V + (size_t)idx * D) + ch);
+    const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(&uk);
+    const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&uv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      s.k[t][ch * 8 + e] = __bfloat162float(hk[e]);
+      s.v[t][ch * 8 + e] = __bfloat162float(hv[e]);
+    }
   }
   __syncthreads();
   uint8_t* blk = packed + ((size_t)unit * cap_groups + j) * block_bytes;
-  quantize_block<D, BITS>(s, blk);
-}
-
-// Window rows: keys permuted by kperm, values in token pairs permuted by vperm.
-__device__ __forceinline__ void window_store(__nv_bfloat16* __restrict__ wk,
-                                             __nv_bfloat16* __restrict__ wv, int slot, int c, int D,
-                                             __nv_bfloat16 kval, __nv_bfloat16 vval) {
-  wk[(size_t)slot * D + kperm(c, D)] = kval;
-  wv[((size_t)(slot >> 1) * D + vperm(c, D)) * 2 + (slot & 1)] = vval;
-}
-
-__device__ __forceinline__ __nv_bfloat16 window_load_k(const __nv_bfloat16* wk, int slot, int c,
-                                                       int D) {
-  return wk[(size_t)slot * D + kperm(c, D)];
-}
-__device__ __forceinline__ __nv_bfloat16 window_load_v(const __nv_bfloat16* wv, int slot, int c,
-                                                       int D) {
-  return wv[((size_t)(slot >> 1) * D + vperm(c, D)) * 2 + (slot & 1)];
-}
-
-// grid.x = unit; copies the initial window (kept tail, then observation tokens)
-__global__ void __launch_bounds__(kThreads)
-window_init_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-                   const int32_t* __restrict__ kept, int n_kept, int n_full, int n, int alpha,
-                   int D, int R, __nv_bfloat16* __restrict__ win_k,
-                   __nv_bfloat16* __restrict__ win_v) {
-  const int unit = blockIdx.x;
-  const int tail = n_kept - n_full;
-  const int W = tail + alpha;
-  const __nv_bfloat16* K = k + (size_t)unit * n * D;
-  const __nv_bfloat16* V = v + (size_t)unit * n * D;
-  __nv_bfloat16* wk = win_k + (size_t)unit * R * D;
-  __nv_bfloat16* wv = win_v + (size_t)unit * R * D;
-  const int32_t* kp = kept ? kept + (size_t)unit * n_kept : nullptr;
-  for (int i = threadIdx.x; i < W * D; i += kThreads) {
-    int w = i / D, c = i % D;
-    int idx = w < tail ? (kp ? kp[n_full + w] : n_full + w) : n - alpha + (w - tail);
-    window_store(wk, wv, w, c, D, K[(size_t)idx * D + c], V[(size_t)idx * D + c]);
-  }
+  quantize_block<D, BITS, kThreads>(s, blk);
 }
 
 struct AppendParams {
@@ -213,17 +91,17 @@ append_kernel(AppendParams P, int layer_begin, int units, int R, const __nv_bflo
   const int fs = P.flush_start[lrel];
   if (fs < 0) return;
   __syncthreads();   // the new token may belong to the flushed group (R == 32)
-  GroupSmem<D>& s = *reinterpret_cast<GroupSmem<D>*>(smem_raw);
+  GroupSmem<D, kThreads>& s = *reinterpret_cast<GroupSmem<D, kThreads>*>(smem_raw);
   for (int i = threadIdx.x; i < KVC_GROUP * D; i += kThreads) {
-    int t = i / D, c = i % D;
-    int sl = fs + t;
+    const int t = i / D, c = i % D;
+    const int sl = fs + t;
     s.k[t][c] = __bfloat162float(window_load_k(wk, sl, c, D));
     s.v[t][c] = __bfloat162float(window_load_v(wv, sl, c, D));
   }
   __syncthreads();
   uint8_t* blk = packed + P.packed_off[lrel] +
                  ((size_t)unit * P.cap_groups[lrel] + P.flush_group[lrel]) * block_bytes;
-  quantize_block<D, BITS>(s, blk);
+  quantize_block<D, BITS, kThreads>(s, blk);
 }
 
 // Export: grid.x = group j (or window when j == n_groups), grid.y = unit
@@ -239,9 +117,9 @@ export_kernel(const uint8_t* __restrict__ packed, int cap_groups, int n_groups, 
     __nv_bfloat16* ok = reinterpret_cast<__nv_bfloat16*>(dst.win_k);
     __nv_bfloat16* ov = reinterpret_cast<__nv_bfloat16*>(dst.win_v);
     for (int i = threadIdx.x; i < win_len * D; i += kThreads) {
-      int w = i / D, c = i % D;
-      int slot = (win_start + w) % R;
-      size_t o = ((size_t)unit * win_len + w) * D + c;
+      const int w = i / D, c = i % D;
+      const int slot = (win_start + w) % R;
+      const size_t o = ((size_t)unit * win_len + w) * D + c;
       if (ok) ok[o] = window_load_k(wk, slot, c, D);
       if (ov) ov[o] = window_load_v(wv, slot, c, D);
     }
@@ -257,22 +135,22 @@ export_kernel(const uint8_t* __restrict__ packed, int cap_groups, int n_groups, 
   const int T = n_groups * KVC_GROUP;
   const uint32_t mask = (1u << BITS) - 1;
   for (int i = threadIdx.x; i < KVC_GROUP * D; i += kThreads) {
-    int t = i / D, c = i % D;
-    size_t o = ((size_t)unit * T + (size_t)j * KVC_GROUP + t) * D + c;
-    CodePos pk = kcode_pos(t, c, D, BITS);
-    CodePos pv = vcode_pos(t, c, D, BITS);
+    const int t = i / D, c = i % D;
+    const size_t o = ((size_t)unit * T + (size_t)j * KVC_GROUP + t) * D + c;
+    const CodePos pk = kcode_pos(t, c, D, BITS);
+    const CodePos pv = vcode_pos(t, c, D, BITS);
     if (dst.k_codes) dst.k_codes[o] = (uint8_t)((kw[pk.word] >> pk.bit) & mask);
     if (dst.v_codes) dst.v_codes[o] = (uint8_t)((vw[pv.word] >> pv.bit) & mask);
   }
   constexpr int NGC = D / KVC_GROUP;
   for (int c = threadIdx.x; c < D; c += kThreads) {
-    size_t o = ((size_t)unit * n_groups + j) * D + c;
+    const size_t o = ((size_t)unit * n_groups + j) * D + c;
     if (dst.k_scale) reinterpret_cast<__half*>(dst.k_scale)[o] = kS[kperm(c, D)];
     if (dst.k_zero) reinterpret_cast<__half*>(dst.k_zero)[o] = kZ[kperm(c, D)];
   }
   for (int i = threadIdx.x; i < KVC_GROUP * NGC; i += kThreads) {
     const int t = i / NGC, gc = i % NGC;
-    size_t o = ((size_t)unit * T + (size_t)j * KVC_GROUP) * NGC + i;
+    const size_t o = ((size_t)unit * T + (size_t)j * KVC_GROUP) * NGC + i;
     if (dst.v_scale) reinterpret_cast<__half*>(dst.v_scale)[o] = vS[vsz_index(t, gc, NGC)];
     if (dst.v_zero) reinterpret_cast<__half*>(dst.v_zero)[o] = vZ[vsz_index(t, gc, NGC)];
   }
@@ -280,14 +158,14 @@ export_kernel(const uint8_t* __restrict__ packed, int cap_groups, int n_groups, 
 
 __global__ void export_kept_kernel(const int32_t* __restrict__ kept, int n_kept, int units,
                                    int32_t* __restrict__ out) {
-  size_t total = (size_t)units * n_kept;
+  const size_t total = (size_t)units * n_kept;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
        i += (size_t)gridDim.x * blockDim.x)
     out[i] = kept ? kept[i] : (int32_t)(i % n_kept);
 }
 
 template <int D>
-constexpr size_t group_smem() { return sizeof(GroupSmem<D>); }
+constexpr size_t group_smem() { return sizeof(GroupSmem<D, kThreads>); }
 
 }  // namespace
 
@@ -301,41 +179,28 @@ constexpr size_t group_smem() { return sizeof(GroupSmem<D>); }
     else return cudaErrorInvalidValue;                                            \
   } while (0)
 
-template <typename K>
-static cudaError_t set_smem(K kernel, size_t bytes) {
+template <typename Kern>
+static cudaError_t set_smem(Kern kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+// Packs the kept tokens' whole groups and writes the initial window (one launch).
 cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* kept, int n_kept,
                                 const __nv_bfloat16* k, const __nv_bfloat16* v,
                                 cudaStream_t stream) {
   const kvc_dims& d = c->dims;
   const LayerState& ls = c->L[layer];
-  int groups = n_kept / KVC_GROUP;
-  int units = d.batch * d.n_kv_heads;
-  if (groups == 0) return cudaSuccess;
+  const int groups = n_kept / KVC_GROUP;
+  const int units = d.batch * d.n_kv_heads;
+  const size_t woff = (size_t)layer * units * d.window_len * d.head_dim;
   KVC_DISPATCH_DB(d.head_dim, d.bits, {
-    size_t sm = group_smem<D>();
+    const size_t sm = group_smem<D>();
     cudaError_t e = set_smem(gather_quant_kernel<D, BITS>, sm);
     if (e != cudaSuccess) return e;
-    gather_quant_kernel<D, BITS><<<dim3(groups, units), kThreads, sm, stream>>>(
-        k, v, kept, n_kept, d.prompt_len, c->packed + ls.packed_off, ls.cap_groups,
-        c->block_bytes);
+    gather_quant_kernel<D, BITS><<<dim3(groups + 1, units), kThreads, sm, stream>>>(
+        k, v, kept, n_kept, d.prompt_len, d.obs_window, c->packed + ls.packed_off, ls.cap_groups,
+        c->block_bytes, d.window_len, c->win_k + woff, c->win_v + woff);
   });
-  count_launches(1);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_window_init(const kvc_cache* c, int layer, const int32_t* kept, int n_kept,
-                               const __nv_bfloat16* k, const __nv_bfloat16* v,
-                               cudaStream_t stream) {
-  const kvc_dims& d = c->dims;
-  int units = d.batch * d.n_kv_heads;
-  int n_full = (n_kept / KVC_GROUP) * KVC_GROUP;
-  size_t off = (size_t)layer * units * d.window_len * d.head_dim;
-  window_init_kernel<<<units, kThreads, 0, stream>>>(k, v, kept, n_kept, n_full, d.prompt_len,
-                                                      d.obs_window, d.head_dim, d.window_len,
-                                                      c->win_k + off, c->win_v + off);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -344,10 +209,10 @@ cudaError_t launch_append(const kvc_cache* c, int layer_begin, int layer_count,
                           const __nv_bfloat16* k_new, const __nv_bfloat16* v_new,
                           const int* flush_flags, cudaStream_t stream) {
   const kvc_dims& d = c->dims;
-  int units = d.batch * d.n_kv_heads;
+  const int units = d.batch * d.n_kv_heads;
   for (int base = 0; base < layer_count; base += KVC_MAX_LAUNCH_LAYERS) {
-    int cnt = layer_count - base < KVC_MAX_LAUNCH_LAYERS ? layer_count - base
-                                                         : KVC_MAX_LAUNCH_LAYERS;
+    const int cnt = layer_count - base < KVC_MAX_LAUNCH_LAYERS ? layer_count - base
+                                                               : KVC_MAX_LAUNCH_LAYERS;
     AppendParams P;
     for (int i = 0; i < cnt; ++i) {
       const LayerState& ls = c->L[layer_begin + base + i];
@@ -360,7 +225,7 @@ cudaError_t launch_append(const kvc_cache* c, int layer_begin, int layer_count,
     const __nv_bfloat16* kn = k_new + (size_t)base * units * d.head_dim;
     const __nv_bfloat16* vn = v_new + (size_t)base * units * d.head_dim;
     KVC_DISPATCH_DB(d.head_dim, d.bits, {
-      size_t sm = group_smem<D>();
+      const size_t sm = group_smem<D>();
       cudaError_t e = set_smem(append_kernel<D, BITS>, sm);
       if (e != cudaSuccess) return e;
       append_kernel<D, BITS><<<cnt * units, kThreads, sm, stream>>>(
@@ -368,7 +233,7 @@ cudaError_t launch_append(const kvc_cache* c, int layer_begin, int layer_count,
           c->block_bytes);
     });
     count_launches(1);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -378,8 +243,8 @@ cudaError_t launch_export(const kvc_cache* c, int layer, const kvc_export* dst,
                           cudaStream_t stream) {
   const kvc_dims& d = c->dims;
   const LayerState& ls = c->L[layer];
-  int units = d.batch * d.n_kv_heads;
-  size_t woff = (size_t)layer * units * d.window_len * d.head_dim;
+  const int units = d.batch * d.n_kv_heads;
+  const size_t woff = (size_t)layer * units * d.window_len * d.head_dim;
   KVC_DISPATCH_DB(d.head_dim, d.bits, {
     export_kernel<D, BITS><<<dim3(ls.n_groups + 1, units), kThreads, 0, stream>>>(
         c->packed + ls.packed_off, ls.cap_groups, ls.n_groups, c->block_bytes, c->win_k + woff,

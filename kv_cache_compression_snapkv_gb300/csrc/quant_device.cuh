@@ -1,0 +1,152 @@
+// quant_device.cuh -- the group quantizer and window-ring accessors, shared by
+// the prefill/append kernels (quant.cu) and the fused decode step (decode.cu).
+//
+// KIVI-style asymmetric groups (blog "Quantization: keep each token in fewer
+// bits"; MiniKV §4.4): keys per channel over 32 consecutive stored tokens,
+// values per token over 32 consecutive channels; zero-point = group min,
+// scale = (max - min) / (2^b - 1), both stored as fp16 (round to nearest even).
+// Codes use the stored fp16 values: code = rint((x - Z) / S) clamped to
+// [0, 2^b - 1], with explicit IEEE round-to-nearest fp32 subtract and divide (no
+// contraction, no reciprocal) and round-half-to-even conversion; S == 0 gives 0.
+#pragma once
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+__device__ __forceinline__ void group_params(float lo, float hi, int bits, __half& S, __half& Z,
+                                             float& Sf, float& Zf) {
+  const float rng = __fsub_rn(hi, lo);
+  const float s32 = __fdiv_rn(rng, (float)((1 << bits) - 1));
+  S = __float2half_rn(s32);
+  Z = __float2half_rn(lo);
+  Sf = __half2float(S);
+  Zf = __half2float(Z);
+}
+
+__device__ __forceinline__ int quant_code(float x, float Zf, float Sf, int bits) {
+  if (Sf == 0.f) return 0;
+  const float q = __fdiv_rn(__fsub_rn(x, Zf), Sf);
+  const int c = __float2int_rn(q);
+  const int top = (1 << bits) - 1;
+  return c < 0 ? 0 : (c > top ? top : c);
+}
+
+// Staging of one group: 32 key rows and 32 value rows (fp32, natural channel
+// order), their codes, and partial min/max when a group is split over threads.
+template <int D, int NT>
+struct GroupSmem {
+  static constexpr int NP = NT / D;   // threads per quantization group
+  static_assert(NP >= 1 && KVC_GROUP % NP == 0, "thread count must be a multiple of D");
+  float k[KVC_GROUP][D + 1];
+  float v[KVC_GROUP][D + 1];
+  uint8_t kc[KVC_GROUP][D];
+  uint8_t vc[KVC_GROUP][D];
+  float klo[NP][D], khi[NP][D], vlo[NP][D], vhi[NP][D];
+};
+
+// Quantize the staged group into one block at `blk` (global or shared). All NT
+// threads of the block call it. Each of the D key groups (channels) and D value
+// groups (token, 32 channels) is handled by NP threads taking 32/NP elements.
+template <int D, int BITS, int NT>
+__device__ void quantize_block(GroupSmem<D, NT>& s, uint8_t* __restrict__ blk) {
+  constexpr int NP = GroupSmem<D, NT>::NP, PER = KVC_GROUP / NP, NGC = D / KVC_GROUP;
+  __half* kS = reinterpret_cast<__half*>(blk + off_kscale(D, BITS));
+  __half* kZ = reinterpret_cast<__half*>(blk + off_kzero(D, BITS));
+  __half* vS = reinterpret_cast<__half*>(blk + off_vscale(D, BITS));
+  __half* vZ = reinterpret_cast<__half*>(blk + off_vzero(D, BITS));
+  const int g = threadIdx.x % D, part = threadIdx.x / D;
+  const bool act = threadIdx.x < NP * D;
+  const int vt = g / NGC, vgc = g % NGC;       // value group g = (token vt, channels vgc*32..)
+  const float* vrow = &s.v[vt][vgc * KVC_GROUP + part * PER];
+  if (act) {
+    float lo = s.k[part * PER][g], hi = lo;
+#pragma unroll
+    for (int t = 1; t < PER; ++t) {
+      lo = fminf(lo, s.k[part * PER + t][g]);
+      hi = fmaxf(hi, s.k[part * PER + t][g]);
+    }
+    s.klo[part][g] = lo;
+    s.khi[part][g] = hi;
+    float vl = vrow[0], vh = vl;
+#pragma unroll
+    for (int j = 1; j < PER; ++j) { vl = fminf(vl, vrow[j]); vh = fmaxf(vh, vrow[j]); }
+    s.vlo[part][g] = vl;
+    s.vhi[part][g] = vh;
+  }
+  __syncthreads();
+  if (act) {
+    float lo = s.klo[0][g], hi = s.khi[0][g];
+#pragma unroll
+    for (int p = 1; p < NP; ++p) { lo = fminf(lo, s.klo[p][g]); hi = fmaxf(hi, s.khi[p][g]); }
+    __half S, Z; float Sf, Zf;
+    group_params(lo, hi, BITS, S, Z, Sf, Zf);
+#pragma unroll
+    for (int t = 0; t < PER; ++t)
+      s.kc[part * PER + t][g] = (uint8_t)quant_code(s.k[part * PER + t][g], Zf, Sf, BITS);
+    if (part == 0) { kS[kperm(g, D)] = S; kZ[kperm(g, D)] = Z; }
+  }
+  if (act) {
+    float lo = s.vlo[0][g], hi = s.vhi[0][g];
+#pragma unroll
+    for (int p = 1; p < NP; ++p) { lo = fminf(lo, s.vlo[p][g]); hi = fmaxf(hi, s.vhi[p][g]); }
+    __half S, Z; float Sf, Zf;
+    group_params(lo, hi, BITS, S, Z, Sf, Zf);
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+      s.vc[vt][vgc * KVC_GROUP + part * PER + j] = (uint8_t)quant_code(vrow[j], Zf, Sf, BITS);
+    if (part == 0) { vS[vsz_index(vt, vgc, NGC)] = S; vZ[vsz_index(vt, vgc, NGC)] = Z; }
+  }
+  __syncthreads();
+  // pack code words in fragment order
+  constexpr int WPL = D * BITS / 32;
+  constexpr int PPW = 16 / BITS;
+  constexpr int NW = 32 * WPL;
+  uint32_t* kw = reinterpret_cast<uint32_t*>(blk + off_kcodes(D, BITS));
+  uint32_t* vw = reinterpret_cast<uint32_t*>(blk + off_vcodes(D, BITS));
+  for (int widx = threadIdx.x; widx < 2 * NW; widx += NT) {
+    const bool is_v = widx >= NW;
+    const int w = is_v ? widx - NW : widx;
+    const int lane = (w & 127) >> 2;
+    const int wi = (w >> 7) * 4 + (w & 3);
+    const int gid = lane >> 2, tid = lane & 3;
+    uint32_t word = 0;
+#pragma unroll
+    for (int p = 0; p < PPW; ++p) {
+      const int pi = wi * PPW + p;
+      const int half = pi & 1, q = pi >> 1;
+      uint32_t ce, co;
+      if (!is_v) {
+        const int nt = q / (D / 16), ks = q % (D / 16);
+        const int t = nt * 8 + gid, c = 16 * ks + 2 * tid + 8 * half;
+        ce = s.kc[t][c]; co = s.kc[t][c + 1];
+      } else {
+        const int ks = q / (D / 8), nt = q % (D / 8);
+        const int t = 16 * ks + 2 * tid + 8 * half, c = 8 * nt + gid;
+        ce = s.vc[t][c]; co = s.vc[t + 1][c];
+      }
+      word |= ce << (BITS * p);
+      word |= co << (16 + BITS * p);
+    }
+    (is_v ? vw : kw)[w] = word;
+  }
+}
+
+// Window ring rows: keys permuted by kperm, values in token pairs permuted by vperm.
+__device__ __forceinline__ void window_store(__nv_bfloat16* __restrict__ wk,
+                                             __nv_bfloat16* __restrict__ wv, int slot, int c, int D,
+                                             __nv_bfloat16 kval, __nv_bfloat16 vval) {
+  wk[(size_t)slot * D + kperm(c, D)] = kval;
+  wv[((size_t)(slot >> 1) * D + vperm(c, D)) * 2 + (slot & 1)] = vval;
+}
+
+__device__ __forceinline__ __nv_bfloat16 window_load_k(const __nv_bfloat16* wk, int slot, int c,
+                                                       int D) {
+  return wk[(size_t)slot * D + kperm(c, D)];
+}
+__device__ __forceinline__ __nv_bfloat16 window_load_v(const __nv_bfloat16* wv, int slot, int c,
+                                                       int D) {
+  return wv[((size_t)(slot >> 1) * D + vperm(c, D)) * 2 + (slot & 1)];
+}
+
+}  // namespace kvc

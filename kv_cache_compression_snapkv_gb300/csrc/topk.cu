@@ -7,6 +7,8 @@
 //
 // One CTA of 1024 threads per (sequence, kv head):
 //   1. pooled[i] = max of scores[i - (w-1)/2 .. i + (w-1)/2] clipped to the range;
+//      the pooled row is staged in shared memory when it fits (n - alpha <=
+//      kSmemMax), otherwise it is re-read from global memory (L2);
 //   2. radix select of the k-th largest pooled value tau on its fp32 bit pattern
 //      (scores are >= 0, so unsigned order == float order), four 8-bit passes;
 //   3. ordered compaction: every index with pooled > tau, plus the lowest-index
@@ -18,6 +20,7 @@ namespace {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kWarps = kTopkThreads / 32;
+constexpr int kSmemMax = 32 * 1024;     // rows up to this length are staged in shared memory
 
 struct TopkSmem {
   unsigned hist[256];
@@ -58,20 +61,49 @@ __device__ __forceinline__ void block_scan2(TopkSmem& s, unsigned a, unsigned b,
   eb = pb + ib - b;
 }
 
+// SMEM: the pooled row lives in dynamic shared memory; else in `pooled` (global).
+template <bool SMEM>
 __global__ void __launch_bounds__(kTopkThreads)
 pool_topk_kernel(const float* __restrict__ scores, float* __restrict__ pooled, int ns, int w,
                  int k_sel, int32_t* __restrict__ kept) {
   __shared__ TopkSmem s;
+  extern __shared__ __align__(16) float spool[];
   const int unit = blockIdx.x;
   const float* sc = scores + (size_t)unit * ns;
-  float* pl = pooled + (size_t)unit * ns;
+  float* pg = pooled + (size_t)unit * ns;
+  float* pl = SMEM ? spool : pg;
   int32_t* out = kept + (size_t)unit * k_sel;
   const int r = (w - 1) / 2;
-  for (int i = threadIdx.x; i < ns; i += kTopkThreads) {
-    float m = sc[i];
-    const int lo = i - r < 0 ? 0 : i - r, hi = i + r >= ns ? ns - 1 : i + r;
-    for (int t = lo; t <= hi; ++t) m = fmaxf(m, sc[t]);
-    pl[i] = m;
+  if constexpr (SMEM) {
+    // stage the scores (coalesced), pool from shared memory into registers, write back
+    constexpr int PER = kSmemMax / kTopkThreads;
+    for (int i = threadIdx.x; i < ns; i += kTopkThreads) spool[i] = __ldg(sc + i);
+    __syncthreads();
+    float pv[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = threadIdx.x + j * kTopkThreads;
+      float m = 0.f;
+      if (i < ns) {
+        m = spool[i];
+        const int lo = i - r < 0 ? 0 : i - r, hi = i + r >= ns ? ns - 1 : i + r;
+        for (int t = lo; t <= hi; ++t) m = fmaxf(m, spool[t]);
+      }
+      pv[j] = m;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = threadIdx.x + j * kTopkThreads;
+      if (i < ns) { spool[i] = pv[j]; pg[i] = pv[j]; }
+    }
+  } else {
+    for (int i = threadIdx.x; i < ns; i += kTopkThreads) {
+      float m = __ldg(sc + i);
+      const int lo = i - r < 0 ? 0 : i - r, hi = i + r >= ns ? ns - 1 : i + r;
+      for (int t = lo; t <= hi; ++t) m = fmaxf(m, __ldg(sc + t));
+      pg[i] = m;
+    }
   }
   if (k_sel >= ns) {
     for (int i = threadIdx.x; i < ns; i += kTopkThreads) out[i] = i;
@@ -86,9 +118,18 @@ pool_topk_kernel(const float* __restrict__ scores, float* __restrict__ pooled, i
     const int shift = 24 - 8 * pass;
     for (int b = threadIdx.x; b < 256; b += kTopkThreads) s.hist[b] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < ns; i += kTopkThreads) {
-      const unsigned u = __float_as_uint(pl[i]);
-      if ((u & mask) == prefix) atomicAdd(&s.hist[(u >> shift) & 255u], 1u);
+    // scores cluster in a few bins: aggregate equal bins within a warp first so
+    // the shared-memory atomics do not serialize on one address
+    for (int base = 0; base < ns; base += kTopkThreads) {
+      const int i = base + threadIdx.x;
+      unsigned key = 256u;                              // "no bin"
+      if (i < ns) {
+        const unsigned u = __float_as_uint(pl[i]);
+        if ((u & mask) == prefix) key = (u >> shift) & 255u;
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      if (key < 256u && (threadIdx.x & 31) == __ffs(peers) - 1)
+        atomicAdd(&s.hist[key], (unsigned)__popc(peers));
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -122,29 +163,59 @@ pool_topk_kernel(const float* __restrict__ scores, float* __restrict__ pooled, i
   const unsigned tau = prefix;
   const unsigned need_eq = s.krem;
 
-  // ordered compaction over contiguous per-thread segments
-  const int seg = (ns + kTopkThreads - 1) / kTopkThreads;
-  const int i0 = threadIdx.x * seg;
-  const int i1 = i0 + seg < ns ? i0 + seg : ns;
+  // ordered compaction: warp w owns the contiguous span [w*span, (w+1)*span) and
+  // walks it 32 consecutive indices at a time (lanes read consecutive elements, so
+  // shared-memory reads are conflict-free); ballots give in-order ranks.
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int span = (ns + kWarps - 1) / kWarps;
+  const int w0 = warp * span, w1 = w0 + span < ns ? w0 + span : ns;
   unsigned gt = 0, eq = 0;
-  for (int i = i0; i < i1; ++i) {
-    const unsigned u = __float_as_uint(pl[i]);
-    gt += u > tau;
-    eq += u == tau;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const unsigned u = i < w1 ? __float_as_uint(pl[i]) : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, i < w1 && u > tau));
+    eq += __popc(__ballot_sync(0xffffffffu, i < w1 && u == tau));
   }
+  // exclusive scan over warps (lane 0 of each warp contributes its totals)
   unsigned egt, eeq;
-  block_scan2(s, gt, eq, egt, eeq);
+  block_scan2(s, threadIdx.x == warp * 32 ? gt : 0u, threadIdx.x == warp * 32 ? eq : 0u, egt,
+              eeq);
+  egt = __shfl_sync(0xffffffffu, egt, 0);
+  eeq = __shfl_sync(0xffffffffu, eeq, 0);
   unsigned pos = egt + (eeq < need_eq ? eeq : need_eq);
   unsigned eq_seen = eeq;
-  for (int i = i0; i < i1; ++i) {
-    const unsigned u = __float_as_uint(pl[i]);
-    bool take = u > tau;
-    if (u == tau) take = eq_seen++ < need_eq;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const unsigned u = i < w1 ? __float_as_uint(pl[i]) : 0u;
+    const bool is_gt = i < w1 && u > tau, is_eq = i < w1 && u == tau;
+    const unsigned beq = __ballot_sync(0xffffffffu, is_eq);
+    const bool take = is_gt || (is_eq && eq_seen + __popc(beq & lt) < need_eq);
+    const unsigned bt = __ballot_sync(0xffffffffu, take);
     if (take) {
-      if (pos < (unsigned)k_sel) out[pos] = i;   // bounded even if the select were wrong
-      ++pos;
+      const unsigned p = pos + __popc(bt & lt);
+      if (p < (unsigned)k_sel) out[p] = i;   // bounded even if the select were wrong
     }
+    pos += __popc(bt);
+    eq_seen += __popc(beq);
   }
+}
+
+cudaError_t launch_topk(const float* scores, float* pooled, int units, int ns, int w, int k_sel,
+                        int32_t* kept, cudaStream_t stream) {
+  if (ns <= kSmemMax) {
+    const size_t sm = (size_t)ns * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(pool_topk_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    pool_topk_kernel<true><<<units, kTopkThreads, sm, stream>>>(scores, pooled, ns, w, k_sel,
+                                                                 kept);
+  } else {
+    pool_topk_kernel<false><<<units, kTopkThreads, 0, stream>>>(scores, pooled, ns, w, k_sel,
+                                                                 kept);
+  }
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -153,24 +224,16 @@ cudaError_t launch_pool_topk(const kvc_cache* c, int layer, int32_t* kept_out, i
                              cudaStream_t stream) {
   (void)layer;
   const kvc_dims& d = c->dims;
-  const int units = d.batch * d.n_kv_heads;
-  const int ns = d.prompt_len - d.obs_window;
-  pool_topk_kernel<<<units, kTopkThreads, 0, stream>>>(c->scores, c->pooled, ns, d.pool_kernel,
-                                                        k_sel, kept_out);
-  count_launches(1);
-  return cudaGetLastError();
+  return launch_topk(c->scores, c->pooled, d.batch * d.n_kv_heads, d.prompt_len - d.obs_window,
+                     d.pool_kernel, k_sel, kept_out, stream);
 }
 
 // The same launch with the score and pooled buffers given explicitly (used by
 // the allocation-free selection entry point).
 cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float* pooled,
                                   int32_t* kept_out, int k_sel, cudaStream_t stream) {
-  const int units = d.batch * d.n_kv_heads;
-  const int ns = d.prompt_len - d.obs_window;
-  pool_topk_kernel<<<units, kTopkThreads, 0, stream>>>(scores, pooled, ns, d.pool_kernel, k_sel,
-                                                        kept_out);
-  count_launches(1);
-  return cudaGetLastError();
+  return launch_topk(scores, pooled, d.batch * d.n_kv_heads, d.prompt_len - d.obs_window,
+                     d.pool_kernel, k_sel, kept_out, stream);
 }
 
 }  // namespace kvc

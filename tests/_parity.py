@@ -184,6 +184,7 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
         ex = K.kvc_export_layer(cache, layer)
         torch.cuda.synchronize()
         check_export(ex, oracles[layer], same[layer], rep)
+    K.kvc_check_device(cache)          # no bounded device wait gave up
     cache.close()
     return rep
 
