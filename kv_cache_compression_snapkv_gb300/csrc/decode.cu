@@ -32,6 +32,9 @@
 // rounding of the operand does not limit accuracy. The zero-point sums are small
 // extra tensor-core products (q against the warp's groups' key zeros; p against
 // the value zeros). The window runs the same flow on bf16 operands.
+#include <algorithm>
+#include <utility>
+
 #include "quant_device.cuh"
 
 namespace kvc {
@@ -40,18 +43,21 @@ namespace {
 constexpr int kThreads = kDecWarps * 32;
 constexpr int kGroupsPerWarp = kGroupsPerCta / kDecWarps;
 constexpr int kSlotsPerWarp = kWinSlotsPerCta / kDecWarps;
-static_assert(kSlotsPerWarp == 16 || kSlotsPerWarp == 32, "window warps take 16 or 32 slots");
+static_assert(kSlotsPerWarp == 32, "window warps take 32 slots");
 constexpr unsigned kWaitLimit = 1u << 20;   // bounded mbarrier polls (far above any copy)
 static_assert(kGroupsPerWarp <= 8, "the key zero-point product covers at most 8 groups");
 
 struct DecLayer {
-  int n_groups;     // packed groups read by the packed CTAs (a group flushed here excluded)
+  int n_groups;     // packed groups read from the store (a group flushed here excluded)
   int win_start;    // ring start slot after this launch's append
   int win_len;      // window tokens after this launch's append
-  int n_pctas, n_ctas, cta_begin, cap_groups;
+  int n_ctas;       // CTAs per unit
+  int cta_begin;    // first CTA of the layer in the grid
+  int cap_groups;
   int new_slot;     // ring slot of the token appended in this launch, or -1
   int flush_start;  // ring slot of the oldest token when this launch flushes a group, or -1
-  int pad;
+  int wchunks;      // window chunks (32 slots) per unit; packed chunks (4 groups) follow
+  int cpc;          // chunks per CTA
   long long packed_off;
 };
 
@@ -79,7 +85,7 @@ __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__
 
 __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -88,7 +94,7 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
 
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -116,442 +122,454 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Stage up to two contiguous global ranges into shared memory (whole warp calls).
+// The warp's barrier was initialised at kernel start; `phase` counts its uses.
 // Returns false if the wait gave up (error word set; a second bounded wait lets
 // copies still in flight land before the CTA can exit).
-__device__ bool warp_stage(uint64_t* bar, void* dst0, const void* src0, uint32_t bytes0,
-                           void* dst1, const void* src1, uint32_t bytes1, unsigned* err) {
+__device__ bool warp_stage(uint64_t* bar, unsigned phase, void* dst0, const void* src0,
+                           uint32_t bytes0, void* dst1, const void* src1, uint32_t bytes1,
+                           unsigned* err) {
   const int lane = threadIdx.x & 31;
+  __syncwarp();   // every lane is done reading the buffer's previous contents
   if (lane == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" :: "r"(smem_u32(bar)) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  }
-  __syncwarp();
-  if (lane == 0) {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
                  :: "r"(smem_u32(bar)), "r"(bytes0 + bytes1) : "memory");
     bulk_g2s(dst0, src0, bytes0, bar);
     if (bytes1) bulk_g2s(dst1, src1, bytes1, bar);
   }
+  const unsigned parity = phase & 1u;
   bool done = false;
-  for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(bar, 0);
+  for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(bar, parity);
   if (!done) {
     if (lane == 0) atomicOr(err, 1u);
-    for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(bar, 0);
+    for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(bar, parity);
     done = false;
   }
   __syncwarp();
   return __all_sync(0xffffffffu, done);
 }
 
-// Two codes of pair slot P of a word as an exact fp16 pair (even code low half).
-// The masked field sits at bit BITS*j of a byte under the fp16 exponent of 1024,
-// so the half is 1024 + code * 2^(BITS*j); one fused multiply-add rescales it.
-template <int BITS, int P>
-__device__ __forceinline__ uint32_t unpack_pair(uint32_t w) {
-  constexpr int CPB = 8 / BITS;              // codes per byte
-  constexpr int S = P / CPB, J = P % CPB;
-  constexpr uint32_t mask = (((1u << BITS) - 1u) * 0x00010001u) << (BITS * J);
-  const uint32_t v = ((w >> (8 * S)) & mask) | 0x64006400u;
-  constexpr float sc = 1.0f / (float)(1 << (BITS * J));
-  const __half2 scale = __float2half2_rn(sc);
-  const __half2 bias = __float2half2_rn(-1024.0f * sc);
-  return h2u(__hfma2(u2h(v), scale, bias));
+// ------------------------------------------------------------ fragment helpers
+template <typename F, int... I>
+__device__ __forceinline__ void static_for_impl(F&& f, std::integer_sequence<int, I...>) {
+  (f(std::integral_constant<int, I>{}), ...);
+}
+// f(integral_constant<int, i>) for i = 0 .. N-1, indices known at compile time
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  static_for_impl(f, std::make_integer_sequence<int, N>{});
 }
 
-template <int BITS>
-__device__ __forceinline__ uint32_t unpack_rt(uint32_t w, int p) {
-  // p is a compile-time constant after unrolling; the switch folds away.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held in the operand-fragment
+// layout (lane = 4*row + col/2): afterwards lane 4*r + c/2 holds row r of the
+// transpose.
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// v as an fp16 pair (hi, lo) with hi = fp16(v), lo = fp16(v - hi): hi in the low half.
+__device__ __forceinline__ uint32_t split_f16(float v) {
+  const float hi = __half2float(__float2half_rn(v));
+  return h2u(__floats2half2_rn(v, v - hi));
+}
+__device__ __forceinline__ uint32_t split_bf16(float v) {
+  const float hi = __bfloat162float(__float2bfloat16_rn(v));
+  const __nv_bfloat162 p = __floats2bfloat162_rn(v, v - hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// Exact fp16 pair of the two codes in pair slot P of word w. The field of slot P
+// is masked in place under the fp16 exponent of 2^e, e = 10 - BITS*j (j = field
+// index inside its byte), so each half reads 2^e + code; one subtraction leaves
+// the code.
+template <int BITS, int P>
+__device__ __forceinline__ uint32_t unpack_pair(uint32_t w) {
+  constexpr int CPB = 8 / BITS, SB = P / CPB, J = P % CPB;
+  constexpr uint32_t mask = (((1u << BITS) - 1u) * 0x00010001u) << (BITS * J);
+  constexpr uint32_t mag = ((uint32_t)(25 - BITS * J) << 10) * 0x00010001u;
+  const uint32_t v = ((SB ? (w >> 8) : w) & mask) | mag;
+  return h2u(__hsub2(u2h(v), u2h(mag)));
+}
+
+// A operand of key product (MT, KS) (rows = tokens, k = channels) from the lane's
+// key code words.
+template <int D, int BITS, int MT, int KS>
+__device__ __forceinline__ void key_afrag(const uint32_t* kw, uint32_t (&a)[4]) {
   if constexpr (BITS == 2) {
-    switch (p) {
-      case 0: return unpack_pair<2, 0>(w); case 1: return unpack_pair<2, 1>(w);
-      case 2: return unpack_pair<2, 2>(w); case 3: return unpack_pair<2, 3>(w);
-      case 4: return unpack_pair<2, 4>(w); case 5: return unpack_pair<2, 5>(w);
-      case 6: return unpack_pair<2, 6>(w); default: return unpack_pair<2, 7>(w);
-    }
+    constexpr int wi = MT * (D / 32) + KS / 2, b = 2 * (KS & 1);
+    a[0] = unpack_pair<2, b>(kw[wi]);
+    a[1] = unpack_pair<2, 4 + b>(kw[wi]);
+    a[2] = unpack_pair<2, b + 1>(kw[wi]);
+    a[3] = unpack_pair<2, 5 + b>(kw[wi]);
   } else {
-    switch (p) {
-      case 0: return unpack_pair<4, 0>(w); case 1: return unpack_pair<4, 1>(w);
-      case 2: return unpack_pair<4, 2>(w); default: return unpack_pair<4, 3>(w);
-    }
+    constexpr int wi = MT * (D / 16) + KS;
+    a[0] = unpack_pair<4, 0>(kw[wi]);
+    a[1] = unpack_pair<4, 2>(kw[wi]);
+    a[2] = unpack_pair<4, 1>(kw[wi]);
+    a[3] = unpack_pair<4, 3>(kw[wi]);
+  }
+}
+// A operand of value product (MT, KS) (rows = channels, k = tokens).
+template <int BITS, int MT, int KS>
+__device__ __forceinline__ void value_afrag(const uint32_t* vw, uint32_t (&a)[4]) {
+  if constexpr (BITS == 2) {
+    constexpr int b = 2 * KS;
+    a[0] = unpack_pair<2, b>(vw[MT]);
+    a[1] = unpack_pair<2, 4 + b>(vw[MT]);
+    a[2] = unpack_pair<2, b + 1>(vw[MT]);
+    a[3] = unpack_pair<2, 5 + b>(vw[MT]);
+  } else {
+    constexpr int wi = 2 * MT + KS;
+    a[0] = unpack_pair<4, 0>(vw[wi]);
+    a[1] = unpack_pair<4, 2>(vw[wi]);
+    a[2] = unpack_pair<4, 1>(vw[wi]);
+    a[3] = unpack_pair<4, 3>(vw[wi]);
   }
 }
 
-// Accumulator registers a lane keeps per C fragment: rows gid and gid+8 when both
-// carry data (g = 8: hi rows 0-7, lo rows 8-15), else only row gid (rows 8-15 of
-// the operands are zero for g <= 4, so their results are never kept).
+// Column layout of the B operands: column n of n-tile u belongs to query head
+// 4u + n/2; even columns carry the leading ("hi") fp16/bf16 part of an operand
+// product, odd columns the remainder ("lo"). A lane's C fragment (columns 2tid,
+// 2tid+1) therefore holds both parts for head 4u + tid, and their sum is the
+// full-precision product.
 template <int GQ>
-constexpr int acc_regs() { return GQ == 8 ? 4 : 2; }
+constexpr int n_tiles() { return (GQ + 3) / 4; }
 
 template <int D, int GQ>
 struct WarpState {
-  float m;                       // running max (log2 domain) of this lane's row
-  float l;                       // lane-partial sum of exp2
-  float o[D / 8][acc_regs<GQ>()];  // value accumulators
-  float cz[acc_regs<GQ>()];      // value zero-point accumulators (cols = channel groups)
+  static constexpr int NH = n_tiles<GQ>();
+  float m[NH];                 // running max of the raw logits (head 4u + tid)
+  float l[NH];                 // lane-partial sum of the weights
+  float o[NH][D / 16][4];      // value accumulators: rows = channels, columns = (head, part)
+  float cz[NH][4];             // value zero-point sums: rows = channel groups
 };
-
-// c += A * B on a kept-rows accumulator (rows gid+8 discarded when g <= 4).
-template <int GQ>
-__device__ __forceinline__ void mma_acc(float (&c)[acc_regs<GQ>()], uint32_t a0, uint32_t a1,
-                                        uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1,
-                                        bool bf16 = false);
-
-template <int GQ>
-__device__ __forceinline__ void mma_acc(float (&c)[acc_regs<GQ>()], uint32_t a0, uint32_t a1,
-                                        uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1,
-                                        bool bf16) {
-  if constexpr (GQ == 8) {
-    if (bf16) mma_bf16(c, a0, a1, a2, a3, b0, b1);
-    else mma_f16(c, a0, a1, a2, a3, b0, b1);
-  } else {
-    // rows gid+8 are zero operands: feed zero accumulators, drop their results
-    float d2, d3;
-    if (bf16)
-      asm volatile(
-          "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-          "{%8,%9}, {%10,%11,%12,%12};\n"
-          : "=f"(c[0]), "=f"(c[1]), "=f"(d2), "=f"(d3)
-          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
-            "f"(0.f));
-    else
-      asm volatile(
-          "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-          "{%8,%9}, {%10,%11,%12,%12};\n"
-          : "=f"(c[0]), "=f"(c[1]), "=f"(d2), "=f"(d3)
-          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
-            "f"(0.f));
-  }
-}
-
-// Row gid+8 of an accumulator (zero when it is not kept).
-template <int GQ>
-__device__ __forceinline__ float row8(const float (&c)[acc_regs<GQ>()], int e) {
-  if constexpr (GQ == 8) return c[2 + e];
-  else return 0.f;
-}
 
 template <int D, int GQ>
 __device__ __forceinline__ void state_init(WarpState<D, GQ>& st) {
-  st.m = -INFINITY;
-  st.l = 0.f;
+  constexpr int NH = n_tiles<GQ>();
 #pragma unroll
-  for (int i = 0; i < D / 8; ++i)
+  for (int u = 0; u < NH; ++u) {
+    st.m[u] = -INFINITY;
+    st.l[u] = 0.f;
 #pragma unroll
-    for (int e = 0; e < acc_regs<GQ>(); ++e) st.o[i][e] = 0.f;
+    for (int i = 0; i < D / 16; ++i)
 #pragma unroll
-  for (int e = 0; e < acc_regs<GQ>(); ++e) st.cz[e] = 0.f;
+      for (int e = 0; e < 4; ++e) st.o[u][i][e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.cz[u][e] = 0.f;
+  }
 }
 
-// Row roles of this lane in the 16-row operands.
-template <int GQ>
-struct Roles {
-  bool hi, lo;
-  int head;
-  __device__ explicit Roles(int gid) {
-    if constexpr (GQ == 8) { hi = true; lo = true; head = gid; }
-    else { hi = gid < GQ; lo = gid >= GQ && gid < 2 * GQ; head = gid % GQ; }
-  }
+// Query operands of the packed path: qh = fp16 query pair of this lane's B column
+// (zero beyond the group's heads); qn = -qh in "lo" columns, 0 in "hi" columns.
+template <int D, int GQ>
+struct QRegs {
+  static constexpr int NH = n_tiles<GQ>();
+  uint32_t qh[NH][D / 16][2];
+  uint32_t qn[NH][D / 16][2];
 };
 
-// Online-softmax update from the combined logits x[NT][2] (exp2 weights returned in x).
-template <int D, int GQ, int NT>
-__device__ __forceinline__ void softmax_update(WarpState<D, GQ>& st, float (&x)[NT][2], float sl2) {
-  float tmax = -INFINITY;
+template <int D, int GQ>
+__device__ __forceinline__ void load_qregs(QRegs<D, GQ>& qr, const __nv_bfloat16* qs) {
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int u = 0; u < n_tiles<GQ>(); ++u) {
+    const int h = 4 * u + (gid >> 1);
 #pragma unroll
-    for (int e = 0; e < 2; ++e) { x[nt][e] *= sl2; tmax = fmaxf(tmax, x[nt][e]); }
-  tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-  tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-  const float mnew = fmaxf(st.m, tmax);
-  if (__any_sync(0xffffffffu, mnew > st.m)) {
-    const float corr = (mnew == -INFINITY) ? 1.f : exp2f(st.m - mnew);
-    st.l *= corr;
+    for (int ks = 0; ks < D / 16; ++ks)
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i)
-#pragma unroll
-      for (int e = 0; e < acc_regs<GQ>(); ++e) st.o[i][e] *= corr;
-#pragma unroll
-    for (int e = 0; e < acc_regs<GQ>(); ++e) st.cz[e] *= corr;
-    st.m = mnew;
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int c = 16 * ks + 2 * tid + 8 * e2;
+        float a = 0.f, b = 0.f;
+        if (h < GQ) {
+          a = __bfloat162float(qs[h * D + c]);
+          b = __bfloat162float(qs[h * D + c + 1]);
+        }
+        const __half2 q2 = __floats2half2_rn(a, b);
+        qr.qh[u][ks][e2] = h2u(q2);
+        qr.qn[u][ks][e2] = (gid & 1) ? h2u(__hneg2(q2)) : 0u;
+      }
   }
-  float s = 0.f;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float p = (x[nt][e] == -INFINITY) ? 0.f : exp2f(x[nt][e] - st.m);
-      x[nt][e] = p;
-      s += p;
-    }
-  st.l += s;
 }
 
-// Combine the hi and lo rows of a C fragment into the full per-head value.
-template <int GQ>
-__device__ __forceinline__ float combine_rows(float c_row, float c_row8) {
-  if constexpr (GQ == 8) return c_row + c_row8;
-  else return c_row + __shfl_xor_sync(0xffffffffu, c_row, 4 * GQ);
+// Online-softmax update with the logits of 32 tokens: x[u][mt][r] is token
+// 16mt + gid + 8r for head 4u + tid. The weights replace the logits.
+template <int D, int GQ>
+__device__ __forceinline__ void softmax_update(WarpState<D, GQ>& st, float (&x)[n_tiles<GQ>()][2][2],
+                                               float sl2) {
+#pragma unroll
+  for (int u = 0; u < n_tiles<GQ>(); ++u) {
+    float gm = fmaxf(fmaxf(x[u][0][0], x[u][0][1]), fmaxf(x[u][1][0], x[u][1][1]));
+    gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
+    gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
+    gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
+    const float mnew = fmaxf(st.m[u], gm);
+    if (__any_sync(0xffffffffu, mnew > st.m[u])) {
+      const float corr = (st.m[u] == -INFINITY) ? 0.f : fast_exp2((st.m[u] - mnew) * sl2);
+      st.l[u] *= corr;
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st.o[u][i][e] *= corr;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) st.cz[u][e] *= corr;
+      st.m[u] = mnew;
+    }
+    const float msl = (st.m[u] == -INFINITY) ? 0.f : st.m[u] * sl2;
+    float s = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float p = fast_exp2(fmaf(x[u][mt][r], sl2, -msl));
+        x[u][mt][r] = p;
+        s += p;
+      }
+    st.l[u] += s;
+  }
 }
 
 // ------------------------------------------------------------ packed groups
 // `base` points at n_grp (<= kGroupsPerWarp) consecutive group blocks in shared
-// memory. Two phases: the key logits of every group (independent tensor-core
-// chains, each split over two accumulators), one online-softmax update over all
-// the warp's tokens, then the value products.
+// memory. Per group: key logits (rows = tokens), one online-softmax update, the
+// value products (rows = channels). The group loop stays rolled so that the hot
+// code fits the instruction cache.
 template <int D, int BITS, int GQ>
-__device__ void packed_warp(WarpState<D, GQ>& st, const uint8_t* base, int n_grp,
-                            const __nv_bfloat16* __restrict__ qrow_base, float sl2) {
-  constexpr int KS = D / 16, NTV = D / 8, WPL = D * BITS / 32, PPW = 16 / BITS;
-  constexpr int NGC = D / 32, BB = 8 * D * (BITS + 1), R2 = acc_regs<GQ>();
+__device__ void packed_warp(WarpState<D, GQ>& st, const QRegs<D, GQ>& qr, const uint8_t* base,
+                            int n_grp, float sl2) {
+  constexpr int KS = D / 16, NGC = D / 32, BB = 8 * D * (BITS + 1), WPL = D * BITS / 32;
+  constexpr int NH = n_tiles<GQ>();
   const int lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
-  const Roles<GQ> R(gid);
-  const bool active = R.hi || R.lo;
 
-  // query pairs for this lane's channels, fp16 (exact for bf16 queries in range)
-  __half2 qh[KS][2];
+  // key zero-point sums of every group of the chunk: C[group][n] = Z_group . q_n
+  // (A rows = groups, B = the queries in the "hi" columns)
+  float zb[NH];
   {
-    const __nv_bfloat16* qr = qrow_base + (size_t)R.head * D;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int c = 16 * ks + 2 * tid + 8 * e2;
-        const float a = active ? __bfloat162float(qr[c]) : 0.f;
-        const float b = active ? __bfloat162float(qr[c + 1]) : 0.f;
-        qh[ks][e2] = __floats2half2_rn(a, b);
-      }
-  }
-  // key zero-point sums for all the warp's groups: C[row][col] = q_row . Z_{col}
-  float zb0, zb1;
-  {
+    uint32_t za[KS][2];
     const int gz = gid < n_grp ? gid : 0;
     const uint4* zp = reinterpret_cast<const uint4*>(base + (size_t)gz * BB + off_kzero(D, BITS) +
                                                      tid * (D / 4) * 2);
-    float cz4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      const uint4 z = zp[ch];
-      const int ks0 = 2 * ch;
-      mma_f16(cz4, R.hi ? h2u(qh[ks0][0]) : 0u, 0u, R.hi ? h2u(qh[ks0][1]) : 0u, 0u, z.x, z.y);
-      mma_f16(cz4, R.hi ? h2u(qh[ks0 + 1][0]) : 0u, 0u, R.hi ? h2u(qh[ks0 + 1][1]) : 0u, 0u,
-              z.z, z.w);
+    for (int i = 0; i < KS / 2; ++i) {
+      const uint4 z = zp[i];
+      const bool live = gid < n_grp;
+      za[2 * i][0] = live ? z.x : 0u;
+      za[2 * i][1] = live ? z.y : 0u;
+      za[2 * i + 1][0] = live ? z.z : 0u;
+      za[2 * i + 1][1] = live ? z.w : 0u;
     }
-    zb0 = cz4[0];
-    zb1 = cz4[1];
-  }
-
-  // ---- phase 1: key logits of every group
-  float x[kGroupsPerWarp * 4][2];
 #pragma unroll
-  for (int j = 0; j < kGroupsPerWarp; ++j) {
-    if (j >= n_grp) {
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) x[j * 4 + nt][0] = x[j * 4 + nt][1] = -INFINITY;
-      continue;
-    }
-    const int src = gid * 4 + (j >> 1);
-    const float z0 = __shfl_sync(0xffffffffu, zb0, src);
-    const float z1 = __shfl_sync(0xffffffffu, zb1, src);
-    const float bias = (j & 1) ? z1 : z0;
-    const uint8_t* blk = base + (size_t)j * BB;
-    // operand A = hi/lo(q * S) per channel pair
-    uint32_t ak[KS][4];
-    {
-      const uint4* sp = reinterpret_cast<const uint4*>(blk + off_kscale(D, BITS) + tid * (D / 4) * 2);
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        const uint4 s = sp[ch];
-        const uint32_t sv[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int ks = 2 * ch + h;
-#pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            const __half2 S2 = u2h(sv[2 * h + e2]);
-            const __half2 hi = __hmul2(qh[ks][e2], S2);
-            const __half2 lo = __hfma2(qh[ks][e2], S2, __hneg2(hi));
-            if constexpr (GQ == 8) {
-              ak[ks][e2 * 2] = h2u(hi);
-              ak[ks][e2 * 2 + 1] = h2u(lo);
-            } else {
-              ak[ks][e2 * 2] = R.hi ? h2u(hi) : (R.lo ? h2u(lo) : 0u);
-              ak[ks][e2 * 2 + 1] = 0u;
-            }
-          }
-        }
-      }
-    }
-    uint32_t kw[WPL];
-    {
-      const uint4* p = reinterpret_cast<const uint4*>(blk);
-#pragma unroll
-      for (int i = 0; i < WPL / 4; ++i) {
-        const uint4 u = p[i * 32 + lane];
-        kw[4 * i] = u.x; kw[4 * i + 1] = u.y; kw[4 * i + 2] = u.z; kw[4 * i + 3] = u.w;
-      }
-    }
-    float ca[4][R2], cb[4][R2];   // even / odd k-steps: two independent chains
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-      for (int e = 0; e < R2; ++e) { ca[nt][e] = (e < 2) ? bias : 0.f; cb[nt][e] = 0.f; }
+    for (int u = 0; u < NH; ++u) {
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        const int pi = (nt * KS + ks) * 2;
-        const uint32_t b0 = unpack_rt<BITS>(kw[pi / PPW], pi % PPW);
-        const uint32_t b1 = unpack_rt<BITS>(kw[(pi + 1) / PPW], (pi + 1) % PPW);
-        if (ks & 1) mma_acc<GQ>(cb[nt], ak[ks][0], ak[ks][1], ak[ks][2], ak[ks][3], b0, b1);
-        else mma_acc<GQ>(ca[nt], ak[ks][0], ak[ks][1], ak[ks][2], ak[ks][3], b0, b1);
+        const uint32_t b0 = (gid & 1) ? 0u : qr.qh[u][ks][0];
+        const uint32_t b1 = (gid & 1) ? 0u : qr.qh[u][ks][1];
+        mma_f16(c, za[ks][0], 0u, za[ks][1], 0u, b0, b1);
       }
+      zb[u] = c[0];   // group gid, head 4u + tid
     }
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float c8 = 0.f;
-        if constexpr (GQ == 8) c8 = ca[nt][2 + e] + cb[nt][2 + e];
-        x[j * 4 + nt][e] = combine_rows<GQ>(ca[nt][e] + cb[nt][e], c8);
-      }
   }
-  softmax_update<D, GQ, kGroupsPerWarp * 4>(st, x, sl2);
 
-  // ---- phase 2: values
-#pragma unroll
-  for (int j = 0; j < kGroupsPerWarp; ++j) {
-    if (j >= n_grp) continue;
+#pragma unroll 1
+  for (int j = 0; j < n_grp; ++j) {
     const uint8_t* blk = base + (size_t)j * BB;
+    float x[NH][2][2];
+    {
+      // B = hi/lo(q * S_k): one fp16 product, or its rounding remainder
+      uint32_t bq[NH][KS][2];
+      const uint4* sp = reinterpret_cast<const uint4*>(blk + off_kscale(D, BITS) + tid * (D / 4) * 2);
+#pragma unroll
+      for (int i = 0; i < KS / 2; ++i) {
+        const uint4 s4 = sp[i];
+        const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+        for (int u = 0; u < NH; ++u)
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int ks = 2 * i + (h >> 1), e2 = h & 1;
+            const __half2 S2 = u2h(sv[h]);
+            bq[u][ks][e2] = h2u(__hfma2(u2h(qr.qh[u][ks][e2]), S2,
+                                        __hmul2(u2h(qr.qn[u][ks][e2]), S2)));
+          }
+      }
+      uint32_t kw[WPL];
+      {
+        const uint4* p = reinterpret_cast<const uint4*>(blk);
+#pragma unroll
+        for (int i = 0; i < WPL / 4; ++i) {
+          const uint4 w4 = p[i * 32 + lane];
+          kw[4 * i] = w4.x; kw[4 * i + 1] = w4.y; kw[4 * i + 2] = w4.z; kw[4 * i + 3] = w4.w;
+        }
+      }
+      float acc[NH][2][2][4];   // [u][mt][chain][C]: even / odd k-steps
+#pragma unroll
+      for (int u = 0; u < NH; ++u) {
+        const float bias = __shfl_sync(0xffffffffu, zb[u], j * 4 + tid);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[u][mt][0][e] = (e & 1) ? 0.f : bias;
+            acc[u][mt][1][e] = 0.f;
+          }
+      }
+      static_for<2>([&](auto MT_) {
+        constexpr int MT = decltype(MT_)::value;
+        static_for<KS>([&](auto KS_) {
+          constexpr int K = decltype(KS_)::value;
+          uint32_t a[4];
+          key_afrag<D, BITS, MT, K>(kw, a);
+#pragma unroll
+          for (int u = 0; u < NH; ++u)
+            mma_f16(acc[u][MT][K & 1], a[0], a[1], a[2], a[3], bq[u][K][0], bq[u][K][1]);
+        });
+      });
+#pragma unroll
+      for (int u = 0; u < NH; ++u)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          x[u][mt][0] = (acc[u][mt][0][0] + acc[u][mt][0][1]) + (acc[u][mt][1][0] + acc[u][mt][1][1]);
+          x[u][mt][1] = (acc[u][mt][0][2] + acc[u][mt][0][3]) + (acc[u][mt][1][2] + acc[u][mt][1][3]);
+        }
+    }
+    softmax_update<D, GQ>(st, x, sl2);
+
+    // values: o[channel][n] += sum_t code[channel][t] * hi/lo(p_t S_t,gc)[t][n]
     uint32_t vw[WPL];
     {
       const uint4* p = reinterpret_cast<const uint4*>(blk + off_vcodes(D, BITS));
 #pragma unroll
       for (int i = 0; i < WPL / 4; ++i) {
-        const uint4 u = p[i * 32 + lane];
-        vw[4 * i] = u.x; vw[4 * i + 1] = u.y; vw[4 * i + 2] = u.z; vw[4 * i + 3] = u.w;
+        const uint4 w4 = p[i * 32 + lane];
+        vw[4 * i] = w4.x; vw[4 * i + 1] = w4.y; vw[4 * i + 2] = w4.z; vw[4 * i + 3] = w4.w;
       }
     }
-    const uint32_t* vs = reinterpret_cast<const uint32_t*>(blk + off_vscale(D, BITS));
+    const __half* vs = reinterpret_cast<const __half*>(blk + off_vscale(D, BITS));
     const uint32_t* vz = reinterpret_cast<const uint32_t*>(blk + off_vzero(D, BITS));
+    static_for<2>([&](auto KS_) {
+      constexpr int K = decltype(KS_)::value;
+      // scales of this lane's tokens 16K + gid and 16K + gid + 8, all channel groups
+      float S[2][NGC];
 #pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-      // p of tokens 16ks + 2tid + {0,1} and + 8 + {0,1}
-      const float p0 = x[j * 4 + 2 * ks][0], p1 = x[j * 4 + 2 * ks][1];
-      const float p2 = x[j * 4 + 2 * ks + 1][0], p3 = x[j * 4 + 2 * ks + 1][1];
-      const __half2 ph01 = __floats2half2_rn(p0, p1), ph23 = __floats2half2_rn(p2, p3);
-      const __half2 pl01 = __floats2half2_rn(p0 - __low2float(ph01), p1 - __high2float(ph01));
-      const __half2 pl23 = __floats2half2_rn(p2 - __low2float(ph23), p3 - __high2float(ph23));
-      const int P0 = 8 * ks + tid, P1 = P0 + 4;     // token-pair indices
-      {
-        // value zero-points: C[row][gc] += p_row,t * Z_t,gc  (B column gc = gid)
-        const uint32_t bz0 = gid < NGC ? vz[P0 * NGC + gid] : 0u;
-        const uint32_t bz1 = gid < NGC ? vz[P1 * NGC + gid] : 0u;
-        if constexpr (GQ == 8) {
-          mma_acc<GQ>(st.cz, h2u(ph01), h2u(pl01), h2u(ph23), h2u(pl23), bz0, bz1);
-        } else {
-          const uint32_t a0 = R.hi ? h2u(ph01) : (R.lo ? h2u(pl01) : 0u);
-          const uint32_t a2 = R.hi ? h2u(ph23) : (R.lo ? h2u(pl23) : 0u);
-          mma_acc<GQ>(st.cz, a0, 0u, a2, 0u, bz0, bz1);
-        }
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int gc = 0; gc < NGC; ++gc)
+          S[r][gc] = __half2float(vs[vs_index(16 * K + gid + 8 * r, gc, NGC)]);
+      // zero-point sums: rows = channel groups (A = zeros, token pairs), B = hi/lo(p)
+      const uint32_t az0 = gid < NGC ? vz[(8 * K + tid) * NGC + gid] : 0u;
+      const uint32_t az2 = gid < NGC ? vz[(8 * K + 4 + tid) * NGC + gid] : 0u;
+#pragma unroll
+      for (int u = 0; u < NH; ++u) {
+        const uint32_t bz0 = movm_t(split_f16(x[u][K][0]));
+        const uint32_t bz1 = movm_t(split_f16(x[u][K][1]));
+        mma_f16(st.cz[u], az0, 0u, az2, 0u, bz0, bz1);
       }
+      static_for<NGC>([&](auto GC_) {
+        constexpr int GC = decltype(GC_)::value;
 #pragma unroll
-      for (int gc = 0; gc < NGC; ++gc) {
-        const __half2 S01 = u2h(vs[P0 * NGC + gc]);
-        const __half2 S23 = u2h(vs[P1 * NGC + gc]);
-        const __half2 h01 = __hmul2(ph01, S01), h23 = __hmul2(ph23, S23);
-        const __half2 l01 = __hfma2(pl01, S01, __hfma2(ph01, S01, __hneg2(h01)));
-        const __half2 l23 = __hfma2(pl23, S23, __hfma2(ph23, S23, __hneg2(h23)));
-        uint32_t a0, a1, a2, a3;
-        if constexpr (GQ == 8) { a0 = h2u(h01); a1 = h2u(l01); a2 = h2u(h23); a3 = h2u(l23); }
-        else {
-          a0 = R.hi ? h2u(h01) : (R.lo ? h2u(l01) : 0u); a1 = 0u;
-          a2 = R.hi ? h2u(h23) : (R.lo ? h2u(l23) : 0u); a3 = 0u;
+        for (int u = 0; u < NH; ++u) {
+          const uint32_t b0 = movm_t(split_f16(x[u][K][0] * S[0][GC]));
+          const uint32_t b1 = movm_t(split_f16(x[u][K][1] * S[1][GC]));
+          static_for<2>([&](auto H_) {
+            constexpr int MV = 2 * GC + decltype(H_)::value;
+            uint32_t a[4];
+            value_afrag<BITS, MV, K>(vw, a);
+            mma_f16(st.o[u][MV], a[0], a[1], a[2], a[3], b0, b1);
+          });
         }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int nt = gc * 4 + q4;
-          const int pi = (ks * NTV + nt) * 2;
-          const uint32_t b0 = unpack_rt<BITS>(vw[pi / PPW], pi % PPW);
-          const uint32_t b1 = unpack_rt<BITS>(vw[(pi + 1) / PPW], (pi + 1) % PPW);
-          mma_acc<GQ>(st.o[nt], a0, a1, a2, a3, b0, b1);
-        }
-      }
-    }
+      });
+    });
   }
 }
 
 // ------------------------------------------------------------- window slots
-// wk: NS staged key rows [slot][D] (kperm order); wv: NS/2 staged value pair rows
-// [pair][D] of 32-bit words (vperm order); the first n_valid slots are live.
-template <int D, int GQ, int NS>
-__device__ void window_warp(WarpState<D, GQ>& st, const __nv_bfloat16* wk, const uint32_t* wv,
-                            int n_valid, const __nv_bfloat16* __restrict__ qrow_base, float sl2) {
-  constexpr int KS = D / 16, NTV = D / 8, NT = NS / 8, KSV = NS / 16;
+// wk: NS = 32 staged key rows (win_k_index layout); wv: 16 staged value pair rows
+// (win_v_index layout); the first n_valid slots are live. bf16 products, exact
+// queries, hi/lo weights.
+template <int D, int GQ>
+__device__ void window_warp(WarpState<D, GQ>& st, const __nv_bfloat16* qs, const __nv_bfloat16* wk,
+                            const uint32_t* wv, int n_valid, float sl2) {
+  constexpr int KS = D / 16, NH = n_tiles<GQ>();
   const int lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
-  const Roles<GQ> R(gid);
-  // A = q (bf16, exact) in the hi rows only
-  uint32_t aq[KS][2];
+  float x[NH][2][2];
   {
-    const __nv_bfloat16* qr = qrow_base + (size_t)R.head * D;
+    uint32_t bq[NH][KS][2];
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
+    for (int u = 0; u < NH; ++u) {
+      const int h = 4 * u + (gid >> 1);
+      const bool live = h < GQ && !(gid & 1);
 #pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int c = 16 * ks + 2 * tid + 8 * e2;
-        const uint32_t u = *reinterpret_cast<const uint32_t*>(qr + c);
-        aq[ks][e2] = R.hi ? u : 0u;
+      for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2)
+          bq[u][ks][e2] = live ? *reinterpret_cast<const uint32_t*>(qs + h * D + 16 * ks + 2 * tid + 8 * e2)
+                               : 0u;
+    }
+    float acc[NH][2][2][4];
+#pragma unroll
+    for (int u = 0; u < NH; ++u)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) { acc[u][mt][0][e] = 0.f; acc[u][mt][1][e] = 0.f; }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      // rows 16mt + gid (rl 0) and 16mt + gid + 8 (rl 1); 16-byte chunks swizzled by gid
+      const uint4* r0 = reinterpret_cast<const uint4*>(wk + (size_t)(16 * mt + gid) * D);
+      const uint4* r1 = reinterpret_cast<const uint4*>(wk + (size_t)(16 * mt + gid + 8) * D);
+#pragma unroll
+      for (int i = 0; i < KS / 2; ++i) {
+        const int ch = (tid * (KS / 2) + i) ^ gid;
+        const uint4 u0 = r0[ch], u1 = r1[ch];
+#pragma unroll
+        for (int u = 0; u < NH; ++u) {
+          mma_bf16(acc[u][mt][0], u0.x, u1.x, u0.y, u1.y, bq[u][2 * i][0], bq[u][2 * i][1]);
+          mma_bf16(acc[u][mt][1], u0.z, u1.z, u0.w, u1.w, bq[u][2 * i + 1][0], bq[u][2 * i + 1][1]);
+        }
       }
-  }
-  float x[NT][2];
-  {
-    float c[NT][acc_regs<GQ>()], cb[NT][acc_regs<GQ>()];   // even / odd k-steps
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-      for (int e = 0; e < acc_regs<GQ>(); ++e) { c[nt][e] = 0.f; cb[nt][e] = 0.f; }
-      const uint4* kr = reinterpret_cast<const uint4*>(wk + (size_t)(nt * 8 + gid) * D + tid * (D / 4));
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        const uint4 u = kr[ch];
-        mma_acc<GQ>(c[nt], aq[2 * ch][0], 0u, aq[2 * ch][1], 0u, u.x, u.y, true);
-        mma_acc<GQ>(cb[nt], aq[2 * ch + 1][0], 0u, aq[2 * ch + 1][1], 0u, u.z, u.w, true);
-      }
-#pragma unroll
-      for (int e = 0; e < acc_regs<GQ>(); ++e) c[nt][e] += cb[nt][e];
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int u = 0; u < NH; ++u)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float v = combine_rows<GQ>(c[nt][e], row8<GQ>(c[nt], e));
-        const int col = nt * 8 + 2 * tid + e;
-        x[nt][e] = col < n_valid ? v : -INFINITY;
-      }
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float v = (acc[u][mt][0][2 * r] + acc[u][mt][0][2 * r + 1]) +
+                          (acc[u][mt][1][2 * r] + acc[u][mt][1][2 * r + 1]);
+          x[u][mt][r] = (16 * mt + gid + 8 * r) < n_valid ? v : -INFINITY;
+        }
   }
-  softmax_update<D, GQ, NT>(st, x, sl2);
+  softmax_update<D, GQ>(st, x, sl2);
 #pragma unroll
-  for (int ks = 0; ks < KSV; ++ks) {
-    const float p0 = x[2 * ks][0], p1 = x[2 * ks][1], p2 = x[2 * ks + 1][0], p3 = x[2 * ks + 1][1];
-    __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1), h23 = __floats2bfloat162_rn(p2, p3);
-    __nv_bfloat162 l01 = __floats2bfloat162_rn(p0 - __low2float(h01), p1 - __high2float(h01));
-    __nv_bfloat162 l23 = __floats2bfloat162_rn(p2 - __low2float(h23), p3 - __high2float(h23));
-    const uint32_t H01 = *reinterpret_cast<uint32_t*>(&h01), H23 = *reinterpret_cast<uint32_t*>(&h23);
-    const uint32_t L01 = *reinterpret_cast<uint32_t*>(&l01), L23 = *reinterpret_cast<uint32_t*>(&l23);
-    uint32_t a0, a1, a2, a3;
-    if constexpr (GQ == 8) { a0 = H01; a1 = L01; a2 = H23; a3 = L23; }
-    else {
-      a0 = R.hi ? H01 : (R.lo ? L01 : 0u); a1 = 0u;
-      a2 = R.hi ? H23 : (R.lo ? L23 : 0u); a3 = 0u;
+  for (int ks = 0; ks < 2; ++ks) {
+    uint32_t b0[NH], b1[NH];
+#pragma unroll
+    for (int u = 0; u < NH; ++u) {
+      b0[u] = movm_t(split_bf16(x[u][ks][0]));
+      b1[u] = movm_t(split_bf16(x[u][ks][1]));
     }
-    const int P0 = 8 * ks + tid, P1 = P0 + 4;
-    const uint4* v0 = reinterpret_cast<const uint4*>(wv + (size_t)P0 * D + gid * (D / 8));
-    const uint4* v1 = reinterpret_cast<const uint4*>(wv + (size_t)P1 * D + gid * (D / 8));
+    // pair rows 8ks + tid (tokens 16ks + 2tid, +1) and 8ks + 4 + tid; chunks swizzled by tid
+    const uint4* p0 = reinterpret_cast<const uint4*>(wv + (size_t)(8 * ks + tid) * D);
+    const uint4* p1 = reinterpret_cast<const uint4*>(wv + (size_t)(8 * ks + 4 + tid) * D);
 #pragma unroll
-    for (int ch = 0; ch < NTV / 4; ++ch) {
-      const uint4 b0 = v0[ch], b1 = v1[ch];
-      mma_acc<GQ>(st.o[4 * ch + 0], a0, a1, a2, a3, b0.x, b1.x, true);
-      mma_acc<GQ>(st.o[4 * ch + 1], a0, a1, a2, a3, b0.y, b1.y, true);
-      mma_acc<GQ>(st.o[4 * ch + 2], a0, a1, a2, a3, b0.z, b1.z, true);
-      mma_acc<GQ>(st.o[4 * ch + 3], a0, a1, a2, a3, b0.w, b1.w, true);
+    for (int i = 0; i < D / 32; ++i) {
+      const int ch = (gid * (D / 32) + i) ^ tid;
+      const uint4 v0 = p0[ch], v1 = p1[ch];
+      // words: (mt = 2i, rl 0), (2i, rl 1), (2i + 1, rl 0), (2i + 1, rl 1)
+#pragma unroll
+      for (int u = 0; u < NH; ++u) {
+        mma_bf16(st.o[u][2 * i], v0.x, v0.y, v1.x, v1.y, b0[u], b1[u]);
+        mma_bf16(st.o[u][2 * i + 1], v0.z, v0.w, v1.z, v1.w, b0[u], b1[u]);
+      }
     }
   }
 }
@@ -559,39 +577,42 @@ __device__ void window_warp(WarpState<D, GQ>& st, const __nv_bfloat16* wk, const
 // ----------------------------------------------------------- merge helpers
 template <int D, int GQ>
 struct DecSmem {
-  float m[kDecWarps][GQ];
+  float m[kDecWarps][GQ];      // log2-domain running max per warp and head
   float l[kDecWarps][GQ];
   float o[kDecWarps][GQ][D];
-  float bias[kDecWarps][GQ][D / 32];
-  float wt[kDecWarps][GQ];   // CTA merge weights
+  float wt[kDecWarps][GQ];     // CTA merge weights
   float M[GQ], L[GQ];
   int last;
 };
 
-// Write the warp's per-head state (hi + lo rows combined) into shared memory.
+// Write the warp's per-head state (both column parts and the value zero-point
+// sums folded in) into shared memory.
 template <int D, int GQ>
-__device__ void warp_to_smem(WarpState<D, GQ>& st, DecSmem<D, GQ>& sm, int warp) {
-  constexpr int NTV = D / 8;
+__device__ void warp_to_smem(WarpState<D, GQ>& st, DecSmem<D, GQ>& sm, int warp, float sl2) {
+  constexpr int NGC = D / 32, NH = n_tiles<GQ>();
   const int lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
-  const Roles<GQ> R(gid);
-  float l = st.l;
-  l += __shfl_xor_sync(0xffffffffu, l, 1);
-  l += __shfl_xor_sync(0xffffffffu, l, 2);
 #pragma unroll
-  for (int nt = 0; nt < NTV; ++nt) {
-    const float o0 = combine_rows<GQ>(st.o[nt][0], row8<GQ>(st.o[nt], 0));
-    const float o1 = combine_rows<GQ>(st.o[nt][1], row8<GQ>(st.o[nt], 1));
-    if (R.hi) {
-      sm.o[warp][R.head][nt * 8 + 2 * tid] = o0;
-      sm.o[warp][R.head][nt * 8 + 2 * tid + 1] = o1;
+  for (int u = 0; u < NH; ++u) {
+    const int h = 4 * u + tid;
+    float l = st.l[u];
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    float z[NGC];
+    const float zl = st.cz[u][0] + st.cz[u][1];   // channel group gid, head h
+#pragma unroll
+    for (int gc = 0; gc < NGC; ++gc) z[gc] = __shfl_sync(0xffffffffu, zl, gc * 4 + tid);
+    if (h < GQ) {
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        sm.o[warp][h][16 * mt + gid] = st.o[u][mt][0] + st.o[u][mt][1] + z[mt / 2];
+        sm.o[warp][h][16 * mt + gid + 8] = st.o[u][mt][2] + st.o[u][mt][3] + z[mt / 2];
+      }
+      if (gid == 0) {
+        sm.m[warp][h] = st.m[u] == -INFINITY ? -INFINITY : st.m[u] * sl2;
+        sm.l[warp][h] = l;
+      }
     }
-  }
-  const float z0 = combine_rows<GQ>(st.cz[0], row8<GQ>(st.cz, 0));
-  const float z1 = combine_rows<GQ>(st.cz[1], row8<GQ>(st.cz, 1));
-  if (R.hi) {
-    if (2 * tid < D / 32) sm.bias[warp][R.head][2 * tid] = z0;
-    if (2 * tid + 1 < D / 32) sm.bias[warp][R.head][2 * tid + 1] = z1;
-    if (tid == 0) { sm.m[warp][R.head] = st.m; sm.l[warp][R.head] = l; }
   }
 }
 
@@ -608,7 +629,7 @@ constexpr int stage_bytes() {
 }
 template <int D, int BITS, int GQ>
 constexpr int dyn_smem_bytes() {
-  return stage_bytes<D, BITS, GQ>() + block_bytes(D, BITS) + kDecWarps * 8;
+  return stage_bytes<D, BITS, GQ>() + block_bytes(D, BITS) + kDecWarps * 8 + GQ * D * 2;
 }
 
 template <int D, int BITS, int GQ>
@@ -627,6 +648,7 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
   uint8_t* wbuf = dsm + warp * WB;
   uint8_t* fblk = dsm + stage_bytes<D, BITS, GQ>();
   uint64_t* bars = reinterpret_cast<uint64_t*>(fblk + BB);
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(bars + kDecWarps);
 
   // locate (layer, unit, cta index)
   int li = 0;
@@ -639,72 +661,98 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
   const __nv_bfloat16* qrow = q + ((size_t)li * P.units + unit) * GQ * D;
   uint8_t* ubase = packed + Ld.packed_off + (size_t)unit * Ld.cap_groups * BB;
 
+  // the unit's queries, staged once for every warp
+  for (int i = threadIdx.x; i < GQ * D / 8; i += kThreads)
+    reinterpret_cast<uint4*>(qs)[i] = reinterpret_cast<const uint4*>(qrow)[i];
   WarpState<D, GQ> st;
   state_init(st);
-  if (cidx < Ld.n_pctas) {
-    const int g0 = cidx * kGroupsPerCta + warp * kGroupsPerWarp;
-    const int ng = min(kGroupsPerWarp, Ld.n_groups - g0);
-    if (ng > 0 &&
-        warp_stage(&bars[warp], wbuf, ubase + (size_t)g0 * BB, (uint32_t)(ng * BB), nullptr,
-                   nullptr, 0u, P.err))
-      packed_warp<D, BITS, GQ>(st, wbuf, ng, qrow, P.sl2);
-  } else {
-    const int wc = cidx - Ld.n_pctas;
-    const size_t wunit = (size_t)layer * P.units + unit;
-    __nv_bfloat16* wk = win_k + wunit * P.R * D;
-    __nv_bfloat16* wv = win_v + wunit * P.R * D;
-    const bool flush = wc == 0 && Ld.flush_start >= 0;
-    int owner = -1;
-    if (Ld.new_slot >= 0) owner = Ld.win_len == 0 ? 0 : (Ld.win_len - 1) / kWinSlotsPerCta;
-    const __nv_bfloat16* kn = P.k_new + ((size_t)li * P.units + unit) * D;
-    const __nv_bfloat16* vn = P.v_new + ((size_t)li * P.units + unit) * D;
-    if (wc == owner)
+  if (lane == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" :: "r"(smem_u32(&bars[warp])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncwarp();
+  unsigned phase = 0;
+  const size_t wunit = (size_t)layer * P.units + unit;
+  __nv_bfloat16* wk = win_k + wunit * P.R * D;
+  __nv_bfloat16* wv = win_v + wunit * P.R * D;
+  const bool flush = cidx == 0 && Ld.flush_start >= 0;
+  const __nv_bfloat16* kn = P.k_new + ((size_t)li * P.units + unit) * D;
+  const __nv_bfloat16* vn = P.v_new + ((size_t)li * P.units + unit) * D;
+  // the new token: window chunk holding it (-1 if it left the window with a flush); the
+  // CTA covering that chunk (CTA 0 after a flush) stores it into the ring
+  int new_chunk = -1;
+  if (Ld.new_slot >= 0) {
+    new_chunk = Ld.win_len > 0 ? (Ld.win_len - 1) / kSlotsPerWarp : -1;
+    const int owner = new_chunk >= 0 ? new_chunk / Ld.cpc : 0;
+    if (cidx == owner)
       for (int c = threadIdx.x; c < D; c += kThreads)
         window_store(wk, wv, Ld.new_slot, c, D, kn[c], vn[c]);
-    if (flush) {
-      // quantize the oldest group of the window into a new packed block
-      __syncthreads();
-      GroupSmem<D, kThreads>& gs = *reinterpret_cast<GroupSmem<D, kThreads>*>(dsm);
-      for (int i = threadIdx.x; i < KVC_GROUP * D; i += kThreads) {
-        const int t = i / D, c = i % D;
-        gs.k[t][c] = __bfloat162float(window_load_k(wk, Ld.flush_start + t, c, D));
-        gs.v[t][c] = __bfloat162float(window_load_v(wv, Ld.flush_start + t, c, D));
-      }
-      __syncthreads();
-      quantize_block<D, BITS, kThreads>(gs, fblk);
-      __syncthreads();
-      uint4* dst = reinterpret_cast<uint4*>(ubase + (size_t)Ld.n_groups * BB);
-      const uint4* src = reinterpret_cast<const uint4*>(fblk);
-      for (int i = threadIdx.x; i < BB / 16; i += kThreads) dst[i] = src[i];
-      __syncthreads();   // the staging area is reused by the window copies below
+  }
+  __syncthreads();   // queries staged
+  QRegs<D, GQ> qr;
+  load_qregs<D, GQ>(qr, qs);
+  if (flush) {
+    // quantize the oldest group of the window into a new packed block (the new token
+    // belongs to it only when R == 32, and then this CTA stored it above)
+    __syncthreads();
+    GroupSmem<D, kThreads>& gs = *reinterpret_cast<GroupSmem<D, kThreads>*>(dsm);
+    for (int i = threadIdx.x; i < KVC_GROUP * D; i += kThreads) {
+      const int t = i / D, c = i % D;
+      gs.k[t][c] = __bfloat162float(window_load_k(wk, Ld.flush_start + t, c, D));
+      gs.v[t][c] = __bfloat162float(window_load_v(wv, Ld.flush_start + t, c, D));
     }
-    const int pos0 = wc * kWinSlotsPerCta + warp * kSlotsPerWarp;
+    __syncthreads();
+    quantize_block<D, BITS, kThreads>(gs, fblk);
+    __syncthreads();
+    uint4* dst = reinterpret_cast<uint4*>(ubase + (size_t)Ld.n_groups * BB);
+    const uint4* src = reinterpret_cast<const uint4*>(fblk);
+    for (int i = threadIdx.x; i < BB / 16; i += kThreads) dst[i] = src[i];
+    __syncthreads();   // the staging area is reused by the copies below
+    if (warp == 0) packed_warp<D, BITS, GQ>(st, qr, fblk, 1, P.sl2);
+  }
+  // this CTA's chunks of the unit, round robin over the warps
+  const int total = Ld.wchunks + (Ld.n_groups + kGroupsPerWarp - 1) / kGroupsPerWarp;
+  const int cb = cidx * Ld.cpc, ce = min(cb + Ld.cpc, total);
+  const int wend = min(ce, Ld.wchunks);
+  bool ok = true;
+  for (int ch = cb + warp; ch < wend; ch += kDecWarps) {
+    const int pos0 = ch * kSlotsPerWarp;
     const int n_valid = min(kSlotsPerWarp, Ld.win_len - pos0);
-    if (n_valid > 0) {
-      const int slot0 = (Ld.win_start + pos0) % P.R;
-      __nv_bfloat16* sk = reinterpret_cast<__nv_bfloat16*>(wbuf);
-      uint32_t* sv = reinterpret_cast<uint32_t*>(wbuf + kSlotsPerWarp * D * 2);
-      if (warp_stage(&bars[warp], sk, wk + (size_t)slot0 * D, (uint32_t)(kSlotsPerWarp * D * 2),
-                     sv, wv + (size_t)(slot0 >> 1) * D * 2, (uint32_t)(kSlotsPerWarp * D * 2),
-                     P.err)) {
-        if (wc == owner && Ld.new_slot >= slot0 && Ld.new_slot < slot0 + kSlotsPerWarp) {
-          // the new token was stored through the generic path in this launch: take it
-          // from the inputs rather than from the asynchronous copy
-          const int r = Ld.new_slot - slot0;
-          __nv_bfloat16* svh = reinterpret_cast<__nv_bfloat16*>(sv);
-          for (int c = lane; c < D; c += 32) {
-            sk[(size_t)r * D + kperm(c, D)] = kn[c];
-            svh[((size_t)(r >> 1) * D + vperm(c, D)) * 2 + (r & 1)] = vn[c];
-          }
-          __syncwarp();
-        }
-        window_warp<D, GQ, kSlotsPerWarp>(st, sk, sv, n_valid, qrow, P.sl2);
+    const int slot0 = (Ld.win_start + pos0) % P.R;
+    __nv_bfloat16* sk = reinterpret_cast<__nv_bfloat16*>(wbuf);
+    uint32_t* sv = reinterpret_cast<uint32_t*>(wbuf + kSlotsPerWarp * D * 2);
+    ok = warp_stage(&bars[warp], phase++, sk, wk + (size_t)slot0 * D,
+                    (uint32_t)(kSlotsPerWarp * D * 2), sv, wv + (size_t)(slot0 >> 1) * D * 2,
+                    (uint32_t)(kSlotsPerWarp * D * 2), P.err);
+    if (!ok) break;
+    if (ch == new_chunk) {
+      // the new token was stored through the generic path in this launch: take it
+      // from the inputs rather than from the asynchronous copy
+      const int r = Ld.new_slot - slot0;
+      __nv_bfloat16* svh = reinterpret_cast<__nv_bfloat16*>(sv);
+      for (int c = lane; c < D; c += 32) {
+        sk[win_k_index(r, c, D)] = kn[c];
+        svh[win_v_index(r, c, D)] = vn[c];
       }
+      __syncwarp();
     }
-    if (flush && warp == 0) packed_warp<D, BITS, GQ>(st, fblk, 1, qrow, P.sl2);
+    window_warp<D, GQ>(st, qs, sk, sv, n_valid, P.sl2);
+  }
+  // packed chunks continue the round robin where the window chunks left off
+  if (ok) {
+    const int first = max(cb, Ld.wchunks);
+    int ch = first + ((warp - (first - cb)) % kDecWarps + kDecWarps) % kDecWarps;
+    for (; ch < ce; ch += kDecWarps) {
+      const int g0 = (ch - Ld.wchunks) * kGroupsPerWarp;
+      const int ng = min(kGroupsPerWarp, Ld.n_groups - g0);
+      if (!warp_stage(&bars[warp], phase++, wbuf, ubase + (size_t)g0 * BB,
+                      (uint32_t)(ng * BB), nullptr, nullptr, 0u, P.err))
+        break;
+      packed_warp<D, BITS, GQ>(st, qr, wbuf, ng, P.sl2);
+    }
   }
   __syncthreads();   // every warp is done with the staging area
-  warp_to_smem<D, GQ>(st, sm, warp);
+  warp_to_smem<D, GQ>(st, sm, warp, P.sl2);
   __syncthreads();
 
   // merge the CTA's warps into one partial: part[cta][head][0..D+1] = (m, l, o[D]);
@@ -723,12 +771,24 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
     sm.L[r] = L;
   }
   __syncthreads();
+  if (Ld.n_ctas == 1) {
+    // the whole unit ran in this CTA: no partials to merge
+    float* o = out + ((size_t)li * P.units + unit) * GQ * D;
+    for (int i = threadIdx.x; i < GQ * D; i += kThreads) {
+      const int r = i / D, cch = i % D;
+      float O = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) O += sm.o[w][r][cch] * sm.wt[w][r];
+      o[(size_t)r * D + cch] = O / sm.L[r];
+    }
+    return;
+  }
   float* mypart = part + (size_t)blockIdx.x * GQ * (D + 2);
   for (int i = threadIdx.x; i < GQ * D; i += kThreads) {
     const int r = i / D, cch = i % D;
     float O = 0.f;
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) O += (sm.o[w][r][cch] + sm.bias[w][r][cch / 32]) * sm.wt[w][r];
+    for (int w = 0; w < kDecWarps; ++w) O += sm.o[w][r][cch] * sm.wt[w][r];
     mypart[r * (D + 2) + 2 + cch] = O;
     if (cch == 0) { mypart[r * (D + 2)] = sm.M[r]; mypart[r * (D + 2) + 1] = sm.L[r]; }
   }
@@ -834,6 +894,40 @@ cudaError_t launch_g(const DecParams& P, int ctas, const kvc_cache* c, const __n
   }
 }
 
+// CTAs of the decode kernel that fit on the device at once.
+int resident_ctas(const kvc_cache* c) {
+  static int cached[64][2][2][4] = {};
+  int dev = 0, n_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 456;
+  const int di = c->dims.head_dim == 128, bi = c->dims.bits == 4;
+  const int gi = c->g == 1 ? 0 : c->g == 2 ? 1 : c->g == 4 ? 2 : 3;
+  int& v = cached[dev][di][bi][gi];
+  if (v) return v;
+  int per = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+#define KVC_OCC(DD, BB2, GG)                                                                  \
+  if (e == cudaSuccess) {                                                                     \
+    e = cudaFuncSetAttribute(decode_kernel<DD, BB2, GG>,                                      \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,                     \
+                             dyn_smem_bytes<DD, BB2, GG>());                                  \
+    if (e == cudaSuccess)                                                                     \
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_kernel<DD, BB2, GG>,     \
+                                                        kThreads, dyn_smem_bytes<DD, BB2, GG>()); \
+  }
+#define KVC_OCC_G(DD, BB2)                                                            \
+  switch (c->g) {                                                                      \
+    case 1: KVC_OCC(DD, BB2, 1) break; case 2: KVC_OCC(DD, BB2, 2) break;              \
+    case 4: KVC_OCC(DD, BB2, 4) break; default: KVC_OCC(DD, BB2, 8) break;             \
+  }
+  if (c->dims.head_dim == 128) { if (c->dims.bits == 2) { KVC_OCC_G(128, 2) } else { KVC_OCC_G(128, 4) } }
+  else { if (c->dims.bits == 2) { KVC_OCC_G(64, 2) } else { KVC_OCC_G(64, 4) } }
+#undef KVC_OCC_G
+#undef KVC_OCC
+  if (e != cudaSuccess || per < 1) { cudaGetLastError(); per = 1; }
+  v = n_sm * per;
+  return v;
+}
+
 // Shared host path: a non-null k_new selects the fused append + flush + attention.
 cudaError_t launch_common(const kvc_cache* c, int layer_begin, int layer_count,
                           const __nv_bfloat16* q, const __nv_bfloat16* k_new,
@@ -862,7 +956,6 @@ cudaError_t launch_common(const kvc_cache* c, int layer_begin, int layer_count,
       L.n_groups = ls.n_groups;
       L.cap_groups = ls.cap_groups;
       L.packed_off = (long long)ls.packed_off;
-      L.pad = 0;
       bool flush = false;
       if (appending) {
         flush = flush_flags[base + i] != 0;
@@ -876,10 +969,31 @@ cudaError_t launch_common(const kvc_cache* c, int layer_begin, int layer_count,
         L.win_start = ls.win_start;
         L.win_len = ls.win_len;
       }
-      L.n_pctas = packed_ctas(ls.n_groups);
-      int wctas = window_ctas(L.win_len);
-      if (flush && wctas == 0) wctas = 1;
-      L.n_ctas = L.n_pctas + wctas;
+      L.wchunks = (L.win_len + kSlotsPerWarp - 1) / kSlotsPerWarp;
+      L.cta_begin = 0;
+      L.n_ctas = 0;
+      L.cpc = 0;
+    }
+    // chunks per CTA: the smallest multiple of the warp count that keeps the whole
+    // grid resident in one wave
+    const int capacity = resident_ctas(c);
+    int cpc = kDecWarps;
+    for (;;) {
+      ctas = 0;
+      for (int i = 0; i < cnt; ++i) {
+        const DecLayer& L = P.L[i];
+        const int chunks = L.wchunks + (L.n_groups + kGroupsPerWarp - 1) / kGroupsPerWarp;
+        ctas += units * std::max(1, (chunks + cpc - 1) / cpc);
+      }
+      if (ctas <= capacity || cpc >= 1024) break;
+      cpc += kDecWarps;
+    }
+    ctas = 0;
+    for (int i = 0; i < cnt; ++i) {
+      DecLayer& L = P.L[i];
+      const int chunks = L.wchunks + (L.n_groups + kGroupsPerWarp - 1) / kGroupsPerWarp;
+      L.cpc = cpc;
+      L.n_ctas = std::max(1, (chunks + cpc - 1) / cpc);
       L.cta_begin = ctas;
       ctas += units * L.n_ctas;
     }

@@ -5,16 +5,21 @@
 //   packed store  one 32-token "group block" after another, per (layer, b, kv head):
 //     [K codes  D*4*BITS bytes][V codes  D*4*BITS bytes]
 //     [K scale  D fp16][K zero  D fp16]          per-channel key groups
-//     [V scale  32*(D/32) fp16][V zero  ...]     per-token value groups, [pair][gc][2]
+//     [V scale  32*(D/32) fp16][V zero  ...]     per-token value groups: scales
+//                                                [t][gc], zeros [pair][gc][2]
 //   The code words are laid out so that lane l of a warp reading words
-//   (wi/4)*128 + l*4 + wi%4 holds exactly the B-operand fragments of the
-//   m16n8k16 tensor-core products the decode kernel issues (keys: k = channel,
-//   n = token; values: k = token, n = channel), two codes per 16-bit half pair.
-//   Key scales/zeros are stored in the order the A-operand lanes consume them.
+//   (wi/4)*128 + l*4 + wi%4 holds exactly the A-operand fragments of the
+//   m16n8k16 tensor-core products the decode kernel issues (keys: rows = tokens,
+//   k = channels; values: rows = channels, k = tokens), two codes per 16-bit half
+//   pair. Pair slots are arranged so that the bit position of a code depends only
+//   on the operand's k index (see key_pair / value_pair).
+//   Key scales/zeros are stored in the order the operand lanes consume them.
 //
 //   window        bf16 ring of R slots per (layer, b, kv head):
-//     keys   [R][D]     channels permuted (kperm) into fragment order
-//     values [R/2][D][2] token pairs interleaved, channels permuted (vperm)
+//     keys   [R][D]     channels permuted (kperm) into fragment order, 16-byte
+//                       chunks of a row XOR-swizzled by (slot & 7)
+//     values [R/2][D][2] token pairs interleaved, channels permuted (vperm),
+//                       16-byte chunks of a pair row XOR-swizzled by (pair & 3)
 //
 // Every layout map below is used by the writer (quantize / append), the reader
 // (decode) and the exporter, so they cannot drift apart.
@@ -48,11 +53,13 @@ __host__ __device__ constexpr int vperm(int c, int D) {
   return (c & 7) * (D >> 3) + (c >> 3);
 }
 
-// Index (in fp16 units) of the value scale/zero of (token t, channel group gc)
-// inside its section: token pairs interleaved, so (t, t+1) of one gc form a half2.
+// Index (in fp16 units) of the value zero of (token t, channel group gc) inside
+// its section: token pairs interleaved, so (t, t+1) of one gc form a half2.
 __host__ __device__ constexpr int vsz_index(int t, int gc, int ngc) {
   return ((t >> 1) * ngc + gc) * 2 + (t & 1);
 }
+// Index of the value scale of (token t, channel group gc): token-major.
+__host__ __device__ constexpr int vs_index(int t, int gc, int ngc) { return t * ngc + gc; }
 
 // Bytes of one 32-token group block.
 __host__ __device__ constexpr int block_bytes(int D, int bits) { return 8 * D * (bits + 1); }
@@ -66,37 +73,78 @@ struct CodePos {
 // Words of one section a lane owns (D*BITS/32) and pairs per word (16/BITS).
 __host__ __device__ constexpr int words_per_lane(int D, int bits) { return D * bits / 32; }
 
-__host__ __device__ inline CodePos word_pos(int lane, int pi, int bits) {
-  int ppw = 16 / bits;
-  int wi = pi / ppw, p = pi % ppw;
-  CodePos cp;
-  cp.word = (wi >> 2) * 128 + lane * 4 + (wi & 3);
-  cp.bit = bits * p;
-  return cp;
+// Bit of pair slot P inside each 16-bit half of a word: slot P sits in byte
+// P / (8/bits) at field P % (8/bits).
+__host__ __device__ constexpr int pair_bit(int P, int bits) {
+  return 8 * (P / (8 / bits)) + bits * (P % (8 / bits));
 }
+
+// Fragment coordinates of a pair slot. For product (mt, ks) and A register
+// r = 2*rh + rl: keys cover token 16mt + gid + 8rl and channels 16ks + 2tid + 8rh
+// + {0,1}; values cover channel 16mt + gid + 8rl and tokens 16ks + 2tid + 8rh +
+// {0,1}. Word and slot of register (mt, ks, rl, rh):
+//   keys   2-bit: word mt*(D/32) + ks/2, slot 4rl + 2(ks&1) + rh
+//          4-bit: word mt*(D/16) + ks,   slot 2rl + rh
+//   values 2-bit: word mt,               slot 4rl + 2ks + rh
+//          4-bit: word 2mt + ks,         slot 2rl + rh
+// so the field of a code (slot % (8/bits)) depends only on its k index.
+struct FragPos { int mt, ks, rl, rh; };
+
+__host__ __device__ inline FragPos key_frag(int wi, int P, int D, int bits) {
+  const int KS = D >> 4;
+  FragPos f;
+  if (bits == 2) { f.mt = wi / (KS >> 1); f.ks = 2 * (wi % (KS >> 1)) + ((P >> 1) & 1); f.rl = P >> 2; }
+  else { f.mt = wi / KS; f.ks = wi % KS; f.rl = P >> 1; }
+  f.rh = P & 1;
+  return f;
+}
+__host__ __device__ inline FragPos value_frag(int wi, int P, int bits) {
+  FragPos f;
+  if (bits == 2) { f.mt = wi; f.ks = (P >> 1) & 1; f.rl = P >> 2; }
+  else { f.mt = wi >> 1; f.ks = wi & 1; f.rl = P >> 1; }
+  f.rh = P & 1;
+  return f;
+}
+
+__host__ __device__ inline int word_addr(int lane, int wi) { return (wi >> 2) * 128 + lane * 4 + (wi & 3); }
 
 // Key code of (token t in the group, channel c).
 __host__ __device__ inline CodePos kcode_pos(int t, int c, int D, int bits) {
-  int nt = t >> 3, gid = t & 7;
-  int ks = c >> 4, r = c & 15;
-  int tid = (r & 7) >> 1, odd = r & 1, half = r >> 3;
-  int lane = gid * 4 + tid;
-  int pi = (nt * (D >> 4) + ks) * 2 + half;
-  CodePos cp = word_pos(lane, pi, bits);
-  cp.bit += odd ? 16 : 0;
+  const int mt = t >> 4, rl = (t >> 3) & 1, gid = t & 7;
+  const int ks = c >> 4, rh = (c >> 3) & 1, tid = (c & 7) >> 1, odd = c & 1;
+  const int KS = D >> 4;
+  int wi, P;
+  if (bits == 2) { wi = mt * (KS >> 1) + (ks >> 1); P = 4 * rl + 2 * (ks & 1) + rh; }
+  else { wi = mt * KS + ks; P = 2 * rl + rh; }
+  CodePos cp;
+  cp.word = word_addr(gid * 4 + tid, wi);
+  cp.bit = pair_bit(P, bits) + (odd ? 16 : 0);
   return cp;
 }
 
 // Value code of (token t in the group, channel c).
 __host__ __device__ inline CodePos vcode_pos(int t, int c, int D, int bits) {
-  int ks = t >> 4, r = t & 15;
-  int tid = (r & 7) >> 1, odd = r & 1, half = r >> 3;
-  int nt = c >> 3, gid = c & 7;
-  int lane = gid * 4 + tid;
-  int pi = (ks * (D >> 3) + nt) * 2 + half;
-  CodePos cp = word_pos(lane, pi, bits);
-  cp.bit += odd ? 16 : 0;
+  (void)D;
+  const int ks = t >> 4, rh = (t >> 3) & 1, tid = (t & 7) >> 1, odd = t & 1;
+  const int mt = c >> 4, rl = (c >> 3) & 1, gid = c & 7;
+  int wi, P;
+  if (bits == 2) { wi = mt; P = 4 * rl + 2 * ks + rh; }
+  else { wi = 2 * mt + ks; P = 2 * rl + rh; }
+  CodePos cp;
+  cp.word = word_addr(gid * 4 + tid, wi);
+  cp.bit = pair_bit(P, bits) + (odd ? 16 : 0);
   return cp;
+}
+
+// Window ring positions (bf16 element index inside one unit's ring).
+__host__ __device__ inline int win_k_index(int slot, int c, int D) {
+  const int pos = kperm(c, D);
+  return slot * D + ((((pos >> 3) ^ (slot & 7)) << 3) | (pos & 7));
+}
+__host__ __device__ inline int win_v_index(int slot, int c, int D) {
+  const int w = vperm(c, D);
+  const int ws = (((w >> 2) ^ ((slot >> 1) & 3)) << 2) | (w & 3);
+  return ((slot >> 1) * D + ws) * 2 + (slot & 1);
 }
 
 // Section offsets inside a block (bytes).

@@ -151,7 +151,7 @@ export_kernel(const uint8_t* __restrict__ packed, int cap_groups, int n_groups, 
   for (int i = threadIdx.x; i < KVC_GROUP * NGC; i += kThreads) {
     const int t = i / NGC, gc = i % NGC;
     const size_t o = ((size_t)unit * T + (size_t)j * KVC_GROUP) * NGC + i;
-    if (dst.v_scale) reinterpret_cast<__half*>(dst.v_scale)[o] = vS[vsz_index(t, gc, NGC)];
+    if (dst.v_scale) reinterpret_cast<__half*>(dst.v_scale)[o] = vS[vs_index(t, gc, NGC)];
     if (dst.v_zero) reinterpret_cast<__half*>(dst.v_zero)[o] = vZ[vsz_index(t, gc, NGC)];
   }
 }

@@ -95,7 +95,7 @@ __device__ void quantize_block(GroupSmem<D, NT>& s, uint8_t* __restrict__ blk) {
 #pragma unroll
     for (int j = 0; j < PER; ++j)
       s.vc[vt][vgc * KVC_GROUP + part * PER + j] = (uint8_t)quant_code(vrow[j], Zf, Sf, BITS);
-    if (part == 0) { vS[vsz_index(vt, vgc, NGC)] = S; vZ[vsz_index(vt, vgc, NGC)] = Z; }
+    if (part == 0) { vS[vs_index(vt, vgc, NGC)] = S; vZ[vsz_index(vt, vgc, NGC)] = Z; }
   }
   __syncthreads();
   // pack code words in fragment order
@@ -112,41 +112,39 @@ __device__ void quantize_block(GroupSmem<D, NT>& s, uint8_t* __restrict__ blk) {
     const int gid = lane >> 2, tid = lane & 3;
     uint32_t word = 0;
 #pragma unroll
-    for (int p = 0; p < PPW; ++p) {
-      const int pi = wi * PPW + p;
-      const int half = pi & 1, q = pi >> 1;
+    for (int P = 0; P < PPW; ++P) {
       uint32_t ce, co;
       if (!is_v) {
-        const int nt = q / (D / 16), ks = q % (D / 16);
-        const int t = nt * 8 + gid, c = 16 * ks + 2 * tid + 8 * half;
+        const FragPos f = key_frag(wi, P, D, BITS);
+        const int t = 16 * f.mt + gid + 8 * f.rl, c = 16 * f.ks + 2 * tid + 8 * f.rh;
         ce = s.kc[t][c]; co = s.kc[t][c + 1];
       } else {
-        const int ks = q / (D / 8), nt = q % (D / 8);
-        const int t = 16 * ks + 2 * tid + 8 * half, c = 8 * nt + gid;
+        const FragPos f = value_frag(wi, P, BITS);
+        const int t = 16 * f.ks + 2 * tid + 8 * f.rh, c = 16 * f.mt + gid + 8 * f.rl;
         ce = s.vc[t][c]; co = s.vc[t + 1][c];
       }
-      word |= ce << (BITS * p);
-      word |= co << (16 + BITS * p);
+      word |= ce << pair_bit(P, BITS);
+      word |= co << (16 + pair_bit(P, BITS));
     }
     (is_v ? vw : kw)[w] = word;
   }
 }
 
-// Window ring rows: keys permuted by kperm, values in token pairs permuted by vperm.
+// Window ring rows (layout maps win_k_index / win_v_index).
 __device__ __forceinline__ void window_store(__nv_bfloat16* __restrict__ wk,
                                              __nv_bfloat16* __restrict__ wv, int slot, int c, int D,
                                              __nv_bfloat16 kval, __nv_bfloat16 vval) {
-  wk[(size_t)slot * D + kperm(c, D)] = kval;
-  wv[((size_t)(slot >> 1) * D + vperm(c, D)) * 2 + (slot & 1)] = vval;
+  wk[win_k_index(slot, c, D)] = kval;
+  wv[win_v_index(slot, c, D)] = vval;
 }
 
 __device__ __forceinline__ __nv_bfloat16 window_load_k(const __nv_bfloat16* wk, int slot, int c,
                                                        int D) {
-  return wk[(size_t)slot * D + kperm(c, D)];
+  return wk[win_k_index(slot, c, D)];
 }
 __device__ __forceinline__ __nv_bfloat16 window_load_v(const __nv_bfloat16* wv, int slot, int c,
                                                        int D) {
-  return wv[((size_t)(slot >> 1) * D + vperm(c, D)) * 2 + (slot & 1)];
+  return wv[win_v_index(slot, c, D)];
 }
 
 }  // namespace kvc
