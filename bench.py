@@ -210,15 +210,20 @@ def kernel_hash(name):
 
 
 def profiled_traffic(kernel_file):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source
-    is unchanged since the capture (else None)."""
+    """DRAM bytes per launch of the dominant kernel, from the committed ncu summary
+    `profiles/<kernel file stem>_traffic.txt` ("key: value" lines), if the kernel
+    source is unchanged since the capture (else None)."""
+    stem = os.path.splitext(kernel_file)[0]
     try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            t = json.load(f)
-        e = t[kernel_file]
-        if e["source_sha256_16"] != kernel_hash(kernel_file):
+        vals = {}
+        with open(os.path.join(ROOT, "profiles", f"{stem}_traffic.txt")) as f:
+            for line in f:
+                if ":" in line and not line.lstrip().startswith("#"):
+                    k, v = line.split(":", 1)
+                    vals[k.strip()] = v.strip()
+        if vals.get("source_sha256_16") != kernel_hash(kernel_file):
             return None
-        return e
+        return {"dram_bytes_per_launch": float(vals["dram_bytes_per_launch"])}
     except Exception:
         return None
 
