@@ -181,17 +181,20 @@ kvc_status kvc_append_layers(kvc_cache* cache, int32_t layer_begin, int32_t laye
  *   blog "Measured on a real model" (exact window, rounded rest).
  *   q:   device bf16 [layer_count][batch][n_q_heads][head_dim].
  *   out: device fp32 [layer_count][batch][n_q_heads][head_dim] (written).
- *   Query head j reads kv head j / g. Split-K over the packed store and the
- *   window, merged with a log-sum-exp combine inside the same launch.
+ *   Query head j reads kv head j / g. The token axis of each (sequence, kv
+ *   head) is split over warps of one CTA and merged with a log-sum-exp combine
+ *   inside the same launch.
  *   Errors: KVC_E_STATE (a layer not prefilled), KVC_E_ARG, KVC_E_CUDA.
  * ------------------------------------------------------------------------- */
 kvc_status kvc_decode_attn(kvc_cache* cache, int32_t layer_begin, int32_t layer_count,
                            const void* q, float* out, void* stream);
 
 /* kvc_decode_step -- one decode step of Algorithm 1 on layers [layer_begin,
- * +layer_count) in ONE launch: append k_new/v_new (as kvc_append_layers, with
- * the group flush when the window reaches R) and attend q (as kvc_decode_attn);
- * the results equal those two calls made in sequence. Shapes as in those calls. */
+ * +layer_count): append k_new/v_new (as kvc_append_layers, with the group flush
+ * when the window reaches R) and attend q (as kvc_decode_attn); the results equal
+ * those two calls made in sequence. One launch, or two in the steps where some
+ * layer's window fills (the append with its group flush runs first). Shapes as in
+ * those calls. */
 kvc_status kvc_decode_step(kvc_cache* cache, int32_t layer_begin, int32_t layer_count,
                            const void* q, const void* k_new, const void* v_new,
                            float* out, void* stream);

@@ -113,7 +113,7 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
   c->block_bytes = kvc::block_bytes(d.head_dim, d.bits);
   if (cudaGetDevice(&c->device) != cudaSuccess) { delete c; return KVC_E_CUDA; }
   c->L.resize(d.n_layers);
-  size_t packed = 0, part_ctas = 0;
+  size_t packed = 0;
   for (int l = 0; l < d.n_layers; ++l) {
     LayerState& ls = c->L[l];
     ls.budget = kept_cap(d, budgets[l]);
@@ -121,21 +121,15 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
                     (KVC_GROUP - 1 + d.obs_window + d.max_new_tokens + KVC_GROUP - 1) / KVC_GROUP + 1;
     ls.packed_off = packed;
     packed += (size_t)units * ls.cap_groups * c->block_bytes;
-    const int ctas = kvc::packed_ctas(ls.cap_groups) + kvc::window_ctas(d.window_len);
-    part_ctas += (size_t)units * ctas;
   }
   c->packed_bytes = packed;
   c->win_elems = (size_t)d.n_layers * units * d.window_len * d.head_dim;
-  c->dec_part_elems = part_ctas * g * (d.head_dim + 2);
-  c->n_tickets = (size_t)d.n_layers * units;
 
   c->packed = static_cast<uint8_t*>(dev_alloc(c, packed));
   c->win_k = static_cast<__nv_bfloat16*>(dev_alloc(c, c->win_elems * 2));
   c->win_v = static_cast<__nv_bfloat16*>(dev_alloc(c, c->win_elems * 2));
-  c->dec_part = static_cast<float*>(dev_alloc(c, c->dec_part_elems * 4));
-  c->tickets = static_cast<unsigned*>(dev_alloc(c, c->n_tickets * 4));
   c->err = static_cast<unsigned*>(dev_alloc(c, 16));
-  bool ok = c->packed && c->win_k && c->win_v && c->dec_part && c->tickets && c->err;
+  bool ok = c->packed && c->win_k && c->win_v && c->err;
   if (ok && scoring) {
     const int M = g * d.obs_window;
     const int nch = (d.prompt_len + kvc::kScoreChunk - 1) / kvc::kScoreChunk;
@@ -165,7 +159,6 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
     // the window is zero-initialised: masked slots must hold finite values
     ok = cudaMemset(c->win_k, 0, c->win_elems * 2) == cudaSuccess &&
          cudaMemset(c->win_v, 0, c->win_elems * 2) == cudaSuccess &&
-         cudaMemset(c->tickets, 0, c->n_tickets * 4) == cudaSuccess &&
          cudaMemset(c->err, 0, 16) == cudaSuccess &&
          cudaDeviceSynchronize() == cudaSuccess;
   }

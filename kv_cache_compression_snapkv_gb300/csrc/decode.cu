@@ -1,5 +1,5 @@
-// decode.cu -- split-K decode attention over the packed cache plus the bf16 window,
-// optionally fused with the append (and group flush) of the step's new token.
+// decode.cu -- decode attention over the packed cache plus the bf16 window,
+// optionally fused with the append of the step's new token.
 //
 // MiniKV: Pushing the Limits of LLM Inference via 2-Bit Layer-Discriminative KV
 // Cache, §2 eq. (1) and Algorithm 1 (decoding): append the new key/value to the
@@ -8,18 +8,24 @@
 // A_unquant . R_V. Blog "KV Cache Compression: Eviction and Quantization",
 // "Measured on a real model": exact recent window, rounded rest, one softmax.
 //
-// Work decomposition (one launch for a range of layers):
-//   unit = (layer, sequence b, kv head h). "Packed" CTAs take 16 group blocks (2
-//   per warp); "window" CTAs 128 ring slots (16 per warp). Every warp first
-//   stages its whole chunk into shared memory with one or two bulk async copies
-//   (cp.async.bulk on an mbarrier, bounded wait), then computes from shared
-//   memory. Each warp keeps an online softmax for the g query heads of its kv
-//   head; warps merge in shared memory, CTAs write (m, l, o) partials, and the
-//   last CTA of the unit (atomic ticket, no waiting) merges them with a
-//   log-sum-exp combine and writes the fp32 output.
-//   In the fused step the window CTAs also store the new token into the ring and,
-//   when the window reaches R, quantize its oldest group (written to the packed
-//   store and attended from shared memory in the same launch).
+// Work decomposition (one persistent launch for a range of layers):
+//   unit = (layer, sequence b, kv head h); its work is cut into chunks of 16
+//   window slots or 2 packed group blocks. There is one CTA per SM; CTA i takes
+//   the units i, 2P-1-i, 2P+i, ... (P CTAs, snake order over units that come
+//   largest first), lays their chunks end to end, and warp w takes chunks w,
+//   w + NW, w + 2 NW, ... of that list. Each warp double-buffers its chunks in
+//   shared memory with bulk asynchronous copies (cp.async.bulk on per-slot
+//   mbarriers, bounded waits): the copy of its next-but-one chunk is issued as
+//   soon as a slot is read. A warp keeps an online softmax for the g query heads
+//   of its current unit and deposits it (m, l, o) in shared memory when it leaves
+//   the unit; the last warp to deposit merges the deposits with a log-sum-exp
+//   combine and writes the fp32 output. No state crosses CTAs and nothing waits
+//   on another CTA.
+//   The new token of a fused step is stored into the ring by the warp whose
+//   window chunk holds its slot (which also patches its staged copy). A step in
+//   which some layer's window reaches R runs the append kernel first (it stores
+//   the new tokens and quantizes the oldest group of each full window) and then
+//   this kernel over the updated cache.
 //
 // Arithmetic. Per 32-token group block the key logits are
 //     q . k_t = sum_c (q_c S_c) code_tc + sum_c q_c Z_c
@@ -40,10 +46,9 @@
 namespace kvc {
 namespace {
 
-constexpr int kThreads = kDecWarps * 32;
-constexpr int kGroupsPerWarp = kGroupsPerCta / kDecWarps;
-constexpr int kSlotsPerWarp = kWinSlotsPerCta / kDecWarps;
-static_assert(kSlotsPerWarp == 32, "window warps take 32 slots");
+constexpr int kGroupsPerWarp = kDecGroupsPerChunk;
+constexpr int kSlotsPerWarp = kDecSlotsPerChunk;
+static_assert(kSlotsPerWarp == 16, "window warps take 16 slots");
 constexpr unsigned kWaitLimit = 1u << 20;   // bounded mbarrier polls (far above any copy)
 static_assert(kGroupsPerWarp <= 8, "the key zero-point product covers at most 8 groups");
 
@@ -56,14 +61,14 @@ struct DecLayer {
   int cap_groups;
   int new_slot;     // ring slot of the token appended in this launch, or -1
   int flush_start;  // ring slot of the oldest token when this launch flushes a group, or -1
-  int wchunks;      // window chunks (32 slots) per unit; packed chunks (4 groups) follow
-  int cpc;          // chunks per CTA
+  int wchunks;      // window chunks (16 slots) per unit; packed chunks (2 groups) follow
+  int pchunks;      // packed chunks per unit
   long long packed_off;
 };
 
 struct DecParams {
   DecLayer L[KVC_MAX_LAUNCH_LAYERS];
-  const __nv_bfloat16* k_new;   // [n_layers][units][D] (fused step only)
+  const __nv_bfloat16* k_new;   // [n_layers][units][D] (fused append only)
   const __nv_bfloat16* v_new;
   unsigned* err;                // device error word (bit 0: a staging wait gave up)
   int n_layers;                 // layers in this launch
@@ -119,34 +124,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
-}
-
-// Stage up to two contiguous global ranges into shared memory (whole warp calls).
-// The warp's barrier was initialised at kernel start; `phase` counts its uses.
-// Returns false if the wait gave up (error word set; a second bounded wait lets
-// copies still in flight land before the CTA can exit).
-__device__ bool warp_stage(uint64_t* bar, unsigned phase, void* dst0, const void* src0,
-                           uint32_t bytes0, void* dst1, const void* src1, uint32_t bytes1,
-                           unsigned* err) {
-  const int lane = threadIdx.x & 31;
-  __syncwarp();   // every lane is done reading the buffer's previous contents
-  if (lane == 0) {
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
-                 :: "r"(smem_u32(bar)), "r"(bytes0 + bytes1) : "memory");
-    bulk_g2s(dst0, src0, bytes0, bar);
-    if (bytes1) bulk_g2s(dst1, src1, bytes1, bar);
-  }
-  const unsigned parity = phase & 1u;
-  bool done = false;
-  for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(bar, parity);
-  if (!done) {
-    if (lane == 0) atomicOr(err, 1u);
-    for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(bar, parity);
-    done = false;
-  }
-  __syncwarp();
-  return __all_sync(0xffffffffu, done);
 }
 
 // ------------------------------------------------------------ fragment helpers
@@ -288,26 +265,25 @@ __device__ __forceinline__ void load_qregs(QRegs<D, GQ>& qr, const __nv_bfloat16
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int c = 16 * ks + 2 * tid + 8 * e2;
-        float a = 0.f, b = 0.f;
-        if (h < GQ) {
-          a = __bfloat162float(qs[h * D + c]);
-          b = __bfloat162float(qs[h * D + c + 1]);
-        }
-        const __half2 q2 = __floats2half2_rn(a, b);
+        float2 f = make_float2(0.f, 0.f);
+        if (h < GQ) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(qs + h * D + c));
+        const __half2 q2 = __float22half2_rn(f);
         qr.qh[u][ks][e2] = h2u(q2);
         qr.qn[u][ks][e2] = (gid & 1) ? h2u(__hneg2(q2)) : 0u;
       }
   }
 }
 
-// Online-softmax update with the logits of 32 tokens: x[u][mt][r] is token
+// Online-softmax update with the logits of 16 * NMT tokens: x[u][mt][r] is token
 // 16mt + gid + 8r for head 4u + tid. The weights replace the logits.
-template <int D, int GQ>
-__device__ __forceinline__ void softmax_update(WarpState<D, GQ>& st, float (&x)[n_tiles<GQ>()][2][2],
-                                               float sl2) {
+template <int D, int GQ, int NMT>
+__device__ __forceinline__ void softmax_update(WarpState<D, GQ>& st,
+                                               float (&x)[n_tiles<GQ>()][NMT][2], float sl2) {
 #pragma unroll
   for (int u = 0; u < n_tiles<GQ>(); ++u) {
-    float gm = fmaxf(fmaxf(x[u][0][0], x[u][0][1]), fmaxf(x[u][1][0], x[u][1][1]));
+    float gm = fmaxf(x[u][0][0], x[u][0][1]);
+#pragma unroll
+    for (int mt = 1; mt < NMT; ++mt) gm = fmaxf(gm, fmaxf(x[u][mt][0], x[u][mt][1]));
     gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
     gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
     gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
@@ -326,7 +302,7 @@ __device__ __forceinline__ void softmax_update(WarpState<D, GQ>& st, float (&x)[
     const float msl = (st.m[u] == -INFINITY) ? 0.f : st.m[u] * sl2;
     float s = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < NMT; ++mt)
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const float p = fast_exp2(fmaf(x[u][mt][r], sl2, -msl));
@@ -441,7 +417,7 @@ __device__ void packed_warp(WarpState<D, GQ>& st, const QRegs<D, GQ>& qr, const 
           x[u][mt][1] = (acc[u][mt][0][2] + acc[u][mt][0][3]) + (acc[u][mt][1][2] + acc[u][mt][1][3]);
         }
     }
-    softmax_update<D, GQ>(st, x, sl2);
+    softmax_update<D, GQ, 2>(st, x, sl2);
 
     // values: o[channel][n] += sum_t code[channel][t] * hi/lo(p_t S_t,gc)[t][n]
     uint32_t vw[WPL];
@@ -492,15 +468,15 @@ __device__ void packed_warp(WarpState<D, GQ>& st, const QRegs<D, GQ>& qr, const 
 }
 
 // ------------------------------------------------------------- window slots
-// wk: NS = 32 staged key rows (win_k_index layout); wv: 16 staged value pair rows
-// (win_v_index layout); the first n_valid slots are live. bf16 products, exact
-// queries, hi/lo weights.
+// wk: 16 staged key rows (win_k_index layout, first slot a multiple of 16); wv: 8
+// staged value pair rows (win_v_index layout); the first n_valid slots are live.
+// bf16 products, exact queries, hi/lo weights.
 template <int D, int GQ>
 __device__ void window_warp(WarpState<D, GQ>& st, const __nv_bfloat16* qs, const __nv_bfloat16* wk,
                             const uint32_t* wv, int n_valid, float sl2) {
   constexpr int KS = D / 16, NH = n_tiles<GQ>();
   const int lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
-  float x[NH][2][2];
+  float x[NH][1][2];
   {
     uint32_t bq[NH][KS][2];
 #pragma unroll
@@ -514,83 +490,113 @@ __device__ void window_warp(WarpState<D, GQ>& st, const __nv_bfloat16* qs, const
           bq[u][ks][e2] = live ? *reinterpret_cast<const uint32_t*>(qs + h * D + 16 * ks + 2 * tid + 8 * e2)
                                : 0u;
     }
-    float acc[NH][2][2][4];
+    float acc[NH][2][4];
 #pragma unroll
     for (int u = 0; u < NH; ++u)
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+      for (int e = 0; e < 4; ++e) { acc[u][0][e] = 0.f; acc[u][1][e] = 0.f; }
+    // rows gid (rl 0) and gid + 8 (rl 1); 16-byte chunks swizzled by gid
+    const uint4* r0 = reinterpret_cast<const uint4*>(wk + (size_t)gid * D);
+    const uint4* r1 = reinterpret_cast<const uint4*>(wk + (size_t)(gid + 8) * D);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) { acc[u][mt][0][e] = 0.f; acc[u][mt][1][e] = 0.f; }
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      // rows 16mt + gid (rl 0) and 16mt + gid + 8 (rl 1); 16-byte chunks swizzled by gid
-      const uint4* r0 = reinterpret_cast<const uint4*>(wk + (size_t)(16 * mt + gid) * D);
-      const uint4* r1 = reinterpret_cast<const uint4*>(wk + (size_t)(16 * mt + gid + 8) * D);
-#pragma unroll
-      for (int i = 0; i < KS / 2; ++i) {
-        const int ch = (tid * (KS / 2) + i) ^ gid;
-        const uint4 u0 = r0[ch], u1 = r1[ch];
-#pragma unroll
-        for (int u = 0; u < NH; ++u) {
-          mma_bf16(acc[u][mt][0], u0.x, u1.x, u0.y, u1.y, bq[u][2 * i][0], bq[u][2 * i][1]);
-          mma_bf16(acc[u][mt][1], u0.z, u1.z, u0.w, u1.w, bq[u][2 * i + 1][0], bq[u][2 * i + 1][1]);
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < NH; ++u)
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float v = (acc[u][mt][0][2 * r] + acc[u][mt][0][2 * r + 1]) +
-                          (acc[u][mt][1][2 * r] + acc[u][mt][1][2 * r + 1]);
-          x[u][mt][r] = (16 * mt + gid + 8 * r) < n_valid ? v : -INFINITY;
-        }
-  }
-  softmax_update<D, GQ>(st, x, sl2);
-#pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
-    uint32_t b0[NH], b1[NH];
-#pragma unroll
-    for (int u = 0; u < NH; ++u) {
-      b0[u] = movm_t(split_bf16(x[u][ks][0]));
-      b1[u] = movm_t(split_bf16(x[u][ks][1]));
-    }
-    // pair rows 8ks + tid (tokens 16ks + 2tid, +1) and 8ks + 4 + tid; chunks swizzled by tid
-    const uint4* p0 = reinterpret_cast<const uint4*>(wv + (size_t)(8 * ks + tid) * D);
-    const uint4* p1 = reinterpret_cast<const uint4*>(wv + (size_t)(8 * ks + 4 + tid) * D);
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) {
-      const int ch = (gid * (D / 32) + i) ^ tid;
-      const uint4 v0 = p0[ch], v1 = p1[ch];
-      // words: (mt = 2i, rl 0), (2i, rl 1), (2i + 1, rl 0), (2i + 1, rl 1)
+    for (int i = 0; i < KS / 2; ++i) {
+      const int ch = (tid * (KS / 2) + i) ^ gid;
+      const uint4 u0 = r0[ch], u1 = r1[ch];
 #pragma unroll
       for (int u = 0; u < NH; ++u) {
-        mma_bf16(st.o[u][2 * i], v0.x, v0.y, v1.x, v1.y, b0[u], b1[u]);
-        mma_bf16(st.o[u][2 * i + 1], v0.z, v0.w, v1.z, v1.w, b0[u], b1[u]);
+        mma_bf16(acc[u][0], u0.x, u1.x, u0.y, u1.y, bq[u][2 * i][0], bq[u][2 * i][1]);
+        mma_bf16(acc[u][1], u0.z, u1.z, u0.w, u1.w, bq[u][2 * i + 1][0], bq[u][2 * i + 1][1]);
       }
+    }
+#pragma unroll
+    for (int u = 0; u < NH; ++u)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float v = (acc[u][0][2 * r] + acc[u][0][2 * r + 1]) +
+                        (acc[u][1][2 * r] + acc[u][1][2 * r + 1]);
+        x[u][0][r] = (gid + 8 * r) < n_valid ? v : -INFINITY;
+      }
+  }
+  softmax_update<D, GQ, 1>(st, x, sl2);
+  uint32_t b0[NH], b1[NH];
+#pragma unroll
+  for (int u = 0; u < NH; ++u) {
+    b0[u] = movm_t(split_bf16(x[u][0][0]));
+    b1[u] = movm_t(split_bf16(x[u][0][1]));
+  }
+  // pair rows tid (tokens 2tid, 2tid + 1) and 4 + tid (tokens 8 + 2tid, +1); chunks
+  // swizzled by tid
+  const uint4* p0 = reinterpret_cast<const uint4*>(wv + (size_t)tid * D);
+  const uint4* p1 = reinterpret_cast<const uint4*>(wv + (size_t)(4 + tid) * D);
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) {
+    const int ch = (gid * (D / 32) + i) ^ tid;
+    const uint4 v0 = p0[ch], v1 = p1[ch];
+    // words: (mt = 2i, rl 0), (2i, rl 1), (2i + 1, rl 0), (2i + 1, rl 1)
+#pragma unroll
+    for (int u = 0; u < NH; ++u) {
+      mma_bf16(st.o[u][2 * i], v0.x, v0.y, v1.x, v1.y, b0[u], b1[u]);
+      mma_bf16(st.o[u][2 * i + 1], v0.z, v0.w, v1.z, v1.w, b0[u], b1[u]);
     }
   }
 }
 
 // ----------------------------------------------------------- merge helpers
-template <int D, int GQ>
-struct DecSmem {
-  float m[kDecWarps][GQ];      // log2-domain running max per warp and head
-  float l[kDecWarps][GQ];
-  float o[kDecWarps][GQ][D];
-  float wt[kDecWarps][GQ];     // CTA merge weights
-  float M[GQ], L[GQ];
-  int last;
+// ----------------------------------------------------------- persistent layout
+// One CTA per SM. A CTA takes whole units (snake order over the launch's units,
+// which come largest first: layer 0 of a pyramid schedule holds the most groups)
+// and lays their chunks end to end; warp w takes chunks w, w + NW, w + 2 NW, ...
+// of that list, each staged by a bulk copy into one of its two ring slots (the
+// next one is in flight while the current one is computed). A warp deposits its
+// softmax state when it leaves a unit; the last warp to deposit merges the unit's
+// deposits in shared memory and writes the output. No state crosses CTAs.
+template <int D, int BITS, int GQ>
+struct DecCfg {
+  static constexpr int SLOT = warp_buf_bytes<D, BITS>();   // one chunk
+  static constexpr int DEPW = GQ * (D + 2);                // floats of one deposit: m, l, o
+  static constexpr int QB = GQ * D * 2;                    // bytes of one unit's queries
+  static constexpr int kQRing = 4;                         // query ring entries
+  static constexpr int bytes(int nw) {
+    return nw * 2 * SLOT + 2 * nw * DEPW * 4 + kQRing * QB + (2 * nw + kQRing) * 8 + 64 +
+           KVC_MAX_LAUNCH_LAYERS * (int)sizeof(DecLayer);
+  }
+  static constexpr int pick(int nw) { return (nw <= 4 || bytes(nw) <= 220 * 1024) ? nw : pick(nw - 1); }
+  static constexpr int NW = pick(GQ > 4 ? 8 : 12);           // warps per CTA
+  static constexpr int kThreadsC = NW * 32;
+  // byte offsets inside dynamic shared memory
+  static constexpr int oRing = 0;
+  static constexpr int oDep = oRing + NW * 2 * SLOT;
+  static constexpr int oQ = oDep + 2 * NW * DEPW * 4;
+  static constexpr int oBars = oQ + kQRing * QB;
+  static constexpr int oCtl = oBars + (2 * NW + kQRing) * 8;
+  static constexpr int oLay = oCtl + 64;
+  static constexpr int total = oLay + KVC_MAX_LAUNCH_LAYERS * (int)sizeof(DecLayer);
+  static_assert(SLOT % 16 == 0 && DEPW % 1 == 0 && QB % 16 == 0, "alignment");
+  static_assert(oQ % 16 == 0 && oBars % 8 == 0, "alignment");
 };
 
-// Write the warp's per-head state (both column parts and the value zero-point
-// sums folded in) into shared memory.
+// Control words of a CTA (shared memory): per unit parity, the number of deposits,
+// the mask of depositing warps and the number of merges done.
+struct DecCtl {
+  unsigned count[2];
+  unsigned mask[2];
+  unsigned gen[2];
+};
+
+// Unit k of CTA i (snake order): k even -> k*P + i, k odd -> (k+1)*P - 1 - i.
+__device__ __forceinline__ int snake_unit(int k, int i, int P) {
+  return (k & 1) ? (k + 1) * P - 1 - i : k * P + i;
+}
+
+// Write the warp's per-head state (both column parts and the value zero-point sums
+// folded in) as one deposit: m[GQ], l[GQ], o[GQ][D].
 template <int D, int GQ>
-__device__ void warp_to_smem(WarpState<D, GQ>& st, DecSmem<D, GQ>& sm, int warp, float sl2) {
+__device__ void warp_deposit(WarpState<D, GQ>& st, float* dep, float sl2) {
   constexpr int NGC = D / 32, NH = n_tiles<GQ>();
   const int lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
+  float* dm = dep;
+  float* dl = dep + GQ;
+  float* dout = dep + 2 * GQ;
 #pragma unroll
   for (int u = 0; u < NH; ++u) {
     const int h = 4 * u + tid;
@@ -605,330 +611,306 @@ __device__ void warp_to_smem(WarpState<D, GQ>& st, DecSmem<D, GQ>& sm, int warp,
     if (h < GQ) {
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
-        sm.o[warp][h][16 * mt + gid] = st.o[u][mt][0] + st.o[u][mt][1] + z[mt / 2];
-        sm.o[warp][h][16 * mt + gid + 8] = st.o[u][mt][2] + st.o[u][mt][3] + z[mt / 2];
+        dout[h * D + 16 * mt + gid] = st.o[u][mt][0] + st.o[u][mt][1] + z[mt / 2];
+        dout[h * D + 16 * mt + gid + 8] = st.o[u][mt][2] + st.o[u][mt][3] + z[mt / 2];
       }
       if (gid == 0) {
-        sm.m[warp][h] = st.m[u] == -INFINITY ? -INFINITY : st.m[u] * sl2;
-        sm.l[warp][h] = l;
+        dm[h] = st.m[u] == -INFINITY ? -INFINITY : st.m[u] * sl2;
+        dl[h] = l;
       }
     }
   }
 }
 
-// The staging area at the start of dynamic shared memory is shared, in turn, by
-// the warps' staged chunks, the group being flushed (fp32 rows + codes) and the
-// CTA's merge scratch: it is sized for the largest of the three.
-template <int D, int BITS, int GQ>
-constexpr int stage_bytes() {
-  constexpr int a = kDecWarps * warp_buf_bytes<D, BITS>();
-  constexpr int b = (int)sizeof(GroupSmem<D, kThreads>);
-  constexpr int c = (int)sizeof(DecSmem<D, GQ>);
-  constexpr int m = a > b ? (a > c ? a : c) : (b > c ? b : c);
-  return (m + 127) / 128 * 128;
-}
-template <int D, int BITS, int GQ>
-constexpr int dyn_smem_bytes() {
-  return stage_bytes<D, BITS, GQ>() + block_bytes(D, BITS) + kDecWarps * 8 + GQ * D * 2;
-}
-
-template <int D, int BITS, int GQ>
-__global__ void __launch_bounds__(kThreads, 3)
-decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __restrict__ win_k,
-              __nv_bfloat16* __restrict__ win_v, const __nv_bfloat16* __restrict__ q,
-              float* __restrict__ out, float* __restrict__ part, unsigned* __restrict__ tickets) {
-  constexpr int BB = block_bytes(D, BITS), WB = warp_buf_bytes<D, BITS>();
-  extern __shared__ __align__(128) uint8_t dsm[];
-  // the merge scratch reuses the staging buffers once every warp is done with them
-  DecSmem<D, GQ>& sm = *reinterpret_cast<DecSmem<D, GQ>*>(dsm);
-  static_assert(sizeof(DecSmem<D, GQ>) <= stage_bytes<D, BITS, GQ>(), "merge scratch fits");
-  static_assert(sizeof(GroupSmem<D, kThreads>) <= stage_bytes<D, BITS, GQ>(), "flush staging fits");
-  static_assert(kDecWarps * WB <= stage_bytes<D, BITS, GQ>(), "warp buffers fit");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* wbuf = dsm + warp * WB;
-  uint8_t* fblk = dsm + stage_bytes<D, BITS, GQ>();
-  uint64_t* bars = reinterpret_cast<uint64_t*>(fblk + BB);
-  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(bars + kDecWarps);
-
-  // locate (layer, unit, cta index)
-  int li = 0;
-  while (li + 1 < P.n_layers && (int)blockIdx.x >= P.L[li + 1].cta_begin) ++li;
-  const DecLayer& Ld = P.L[li];
-  const int local = blockIdx.x - Ld.cta_begin;
-  const int unit = local / Ld.n_ctas, cidx = local % Ld.n_ctas;
-  const int layer = P.layer_begin + li;
-  // the GQ query heads of kv head h of sequence b are rows unit*GQ .. unit*GQ+GQ-1
-  const __nv_bfloat16* qrow = q + ((size_t)li * P.units + unit) * GQ * D;
-  uint8_t* ubase = packed + Ld.packed_off + (size_t)unit * Ld.cap_groups * BB;
-
-  // the unit's queries, staged once for every warp
-  for (int i = threadIdx.x; i < GQ * D / 8; i += kThreads)
-    reinterpret_cast<uint4*>(qs)[i] = reinterpret_cast<const uint4*>(qrow)[i];
-  WarpState<D, GQ> st;
-  state_init(st);
-  if (lane == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" :: "r"(smem_u32(&bars[warp])) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+// One warp merges the deposits of the warps in `mask` (log-sum-exp combine) and
+// writes o[GQ][D] (fp32). The weight of each (warp, head) replaces its m slot.
+template <int D, int GQ, int NW>
+__device__ void merge_deposits(float* dep, unsigned mask, float* __restrict__ o) {
+  constexpr int DEPW = GQ * (D + 2);
+  constexpr int NWH = (NW * GQ + 31) / 32;
+  const int lane = threadIdx.x & 31;
+  float f[NWH];
+#pragma unroll
+  for (int i = 0; i < NWH; ++i) {
+    const int idx = lane + 32 * i, w = idx / GQ, h = idx % GQ;
+    f[i] = 0.f;
+    if (idx < NW * GQ && (mask >> w & 1u) && dep[w * DEPW + GQ + h] > 0.f) {
+      float M = -INFINITY;
+      for (int v = 0; v < NW; ++v)
+        if (mask >> v & 1u) M = fmaxf(M, dep[v * DEPW + h]);
+      f[i] = exp2f(dep[w * DEPW + h] - M);
+    }
   }
   __syncwarp();
-  unsigned phase = 0;
-  const size_t wunit = (size_t)layer * P.units + unit;
-  __nv_bfloat16* wk = win_k + wunit * P.R * D;
-  __nv_bfloat16* wv = win_v + wunit * P.R * D;
-  const bool flush = cidx == 0 && Ld.flush_start >= 0;
-  const __nv_bfloat16* kn = P.k_new + ((size_t)li * P.units + unit) * D;
-  const __nv_bfloat16* vn = P.v_new + ((size_t)li * P.units + unit) * D;
-  // the new token: window chunk holding it (-1 if it left the window with a flush); the
-  // CTA covering that chunk (CTA 0 after a flush) stores it into the ring
-  int new_chunk = -1;
-  if (Ld.new_slot >= 0) {
-    new_chunk = Ld.win_len > 0 ? (Ld.win_len - 1) / kSlotsPerWarp : -1;
-    const int owner = new_chunk >= 0 ? new_chunk / Ld.cpc : 0;
-    if (cidx == owner)
-      for (int c = threadIdx.x; c < D; c += kThreads)
-        window_store(wk, wv, Ld.new_slot, c, D, kn[c], vn[c]);
-  }
-  __syncthreads();   // queries staged
-  QRegs<D, GQ> qr;
-  load_qregs<D, GQ>(qr, qs);
-  if (flush) {
-    // quantize the oldest group of the window into a new packed block (the new token
-    // belongs to it only when R == 32, and then this CTA stored it above)
-    __syncthreads();
-    GroupSmem<D, kThreads>& gs = *reinterpret_cast<GroupSmem<D, kThreads>*>(dsm);
-    for (int i = threadIdx.x; i < KVC_GROUP * D; i += kThreads) {
-      const int t = i / D, c = i % D;
-      gs.k[t][c] = __bfloat162float(window_load_k(wk, Ld.flush_start + t, c, D));
-      gs.v[t][c] = __bfloat162float(window_load_v(wv, Ld.flush_start + t, c, D));
-    }
-    __syncthreads();
-    quantize_block<D, BITS, kThreads>(gs, fblk);
-    __syncthreads();
-    uint4* dst = reinterpret_cast<uint4*>(ubase + (size_t)Ld.n_groups * BB);
-    const uint4* src = reinterpret_cast<const uint4*>(fblk);
-    for (int i = threadIdx.x; i < BB / 16; i += kThreads) dst[i] = src[i];
-    __syncthreads();   // the staging area is reused by the copies below
-    if (warp == 0) packed_warp<D, BITS, GQ>(st, qr, fblk, 1, P.sl2);
-  }
-  // this CTA's chunks of the unit, round robin over the warps
-  const int total = Ld.wchunks + (Ld.n_groups + kGroupsPerWarp - 1) / kGroupsPerWarp;
-  const int cb = cidx * Ld.cpc, ce = min(cb + Ld.cpc, total);
-  const int wend = min(ce, Ld.wchunks);
-  bool ok = true;
-  for (int ch = cb + warp; ch < wend; ch += kDecWarps) {
-    const int pos0 = ch * kSlotsPerWarp;
-    const int n_valid = min(kSlotsPerWarp, Ld.win_len - pos0);
-    const int slot0 = (Ld.win_start + pos0) % P.R;
-    __nv_bfloat16* sk = reinterpret_cast<__nv_bfloat16*>(wbuf);
-    uint32_t* sv = reinterpret_cast<uint32_t*>(wbuf + kSlotsPerWarp * D * 2);
-    ok = warp_stage(&bars[warp], phase++, sk, wk + (size_t)slot0 * D,
-                    (uint32_t)(kSlotsPerWarp * D * 2), sv, wv + (size_t)(slot0 >> 1) * D * 2,
-                    (uint32_t)(kSlotsPerWarp * D * 2), P.err);
-    if (!ok) break;
-    if (ch == new_chunk) {
-      // the new token was stored through the generic path in this launch: take it
-      // from the inputs rather than from the asynchronous copy
-      const int r = Ld.new_slot - slot0;
-      __nv_bfloat16* svh = reinterpret_cast<__nv_bfloat16*>(sv);
-      for (int c = lane; c < D; c += 32) {
-        sk[win_k_index(r, c, D)] = kn[c];
-        svh[win_v_index(r, c, D)] = vn[c];
-      }
-      __syncwarp();
-    }
-    window_warp<D, GQ>(st, qs, sk, sv, n_valid, P.sl2);
-  }
-  // packed chunks continue the round robin where the window chunks left off
-  if (ok) {
-    const int first = max(cb, Ld.wchunks);
-    int ch = first + ((warp - (first - cb)) % kDecWarps + kDecWarps) % kDecWarps;
-    for (; ch < ce; ch += kDecWarps) {
-      const int g0 = (ch - Ld.wchunks) * kGroupsPerWarp;
-      const int ng = min(kGroupsPerWarp, Ld.n_groups - g0);
-      if (!warp_stage(&bars[warp], phase++, wbuf, ubase + (size_t)g0 * BB,
-                      (uint32_t)(ng * BB), nullptr, nullptr, 0u, P.err))
-        break;
-      packed_warp<D, BITS, GQ>(st, qr, wbuf, ng, P.sl2);
-    }
-  }
-  __syncthreads();   // every warp is done with the staging area
-  warp_to_smem<D, GQ>(st, sm, warp, P.sl2);
-  __syncthreads();
-
-  // merge the CTA's warps into one partial: part[cta][head][0..D+1] = (m, l, o[D]);
-  // the per-(head, warp) weights are computed once
-  if (threadIdx.x < GQ) {
-    const int r = threadIdx.x;
-    float M = -INFINITY;
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm.m[w][r]);
-    float L = 0.f;
-    for (int w = 0; w < kDecWarps; ++w) {
-      const float f = sm.l[w][r] > 0.f ? exp2f(sm.m[w][r] - M) : 0.f;
-      sm.wt[w][r] = f;
-      L += sm.l[w][r] * f;
-    }
-    sm.M[r] = M;
-    sm.L[r] = L;
-  }
-  __syncthreads();
-  if (Ld.n_ctas == 1) {
-    // the whole unit ran in this CTA: no partials to merge
-    float* o = out + ((size_t)li * P.units + unit) * GQ * D;
-    for (int i = threadIdx.x; i < GQ * D; i += kThreads) {
-      const int r = i / D, cch = i % D;
-      float O = 0.f;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) O += sm.o[w][r][cch] * sm.wt[w][r];
-      o[(size_t)r * D + cch] = O / sm.L[r];
-    }
-    return;
+  for (int i = 0; i < NWH; ++i) {
+    const int idx = lane + 32 * i, w = idx / GQ, h = idx % GQ;
+    if (idx < NW * GQ) dep[w * DEPW + h] = f[i];   // unused warps get weight 0
   }
-  float* mypart = part + (size_t)blockIdx.x * GQ * (D + 2);
-  for (int i = threadIdx.x; i < GQ * D; i += kThreads) {
-    const int r = i / D, cch = i % D;
-    float O = 0.f;
+  __syncwarp();
+  float L[GQ];
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) O += sm.o[w][r][cch] * sm.wt[w][r];
-    mypart[r * (D + 2) + 2 + cch] = O;
-    if (cch == 0) { mypart[r * (D + 2)] = sm.M[r]; mypart[r * (D + 2) + 1] = sm.L[r]; }
+  for (int h = 0; h < GQ; ++h) {
+    float s = 0.f;
+    for (int w = 0; w < NW; ++w) s += dep[w * DEPW + h] * (mask >> w & 1u ? dep[w * DEPW + GQ + h] : 0.f);
+    L[h] = s;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned t = atomicAdd(&tickets[(size_t)layer * P.units + unit], 1u);
-    sm.last = (t == (unsigned)(Ld.n_ctas - 1));
-    if (sm.last) tickets[(size_t)layer * P.units + unit] = 0u;
-  }
-  __syncthreads();
-  if (!sm.last) return;
-  __threadfence();
-  // the last CTA of the unit merges all partials: (m, l) of every split in one batch
-  // of loads, the weights once per (head, split), then independent output loads
-  const int nc = Ld.n_ctas;
-  const float* up = part + (size_t)(Ld.cta_begin + unit * nc) * GQ * (D + 2);
-  float* o = out + ((size_t)li * P.units + unit) * GQ * D;
-  constexpr int kMlOff = ((int)sizeof(DecSmem<D, GQ>) + 15) / 16 * 16;
-  float* ml = reinterpret_cast<float*>(dsm + kMlOff);
-  if (kMlOff + nc * GQ * 2 * (int)sizeof(float) <= stage_bytes<D, BITS, GQ>()) {
-    for (int idx = threadIdx.x; idx < nc * GQ; idx += kThreads) {
-      const float* ps = up + (size_t)idx * (D + 2);   // idx = s * GQ + r
-      ml[2 * idx] = __ldcg(ps);
-      ml[2 * idx + 1] = __ldcg(ps + 1);
-    }
-    __syncthreads();
-    if (threadIdx.x < GQ) {
-      const int r = threadIdx.x;
-      float M = -INFINITY;
-      for (int s = 0; s < nc; ++s) M = fmaxf(M, ml[2 * (s * GQ + r)]);
-      float L = 0.f;
-      for (int s = 0; s < nc; ++s) {
-        const float ls = ml[2 * (s * GQ + r) + 1];
-        const float f = ls > 0.f ? exp2f(ml[2 * (s * GQ + r)] - M) : 0.f;
-        ml[2 * (s * GQ + r)] = f;      // the weight replaces the max
-        L += ls * f;
-      }
-      sm.L[r] = L;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < GQ * D; i += kThreads) {
-      const int r = i / D, cch = i % D;
-      float O = 0.f;
-#pragma unroll 4
-      for (int s = 0; s < nc; ++s)
-        O += ml[2 * (s * GQ + r)] * __ldcg(up + ((size_t)s * GQ + r) * (D + 2) + 2 + cch);
-      o[(size_t)r * D + cch] = O / sm.L[r];
-    }
-  } else {
-    for (int i = threadIdx.x; i < GQ * D; i += kThreads) {
-      const int r = i / D, cch = i % D;
-      float M = -INFINITY;
-      for (int s = 0; s < nc; ++s) M = fmaxf(M, __ldcg(up + ((size_t)s * GQ + r) * (D + 2)));
-      float L = 0.f, O = 0.f;
-      for (int s = 0; s < nc; ++s) {
-        const float* ps = up + ((size_t)s * GQ + r) * (D + 2);
-        const float ls = __ldcg(ps + 1);
-        if (ls > 0.f) {
-          const float f = exp2f(__ldcg(ps) - M);
-          L += ls * f;
-          O += __ldcg(ps + 2 + cch) * f;
-        }
-      }
-      o[(size_t)r * D + cch] = O / L;
-    }
+  for (int e = lane; e < GQ * D; e += 32) {
+    const int h = e / D;
+    float acc = 0.f;
+    for (int w = 0; w < NW; ++w)
+      if (mask >> w & 1u) acc += dep[w * DEPW + h] * dep[w * DEPW + 2 * GQ + e];
+    float Lh = 0.f;
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) Lh = hh == h ? L[hh] : Lh;
+    o[e] = Lh > 0.f ? acc / Lh : 0.f;
   }
 }
 
 template <int D, int BITS, int GQ>
-cudaError_t launch_one(const DecParams& P, int ctas, const kvc_cache* c,
-                       const __nv_bfloat16* q, float* out, cudaStream_t stream) {
-  constexpr int sm = dyn_smem_bytes<D, BITS, GQ>();
-  // kernel attributes are set once per device for each instantiation
-  static unsigned long long configured = 0;
+__global__ void __launch_bounds__(DecCfg<D, BITS, GQ>::kThreadsC, 1)
+decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __restrict__ win_k,
+              __nv_bfloat16* __restrict__ win_v, const __nv_bfloat16* __restrict__ q,
+              float* __restrict__ out) {
+  using C = DecCfg<D, BITS, GQ>;
+  constexpr int NW = C::NW, BB = block_bytes(D, BITS), QR = C::kQRing;
+  extern __shared__ __align__(128) uint8_t dsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* cbar = reinterpret_cast<uint64_t*>(dsm + C::oBars);   // [NW][2] chunk slots
+  uint64_t* qbar = cbar + 2 * NW;                                 // [QR] query ring
+  DecCtl& ctl = *reinterpret_cast<DecCtl*>(dsm + C::oCtl);
+  DecLayer* lay = reinterpret_cast<DecLayer*>(dsm + C::oLay);
+  __nv_bfloat16* qring = reinterpret_cast<__nv_bfloat16*>(dsm + C::oQ);
+  const int P_ = gridDim.x, cta = blockIdx.x;
+  const int total_units = P.n_layers * P.units;
+
+  // layer table into shared memory (independent loads), barriers, control words
+  if (threadIdx.x < P.n_layers) lay[threadIdx.x] = P.L[threadIdx.x];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2 * NW + QR; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" :: "r"(smem_u32(&cbar[i])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    for (int p = 0; p < 2; ++p) { ctl.count[p] = 0u; ctl.mask[p] = 0u; ctl.gen[p] = 0u; }
+  }
+  __syncthreads();
+
+  // the CTA's units: k = 0, 1, ... while snake_unit(k) < total_units
+  auto unit_of = [&](int k) { return snake_unit(k, cta, P_); };
+  auto chunks_of = [&](int g) { const DecLayer& L = lay[g / P.units]; return L.wchunks + L.pchunks; };
+  auto q_copy = [&](int k) {   // queries of the CTA's unit k into ring entry k % QR
+    const int g = unit_of(k);
+    if (g >= total_units) return;
+    uint64_t* b = &qbar[k % QR];
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+                 :: "r"(smem_u32(b)), "r"((uint32_t)C::QB) : "memory");
+    bulk_g2s(qring + (k % QR) * GQ * D, q + (size_t)g * GQ * D, (uint32_t)C::QB, b);
+  };
+  if (threadIdx.x == 0)
+    for (int k = 0; k < QR; ++k) q_copy(k);
+
+  // this warp's chunk stream: positions w, w + NW, ... of the CTA's chunk list
+  struct Cursor { int k, base, g, n; };   // unit k of the CTA, first list position, unit, chunks
+  auto advance = [&](Cursor& c, int pos) {   // move c to the unit holding list position pos
+    while (c.g < total_units && pos >= c.base + c.n) {
+      c.base += c.n;
+      ++c.k;
+      c.g = unit_of(c.k);
+      c.n = c.g < total_units ? chunks_of(c.g) : 0;
+    }
+    return c.g < total_units;
+  };
+  auto issue = [&](int slot, const Cursor& c, int pos) {   // lane 0: stage chunk pos - base of unit c.g
+    const DecLayer& L = lay[c.g / P.units];
+    const int unit = c.g % P.units, j = pos - c.base;
+    uint64_t* b = &cbar[warp * 2 + slot];
+    uint8_t* dst = dsm + C::oRing + (warp * 2 + slot) * C::SLOT;
+    if (j < L.wchunks) {
+      const size_t wunit = (size_t)(P.layer_begin + c.g / P.units) * P.units + unit;
+      const int slot0 = (L.win_start + j * kSlotsPerWarp) % P.R;
+      const uint32_t wb = (uint32_t)(kSlotsPerWarp * D * 2);
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+                   :: "r"(smem_u32(b)), "r"(2 * wb) : "memory");
+      bulk_g2s(dst, win_k + (wunit * P.R + slot0) * D, wb, b);
+      bulk_g2s(dst + wb, win_v + wunit * P.R * D + (size_t)(slot0 >> 1) * D * 2, wb, b);
+    } else {
+      const int g0 = (j - L.wchunks) * kGroupsPerWarp;
+      const int ng = min(kGroupsPerWarp, L.n_groups - g0);
+      const uint8_t* src = packed + L.packed_off + ((size_t)unit * L.cap_groups + g0) * BB;
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+                   :: "r"(smem_u32(b)), "r"((uint32_t)(ng * BB)) : "memory");
+      bulk_g2s(dst, src, (uint32_t)(ng * BB), b);
+    }
+  };
+
+  Cursor cur{0, 0, unit_of(0), 0};
+  cur.n = cur.g < total_units ? chunks_of(cur.g) : 0;
+  Cursor pre = cur;   // cursor of the prefetch stream (runs two chunks ahead)
+  // prime the two slots
+  for (int s = 0; s < 2; ++s) {
+    const int pos = warp + s * NW;
+    if (advance(pre, pos) && lane == 0) issue(s, pre, pos);
+  }
+
+  WarpState<D, GQ> st;
+  QRegs<D, GQ> qr;
+  int k_cur = -1;
+  bool ok = true;
+  const int units_per_layer = P.units;
+
+  auto deposit = [&](int k) {   // hand over unit k's state; the last depositor merges
+    const int par = k & 1;
+    const Cursor& cu = cur;   // (unused: expected count from unit k itself)
+    (void)cu;
+    const int g = unit_of(k);
+    const unsigned expect = (unsigned)min(NW, chunks_of(g));
+    // the slot of this parity is free once unit k - 2 is merged
+    if (lane == 0) {
+      bool ready = false;
+      for (unsigned it = 0; it < kWaitLimit && !ready; ++it)
+        ready = *reinterpret_cast<volatile unsigned*>(&ctl.gen[par]) == (unsigned)(k >> 1);
+      if (!ready) { atomicOr(P.err, 2u); ok = false; }
+    }
+    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+    if (!ok) return;
+    float* dep = reinterpret_cast<float*>(dsm + C::oDep) + (par * NW) * C::DEPW;
+    warp_deposit<D, GQ>(st, dep + warp * C::DEPW, P.sl2);
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      atomicOr(&ctl.mask[par], 1u << warp);
+      last = atomicAdd(&ctl.count[par], 1u) == expect - 1u;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence_block();
+    const unsigned mask = *reinterpret_cast<volatile unsigned*>(&ctl.mask[par]);
+    const int li = g / units_per_layer, unit = g % units_per_layer;
+    merge_deposits<D, GQ, NW>(dep, mask, out + ((size_t)li * units_per_layer + unit) * GQ * D);
+    __syncwarp();
+    if (lane == 0) {
+      ctl.count[par] = 0u;
+      ctl.mask[par] = 0u;
+      // the query entry of unit k is free: fetch unit k + QR
+      q_copy(k + QR);
+      __threadfence_block();
+      atomicAdd(&ctl.gen[par], 1u);
+    }
+  };
+
+  for (int n = 0;; ++n) {
+    const int pos = warp + n * NW;
+    if (!advance(cur, pos)) break;
+    const int slot = n & 1;
+    if (cur.k != k_cur) {
+      if (k_cur >= 0) deposit(k_cur);
+      if (!ok) break;
+      k_cur = cur.k;
+      state_init(st);
+      // this unit's queries (bounded wait on the query ring entry)
+      bool done = false;
+      const uint32_t qpar = (uint32_t)((k_cur / QR) & 1);
+      for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(&qbar[k_cur % QR], qpar);
+      if (!__all_sync(0xffffffffu, done)) { if (lane == 0) atomicOr(P.err, 1u); ok = false; break; }
+      load_qregs<D, GQ>(qr, qring + (k_cur % QR) * GQ * D);
+    }
+    // wait for the chunk
+    bool done = false;
+    uint64_t* b = &cbar[warp * 2 + slot];
+    const uint32_t par = (uint32_t)((n >> 1) & 1);
+    for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(b, par);
+    if (!done) {
+      if (lane == 0) atomicOr(P.err, 1u);
+      for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(b, par);
+      ok = false;
+      break;
+    }
+    __syncwarp();
+    const DecLayer& L = lay[cur.g / P.units];
+    const int unit = cur.g % P.units, j = pos - cur.base;
+    uint8_t* sbuf = dsm + C::oRing + (warp * 2 + slot) * C::SLOT;
+    const __nv_bfloat16* qs = qring + (k_cur % QR) * GQ * D;
+    if (j < L.wchunks) {
+      __nv_bfloat16* sk = reinterpret_cast<__nv_bfloat16*>(sbuf);
+      uint32_t* sv = reinterpret_cast<uint32_t*>(sbuf + kSlotsPerWarp * D * 2);
+      const int pos0 = j * kSlotsPerWarp;
+      const int n_valid = min(kSlotsPerWarp, L.win_len - pos0);
+      if (L.new_slot >= 0 && j == (L.win_len - 1) / kSlotsPerWarp) {
+        // the step's new token: store it into the ring (later steps read it) and
+        // patch the staged copy (the bulk copy may predate the store)
+        const int li = cur.g / P.units;
+        const size_t wunit = (size_t)(P.layer_begin + li) * P.units + unit;
+        const __nv_bfloat16* kn = P.k_new + ((size_t)li * P.units + unit) * D;
+        const __nv_bfloat16* vn = P.v_new + ((size_t)li * P.units + unit) * D;
+        const int slot0 = (L.win_start + pos0) % P.R;
+        const int r = L.new_slot - slot0;
+        __nv_bfloat16* svh = reinterpret_cast<__nv_bfloat16*>(sv);
+        for (int c = lane; c < D; c += 32) {
+          const __nv_bfloat16 kv = kn[c], vv = vn[c];
+          window_store(win_k + wunit * P.R * D, win_v + wunit * P.R * D, L.new_slot, c, D, kv, vv);
+          sk[win_k_index(r, c, D)] = kv;
+          svh[win_v_index(r, c, D)] = vv;
+        }
+        __syncwarp();
+      }
+      window_warp<D, GQ>(st, qs, sk, sv, n_valid, P.sl2);
+    } else {
+      const int g0 = (j - L.wchunks) * kGroupsPerWarp;
+      packed_warp<D, BITS, GQ>(st, qr, sbuf, min(kGroupsPerWarp, L.n_groups - g0), P.sl2);
+    }
+    __syncwarp();   // the slot is read: refill it with the chunk two steps ahead
+    const int npos = warp + (n + 2) * NW;
+    if (advance(pre, npos) && lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      issue(slot, pre, npos);
+    }
+  }
+  if (ok && k_cur >= 0) deposit(k_cur);
+}
+
+template <int D, int BITS, int GQ>
+cudaError_t launch_one(const DecParams& P, const kvc_cache* c, const __nv_bfloat16* q, float* out,
+                       cudaStream_t stream) {
+  using C = DecCfg<D, BITS, GQ>;
+  // kernel attributes and the SM count are looked up once per device
+  static int n_sm[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(configured & (1ull << dev))) {
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (!n_sm[dev]) {
     e = cudaFuncSetAttribute(decode_kernel<D, BITS, GQ>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::total);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_kernel<D, BITS, GQ>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    if (dev < 64) configured |= 1ull << dev;
+    n_sm[dev] = n;
   }
-  decode_kernel<D, BITS, GQ><<<ctas, kThreads, sm, stream>>>(P, c->packed, c->win_k, c->win_v, q,
-                                                             out, c->dec_part, c->tickets);
+  const int total_units = P.n_layers * P.units;
+  const int grid = std::min(n_sm[dev], total_units);
+  decode_kernel<D, BITS, GQ><<<grid, C::kThreadsC, C::total, stream>>>(P, c->packed, c->win_k,
+                                                                       c->win_v, q, out);
   return cudaSuccess;
 }
 
 template <int D, int BITS>
-cudaError_t launch_g(const DecParams& P, int ctas, const kvc_cache* c, const __nv_bfloat16* q,
-                     float* out, cudaStream_t stream) {
+cudaError_t launch_g(const DecParams& P, const kvc_cache* c, const __nv_bfloat16* q, float* out,
+                     cudaStream_t stream) {
   switch (c->g) {
-    case 1: return launch_one<D, BITS, 1>(P, ctas, c, q, out, stream);
-    case 2: return launch_one<D, BITS, 2>(P, ctas, c, q, out, stream);
-    case 4: return launch_one<D, BITS, 4>(P, ctas, c, q, out, stream);
-    case 8: return launch_one<D, BITS, 8>(P, ctas, c, q, out, stream);
+    case 1: return launch_one<D, BITS, 1>(P, c, q, out, stream);
+    case 2: return launch_one<D, BITS, 2>(P, c, q, out, stream);
+    case 4: return launch_one<D, BITS, 4>(P, c, q, out, stream);
+    case 8: return launch_one<D, BITS, 8>(P, c, q, out, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-// CTAs of the decode kernel that fit on the device at once.
-int resident_ctas(const kvc_cache* c) {
-  static int cached[64][2][2][4] = {};
-  int dev = 0, n_sm = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 456;
-  const int di = c->dims.head_dim == 128, bi = c->dims.bits == 4;
-  const int gi = c->g == 1 ? 0 : c->g == 2 ? 1 : c->g == 4 ? 2 : 3;
-  int& v = cached[dev][di][bi][gi];
-  if (v) return v;
-  int per = 0;
-  cudaError_t e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-#define KVC_OCC(DD, BB2, GG)                                                                  \
-  if (e == cudaSuccess) {                                                                     \
-    e = cudaFuncSetAttribute(decode_kernel<DD, BB2, GG>,                                      \
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,                     \
-                             dyn_smem_bytes<DD, BB2, GG>());                                  \
-    if (e == cudaSuccess)                                                                     \
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_kernel<DD, BB2, GG>,     \
-                                                        kThreads, dyn_smem_bytes<DD, BB2, GG>()); \
-  }
-#define KVC_OCC_G(DD, BB2)                                                            \
-  switch (c->g) {                                                                      \
-    case 1: KVC_OCC(DD, BB2, 1) break; case 2: KVC_OCC(DD, BB2, 2) break;              \
-    case 4: KVC_OCC(DD, BB2, 4) break; default: KVC_OCC(DD, BB2, 8) break;             \
-  }
-  if (c->dims.head_dim == 128) { if (c->dims.bits == 2) { KVC_OCC_G(128, 2) } else { KVC_OCC_G(128, 4) } }
-  else { if (c->dims.bits == 2) { KVC_OCC_G(64, 2) } else { KVC_OCC_G(64, 4) } }
-#undef KVC_OCC_G
-#undef KVC_OCC
-  if (e != cudaSuccess || per < 1) { cudaGetLastError(); per = 1; }
-  v = n_sm * per;
-  return v;
-}
-
-// Shared host path: a non-null k_new selects the fused append + flush + attention.
+// Shared host path: a non-null k_new appends the step's token first. Without a
+// group flush in the step the decode launch stores the new token itself; when
+// some layer's window reaches R, the append kernel (which also quantizes the
+// flushed groups) runs first and the decode launch reads the updated cache.
 cudaError_t launch_common(const kvc_cache* c, int layer_begin, int layer_count,
                           const __nv_bfloat16* q, const __nv_bfloat16* k_new,
                           const __nv_bfloat16* v_new, const int* flush_flags, float* out,
@@ -936,7 +918,14 @@ cudaError_t launch_common(const kvc_cache* c, int layer_begin, int layer_count,
   const kvc_dims& d = c->dims;
   const int units = d.batch * d.n_kv_heads;
   const int D = d.head_dim, R = d.window_len;
-  const bool appending = k_new != nullptr;
+  bool appending = k_new != nullptr;
+  bool any_flush = false;
+  if (appending)
+    for (int i = 0; i < layer_count; ++i) any_flush = any_flush || flush_flags[i] != 0;
+  if (any_flush) {
+    cudaError_t e = launch_append(c, layer_begin, layer_count, k_new, v_new, flush_flags, stream);
+    if (e != cudaSuccess) return e;
+  }
   for (int base = 0; base < layer_count; base += KVC_MAX_LAUNCH_LAYERS) {
     const int cnt = layer_count - base < KVC_MAX_LAUNCH_LAYERS ? layer_count - base
                                                                : KVC_MAX_LAUNCH_LAYERS;
@@ -947,64 +936,39 @@ cudaError_t launch_common(const kvc_cache* c, int layer_begin, int layer_count,
     P.R = R;
     P.sl2 = 1.4426950408889634f / sqrtf((float)D);
     P.err = c->err;
-    P.k_new = appending ? k_new + (size_t)base * units * D : nullptr;
-    P.v_new = appending ? v_new + (size_t)base * units * D : nullptr;
-    int ctas = 0;
+    const bool fused = appending && !any_flush;
+    P.k_new = fused ? k_new + (size_t)base * units * D : nullptr;
+    P.v_new = fused ? v_new + (size_t)base * units * D : nullptr;
     for (int i = 0; i < cnt; ++i) {
       const LayerState& ls = c->L[layer_begin + base + i];
       DecLayer& L = P.L[i];
-      L.n_groups = ls.n_groups;
       L.cap_groups = ls.cap_groups;
       L.packed_off = (long long)ls.packed_off;
-      bool flush = false;
+      L.flush_start = -1;
+      L.n_ctas = 0;
+      L.cta_begin = 0;
       if (appending) {
-        flush = flush_flags[base + i] != 0;
-        L.new_slot = (ls.win_start + ls.win_len) % R;
-        L.flush_start = flush ? ls.win_start : -1;
+        const bool flush = flush_flags[base + i] != 0;
+        L.new_slot = fused ? (ls.win_start + ls.win_len) % R : -1;
+        L.n_groups = ls.n_groups + (flush ? 1 : 0);
         L.win_start = flush ? (ls.win_start + KVC_GROUP) % R : ls.win_start;
         L.win_len = ls.win_len + 1 - (flush ? KVC_GROUP : 0);
       } else {
         L.new_slot = -1;
-        L.flush_start = -1;
+        L.n_groups = ls.n_groups;
         L.win_start = ls.win_start;
         L.win_len = ls.win_len;
       }
       L.wchunks = (L.win_len + kSlotsPerWarp - 1) / kSlotsPerWarp;
-      L.cta_begin = 0;
-      L.n_ctas = 0;
-      L.cpc = 0;
+      L.pchunks = (L.n_groups + kGroupsPerWarp - 1) / kGroupsPerWarp;
     }
-    // chunks per CTA: the smallest multiple of the warp count that keeps the whole
-    // grid resident in one wave
-    const int capacity = resident_ctas(c);
-    int cpc = kDecWarps;
-    for (;;) {
-      ctas = 0;
-      for (int i = 0; i < cnt; ++i) {
-        const DecLayer& L = P.L[i];
-        const int chunks = L.wchunks + (L.n_groups + kGroupsPerWarp - 1) / kGroupsPerWarp;
-        ctas += units * std::max(1, (chunks + cpc - 1) / cpc);
-      }
-      if (ctas <= capacity || cpc >= 1024) break;
-      cpc += kDecWarps;
-    }
-    ctas = 0;
-    for (int i = 0; i < cnt; ++i) {
-      DecLayer& L = P.L[i];
-      const int chunks = L.wchunks + (L.n_groups + kGroupsPerWarp - 1) / kGroupsPerWarp;
-      L.cpc = cpc;
-      L.n_ctas = std::max(1, (chunks + cpc - 1) / cpc);
-      L.cta_begin = ctas;
-      ctas += units * L.n_ctas;
-    }
-    if ((size_t)ctas * c->g * (D + 2) > c->dec_part_elems) return cudaErrorInvalidValue;
     const __nv_bfloat16* qb = q + (size_t)base * units * c->g * D;
     float* ob = out + (size_t)base * units * c->g * D;
     cudaError_t e;
-    if (D == 128 && d.bits == 2) e = launch_g<128, 2>(P, ctas, c, qb, ob, stream);
-    else if (D == 128 && d.bits == 4) e = launch_g<128, 4>(P, ctas, c, qb, ob, stream);
-    else if (D == 64 && d.bits == 2) e = launch_g<64, 2>(P, ctas, c, qb, ob, stream);
-    else if (D == 64 && d.bits == 4) e = launch_g<64, 4>(P, ctas, c, qb, ob, stream);
+    if (D == 128 && d.bits == 2) e = launch_g<128, 2>(P, c, qb, ob, stream);
+    else if (D == 128 && d.bits == 4) e = launch_g<128, 4>(P, c, qb, ob, stream);
+    else if (D == 64 && d.bits == 2) e = launch_g<64, 2>(P, c, qb, ob, stream);
+    else if (D == 64 && d.bits == 4) e = launch_g<64, 4>(P, c, qb, ob, stream);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
     count_launches(1);

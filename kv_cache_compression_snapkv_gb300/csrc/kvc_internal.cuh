@@ -189,10 +189,7 @@ struct kvc_cache {
   float2* rowstat = nullptr;  size_t rowstat_elems = 0;
   float* scores = nullptr;
   float* pooled = nullptr;    size_t score_elems = 0;
-  float* dec_part = nullptr;  size_t dec_part_elems = 0;
-  unsigned* tickets = nullptr; size_t n_tickets = 0;
   unsigned* err = nullptr;     // device error word (bounded waits that gave up)
-  int max_ctas_per_unit = 0;
   int last_scored_layer = -1;
   std::vector<void*> allocations;
 };
@@ -229,12 +226,10 @@ cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
 cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float* pooled,
                                   int32_t* kept_out, int k_sel, cudaStream_t stream);
 
-// Decode work decomposition shared by the host (sizing) and the kernel.
-constexpr int kDecWarps = 4;
-constexpr int kGroupsPerCta = 16;      // packed groups per decode CTA (4 per warp)
-constexpr int kWinSlotsPerCta = 128;   // window slots per decode CTA (32 per warp)
-inline int packed_ctas(int n_groups) { return (n_groups + kGroupsPerCta - 1) / kGroupsPerCta; }
-inline int window_ctas(int win_len) { return (win_len + kWinSlotsPerCta - 1) / kWinSlotsPerCta; }
+// Decode work decomposition: a unit's work is cut into chunks of 16 window slots
+// or 2 packed groups.
+constexpr int kDecGroupsPerChunk = 2;
+constexpr int kDecSlotsPerChunk = 16;
 
 // Scoring decomposition.
 constexpr int kScoreChunk = 128;       // keys per scoring CTA

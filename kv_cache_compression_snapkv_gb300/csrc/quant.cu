@@ -50,15 +50,10 @@ gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
   for (int i = threadIdx.x; i < KVC_GROUP * CH; i += kThreads) {
     const int t = i / CH, ch = i % CH;
     const int idx = kp ? kp[j * KVC_GROUP + t] : j * KVC_GROUP + t;
-    const uint4 uk = __ldg(reinterpret_cast<const uint4*>(K + (size_t)idx * D) + ch);
-    const uint4 uv = __ldg(reinterpret_cast<const uint4*>(V + (size_t)idx * D) + ch);
-    const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(&uk);
-    const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&uv);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      s.k[t][ch * 8 + e] = __bfloat162float(hk[e]);
-      s.v[t][ch * 8 + e] = __bfloat162float(hv[e]);
-    }
+    *reinterpret_cast<uint4*>(&s.k[t][ch * 8]) =
+        __ldg(reinterpret_cast<const uint4*>(K + (size_t)idx * D) + ch);
+    *reinterpret_cast<uint4*>(&s.v[t][ch * 8]) =
+        __ldg(reinterpret_cast<const uint4*>(V + (size_t)idx * D) + ch);
   }
   __syncthreads();
   uint8_t* blk = packed + ((size_t)unit * cap_groups + j) * block_bytes;
@@ -95,8 +90,8 @@ append_kernel(AppendParams P, int layer_begin, int units, int R, const __nv_bflo
   for (int i = threadIdx.x; i < KVC_GROUP * D; i += kThreads) {
     const int t = i / D, c = i % D;
     const int sl = fs + t;
-    s.k[t][c] = __bfloat162float(window_load_k(wk, sl, c, D));
-    s.v[t][c] = __bfloat162float(window_load_v(wv, sl, c, D));
+    s.k[t][c] = window_load_k(wk, sl, c, D);
+    s.v[t][c] = window_load_v(wv, sl, c, D);
   }
   __syncthreads();
   uint8_t* blk = packed + P.packed_off[lrel] +

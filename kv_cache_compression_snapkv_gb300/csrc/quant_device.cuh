@@ -32,14 +32,15 @@ __device__ __forceinline__ int quant_code(float x, float Zf, float Sf, int bits)
   return c < 0 ? 0 : (c > top ? top : c);
 }
 
-// Staging of one group: 32 key rows and 32 value rows (fp32, natural channel
-// order), their codes, and partial min/max when a group is split over threads.
+// Staging of one group: 32 key rows and 32 value rows (bf16 as stored, natural
+// channel order, rows padded by 8 elements), their codes, and partial min/max
+// when a group is split over threads.
 template <int D, int NT>
 struct GroupSmem {
   static constexpr int NP = NT / D;   // threads per quantization group
   static_assert(NP >= 1 && KVC_GROUP % NP == 0, "thread count must be a multiple of D");
-  float k[KVC_GROUP][D + 1];
-  float v[KVC_GROUP][D + 1];
+  __nv_bfloat16 k[KVC_GROUP][D + 8];
+  __nv_bfloat16 v[KVC_GROUP][D + 8];
   uint8_t kc[KVC_GROUP][D];
   uint8_t vc[KVC_GROUP][D];
   float klo[NP][D], khi[NP][D], vlo[NP][D], vhi[NP][D];
@@ -58,19 +59,24 @@ __device__ void quantize_block(GroupSmem<D, NT>& s, uint8_t* __restrict__ blk) {
   const int g = threadIdx.x % D, part = threadIdx.x / D;
   const bool act = threadIdx.x < NP * D;
   const int vt = g / NGC, vgc = g % NGC;       // value group g = (token vt, channels vgc*32..)
-  const float* vrow = &s.v[vt][vgc * KVC_GROUP + part * PER];
+  const __nv_bfloat16* vrow = &s.v[vt][vgc * KVC_GROUP + part * PER];
   if (act) {
-    float lo = s.k[part * PER][g], hi = lo;
+    float lo = __bfloat162float(s.k[part * PER][g]), hi = lo;
 #pragma unroll
     for (int t = 1; t < PER; ++t) {
-      lo = fminf(lo, s.k[part * PER + t][g]);
-      hi = fmaxf(hi, s.k[part * PER + t][g]);
+      const float x = __bfloat162float(s.k[part * PER + t][g]);
+      lo = fminf(lo, x);
+      hi = fmaxf(hi, x);
     }
     s.klo[part][g] = lo;
     s.khi[part][g] = hi;
-    float vl = vrow[0], vh = vl;
+    float vl = __bfloat162float(vrow[0]), vh = vl;
 #pragma unroll
-    for (int j = 1; j < PER; ++j) { vl = fminf(vl, vrow[j]); vh = fmaxf(vh, vrow[j]); }
+    for (int j = 1; j < PER; ++j) {
+      const float x = __bfloat162float(vrow[j]);
+      vl = fminf(vl, x);
+      vh = fmaxf(vh, x);
+    }
     s.vlo[part][g] = vl;
     s.vhi[part][g] = vh;
   }
@@ -83,7 +89,8 @@ __device__ void quantize_block(GroupSmem<D, NT>& s, uint8_t* __restrict__ blk) {
     group_params(lo, hi, BITS, S, Z, Sf, Zf);
 #pragma unroll
     for (int t = 0; t < PER; ++t)
-      s.kc[part * PER + t][g] = (uint8_t)quant_code(s.k[part * PER + t][g], Zf, Sf, BITS);
+      s.kc[part * PER + t][g] =
+          (uint8_t)quant_code(__bfloat162float(s.k[part * PER + t][g]), Zf, Sf, BITS);
     if (part == 0) { kS[kperm(g, D)] = S; kZ[kperm(g, D)] = Z; }
   }
   if (act) {
@@ -94,7 +101,8 @@ __device__ void quantize_block(GroupSmem<D, NT>& s, uint8_t* __restrict__ blk) {
     group_params(lo, hi, BITS, S, Z, Sf, Zf);
 #pragma unroll
     for (int j = 0; j < PER; ++j)
-      s.vc[vt][vgc * KVC_GROUP + part * PER + j] = (uint8_t)quant_code(vrow[j], Zf, Sf, BITS);
+      s.vc[vt][vgc * KVC_GROUP + part * PER + j] =
+          (uint8_t)quant_code(__bfloat162float(vrow[j]), Zf, Sf, BITS);
     if (part == 0) { vS[vs_index(vt, vgc, NGC)] = S; vZ[vsz_index(vt, vgc, NGC)] = Z; }
   }
   __syncthreads();
