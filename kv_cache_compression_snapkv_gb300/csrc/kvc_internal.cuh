@@ -219,6 +219,13 @@ cudaError_t launch_decode(const kvc_cache* c, int layer_begin, int layer_count,
                           const __nv_bfloat16* q, float* out, cudaStream_t stream);
 cudaError_t launch_export(const kvc_cache* c, int layer, const kvc_export* dst,
                           cudaStream_t stream);
+// Scoring on the tensor cores (row statistics, their merge into row normalisers,
+// per-key column sums); err may be NULL.
+cudaError_t launch_score_tc(const kvc_dims& d, const __nv_bfloat16* q_obs,
+                            const __nv_bfloat16* k, float2* stats, float* rowbias, float* scores,
+                            unsigned* err, cudaStream_t stream);
+cudaError_t launch_score_combine(const float2* stats, int nch, int M, int units, float* rowbias,
+                                 cudaStream_t stream);
 // Selection launches with explicit scratch (allocation-free entry point).
 cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
                               const __nv_bfloat16* k, float2* stats, float* rowbias,

@@ -201,8 +201,235 @@ pool_topk_kernel(const float* __restrict__ scores, float* __restrict__ pooled, i
   }
 }
 
+// ------------------------------------------------------------ cluster version
+// One thread-block cluster of kCluster CTAs per (sequence, kv head). CTA r pools
+// and selects over its segment [r * seg, (r + 1) * seg) of the scores (staged in
+// shared memory with a halo of (w - 1) / 2 on each side). Each radix pass builds a
+// 256-bin histogram per CTA; the CTAs read each other's histograms through
+// distributed shared memory after one cluster barrier, so every CTA takes the same
+// decision. The ordered compaction adds the (greater, equal) counts of the
+// preceding CTAs of the cluster.
+constexpr int kCluster = 8;
+constexpr int kCThreads = 256;
+constexpr int kCWarps = kCThreads / 32;
+constexpr int kMaxSeg = 24 * 1024;   // elements per CTA (two fp32 copies in shared memory)
+
+struct ClusterSmem {
+  unsigned whist[kCWarps][256];   // per-warp histograms of the current pass
+  unsigned hist[2][256];          // this CTA's histogram, by pass parity (read remotely)
+  unsigned total[256];            // the cluster's histogram
+  unsigned cnt[2];                // (greater, equal) counts of this segment (read remotely)
+  unsigned warp_gt[kCWarps], warp_eq[kCWarps];
+  unsigned base_gt, base_eq;
+  unsigned sel_bin, krem;
+};
+
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ unsigned ld_cluster_u32(const unsigned* p, unsigned rank) {
+  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+  unsigned ra, v;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kCThreads)
+pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ pooled, int ns,
+                         int w, int k_sel, int32_t* __restrict__ kept) {
+  __shared__ ClusterSmem s;
+  extern __shared__ __align__(16) float dyn[];
+  const unsigned rank = cluster_rank();
+  const int unit = blockIdx.x / kCluster;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = (ns + kCluster - 1) / kCluster;
+  const int i0 = min(ns, (int)rank * seg), i1 = min(ns, i0 + seg);
+  const int n_loc = i1 - i0;
+  const int hw = (w - 1) / 2;
+  const float* sc = scores + (size_t)unit * ns;
+  float* pg = pooled + (size_t)unit * ns;
+  int32_t* out = kept + (size_t)unit * k_sel;
+  float* sx = dyn;                    // scores of [i0 - hw, i1 + hw) (-inf outside the row)
+  float* pl = dyn + seg + 2 * hw;     // pooled scores of [i0, i1)
+
+  // 1. stage the segment with its halo: every element an independent 4-byte
+  //    asynchronous copy (all in flight at once); -inf outside the row
+  const int n_halo = n_loc + 2 * hw;
+  for (int t = threadIdx.x; t < n_halo; t += kCThreads) {
+    const int i = i0 - hw + t;
+    if (i >= 0 && i < ns) {
+      const unsigned d = (unsigned)__cvta_generic_to_shared(sx + t);
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" :: "r"(d), "l"(sc + i) : "memory");
+    } else {
+      sx[t] = -INFINITY;
+    }
+  }
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+  __syncthreads();
+  // 2. max-pool (window clipped to the row: the halo outside it is -inf)
+  for (int t = threadIdx.x; t < n_loc; t += kCThreads) {
+    float m = sx[t + hw];
+    for (int d = 0; d < 2 * hw + 1; ++d) m = fmaxf(m, sx[t + d]);
+    pl[t] = m;
+    pg[i0 + t] = m;
+  }
+  if (k_sel >= ns) {   // everything is kept
+    for (int t = threadIdx.x; t < n_loc; t += kCThreads) out[i0 + t] = i0 + t;
+    return;
+  }
+  if (k_sel <= 0) return;
+  if (threadIdx.x == 0) s.krem = (unsigned)k_sel;
+  __syncthreads();
+
+  // 3. radix select of the k-th largest pooled score (fp32 bits: scores are >= 0)
+  unsigned prefix = 0, mask = 0;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = threadIdx.x; i < kCWarps * 256; i += kCThreads) (&s.whist[0][0])[i] = 0u;
+    __syncthreads();
+    for (int t = threadIdx.x; t < n_loc; t += kCThreads) {
+      const unsigned u = __float_as_uint(pl[t]);
+      if ((u & mask) == prefix) atomicAdd(&s.whist[warp][(u >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    {
+      const int b = threadIdx.x;   // kCThreads == 256 bins
+      unsigned h = 0;
+#pragma unroll
+      for (int ww = 0; ww < kCWarps; ++ww) h += s.whist[ww][b];
+      s.hist[pass & 1][b] = h;
+    }
+    cluster_sync_all();   // every CTA's histogram of this pass is complete
+    {
+      const int b = threadIdx.x;
+      unsigned v[kCluster];
+#pragma unroll
+      for (int r = 0; r < kCluster; ++r) v[r] = ld_cluster_u32(&s.hist[pass & 1][b], (unsigned)r);
+      unsigned h = 0;
+#pragma unroll
+      for (int r = 0; r < kCluster; ++r) h += v[r];
+      s.total[b] = h;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins [8l, 8l + 8); suffix sums from the top bin down
+      unsigned own = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) own += s.total[8 * lane + j];
+      unsigned suf = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += t;
+      }
+      const unsigned above = suf - own;
+      const unsigned krem = s.krem;
+      __syncwarp();
+      if (suf >= krem && above < krem) {
+        unsigned cum = above;
+        for (int b = 8 * lane + 7; b >= 8 * lane; --b) {
+          const unsigned h = s.total[b];
+          if (cum + h >= krem) { s.sel_bin = (unsigned)b; s.krem = krem - cum; break; }
+          cum += h;
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= s.sel_bin << shift;
+    mask |= 255u << shift;
+  }
+  const unsigned tau = prefix, need_eq = s.krem;
+
+  // 4. ordered compaction: warp w owns the contiguous span [w*span, (w+1)*span) of
+  //    the segment; the counts of the preceding warps and CTAs give the offsets
+  const int span = (n_loc + kCWarps - 1) / kCWarps;
+  const int w0 = min(n_loc, warp * span), w1 = min(n_loc, w0 + span);
+  unsigned gt = 0, eq = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int t = base + lane;
+    const unsigned u = t < w1 ? __float_as_uint(pl[t]) : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, t < w1 && u > tau));
+    eq += __popc(__ballot_sync(0xffffffffu, t < w1 && u == tau));
+  }
+  if (lane == 0) { s.warp_gt[warp] = gt; s.warp_eq[warp] = eq; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned g = 0, e = 0;
+    for (int ww = 0; ww < kCWarps; ++ww) { g += s.warp_gt[ww]; e += s.warp_eq[ww]; }
+    s.cnt[0] = g;
+    s.cnt[1] = e;
+  }
+  cluster_sync_all();
+  if (warp == 0) {
+    // lanes r < rank read CTA r's counts; warp sums
+    unsigned g = 0, e = 0;
+    if (lane < (int)rank) { g = ld_cluster_u32(&s.cnt[0], (unsigned)lane); e = ld_cluster_u32(&s.cnt[1], (unsigned)lane); }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      g += __shfl_xor_sync(0xffffffffu, g, o);
+      e += __shfl_xor_sync(0xffffffffu, e, o);
+    }
+    if (lane == 0) { s.base_gt = g; s.base_eq = e; }
+  }
+  __syncthreads();
+  unsigned egt = s.base_gt, eeq = s.base_eq;
+  for (int ww = 0; ww < warp; ++ww) { egt += s.warp_gt[ww]; eeq += s.warp_eq[ww]; }
+  unsigned pos = egt + (eeq < need_eq ? eeq : need_eq);
+  unsigned eq_seen = eeq;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int t = base + lane;
+    const unsigned u = t < w1 ? __float_as_uint(pl[t]) : 0u;
+    const bool is_gt = t < w1 && u > tau, is_eq = t < w1 && u == tau;
+    const unsigned beq = __ballot_sync(0xffffffffu, is_eq);
+    const bool take = is_gt || (is_eq && eq_seen + __popc(beq & lt) < need_eq);
+    const unsigned bt = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const unsigned p = pos + __popc(bt & lt);
+      if (p < (unsigned)k_sel) out[p] = i0 + t;   // bounded even if the select were wrong
+    }
+    pos += __popc(bt);
+    eq_seen += __popc(beq);
+  }
+  cluster_sync_all();   // no CTA leaves while another may still read its shared memory
+}
+
+cudaError_t launch_topk_cluster(const float* scores, float* pooled, int units, int ns, int w,
+                                int k_sel, int32_t* kept, cudaStream_t stream) {
+  const int seg = (ns + kCluster - 1) / kCluster;
+  const size_t sm = (size_t)(2 * seg + (w - 1)) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(pool_topk_cluster_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(units * kCluster);
+  cfg.blockDim = dim3(kCThreads);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, pool_topk_cluster_kernel, scores, pooled, ns, w, k_sel, kept);
+  count_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_topk(const float* scores, float* pooled, int units, int ns, int w, int k_sel,
                         int32_t* kept, cudaStream_t stream) {
+  if ((ns + kCluster - 1) / kCluster <= kMaxSeg && w <= 129)
+    return launch_topk_cluster(scores, pooled, units, ns, w, k_sel, kept, stream);
   if (ns <= kSmemMax) {
     const size_t sm = (size_t)ns * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(pool_topk_kernel<true>,
