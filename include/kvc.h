@@ -270,9 +270,9 @@ kvc_status kvc_scores_layer(kvc_cache* cache, float* scores, float* pooled, void
  *   value a call reads is written by that call first), so calls that overlap on
  *   the GPU race: serialize them. The first call on a device looks up the
  *   array's device address; make it before any stream capture.
- *   Scratch needed: B*H*ceil(n/128)*g*alpha*8 + B*H*g*alpha*4 + B*H*(n-alpha)*4
- *   bytes (+ the same again for scores when `scores` is NULL), each part
- *   rounded up to 256 bytes.
+ *   Scratch needed: B*H*(4*ceil(n/128)+4)*g*alpha*8 + B*H*g*alpha*4 +
+ *   B*H*(n-alpha)*4 bytes (+ the same again for scores when `scores` is NULL),
+ *   each part rounded up to 256 bytes.
  *   q_obs: device bf16 [B][Hq][alpha][d]; k: device bf16 [B][H][n][d];
  *   kept:  device int32 [B][H][min(budget, n - alpha)] (written, ascending);
  *   scores: optional device fp32 [B][H][n - alpha] (written when not NULL).

@@ -132,8 +132,7 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
   bool ok = c->packed && c->win_k && c->win_v && c->err;
   if (ok && scoring) {
     const int M = g * d.obs_window;
-    const int nch = (d.prompt_len + kvc::kScoreChunk - 1) / kvc::kScoreChunk;
-    c->stats_elems = (size_t)units * nch * M;
+    c->stats_elems = (size_t)units * kvc::score_stat_chunks(d.prompt_len) * M;
     c->rowstat_elems = (size_t)units * M;
     c->score_elems = (size_t)units * ns;
     c->stats = static_cast<float2*>(dev_alloc(c, c->stats_elems * 8));

@@ -238,7 +238,8 @@ cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float*
 constexpr int kDecGroupsPerChunk = 2;
 constexpr int kDecSlotsPerChunk = 16;
 
-// Scoring decomposition.
-constexpr int kScoreChunk = 128;       // keys per scoring CTA
+// Scoring: entries of the per-row statistics kept for a prompt of n keys (up to
+// four column splits per key tile of at least 128 keys).
+inline size_t score_stat_chunks(int n) { return 4 * (size_t)((n + 127) / 128) + 4; }
 
 }  // namespace kvc

@@ -72,7 +72,7 @@ extern "C" kvc_status kvc_select_noalloc(const kvc_dims* dims, int32_t budget, c
   const size_t units = (size_t)d.batch * d.n_kv_heads;
   const size_t M = (size_t)g * d.obs_window;
   const size_t ns = (size_t)d.prompt_len - d.obs_window;
-  const size_t nch = ((size_t)d.prompt_len + kvc::kScoreChunk - 1) / kvc::kScoreChunk;
+  const size_t nch = kvc::score_stat_chunks(d.prompt_len);
   const size_t stats_b = align256(units * nch * M * sizeof(float2));
   const size_t bias_b = align256(units * M * sizeof(float));
   const size_t score_b = align256(units * ns * sizeof(float));

@@ -33,7 +33,9 @@
 namespace kvc {
 namespace {
 
-constexpr int kTcThreads = 192;   // producer, MMA, 4 epilogue warps
+constexpr int kEpiWarps = 16;                      // four per tensor-memory lane quarter
+constexpr int kSplit = kEpiWarps / 4;              // column splits of a tile
+constexpr int kTcThreads = 64 + 32 * kEpiWarps;    // producer, MMA, epilogue warps
 constexpr int kTmemCols = 512;
 
 template <int D, int PASS, int QT>
@@ -43,15 +45,23 @@ struct TcCfg {
   static constexpr int KROWS = PASS == 0 ? (QT == 1 ? 256 : 128) : 128;   // keys per tile
   static constexpr int QBYTES = QROWS * D * 2;
   static constexpr int KBYTES = KROWS * D * 2;
-  static constexpr int STAGES = PASS == 0 ? (QT == 1 ? 2 : 3) : 4;
+  // as many key stages as shared memory holds: the bytes in flight per SM set the
+  // DRAM throughput a pass reaches
+  static constexpr int STAGES = PASS == 0 ? (QT == 1 ? 3 : 5) : (QT == 1 ? 5 : 4);
+  // tensor-memory accumulator buffers: two of 256 columns for the row-stats pass,
+  // four of 128 columns for the column pass (two of 256 when M > 128)
+  static constexpr int NBUF = (PASS == 1 && QT == 1) ? 4 : 2;
+  static constexpr int BUFCOLS = 512 / NBUF;
   static constexpr int oQ = 0;
   static constexpr int oK = QBYTES;
   static constexpr int oBar = oK + STAGES * KBYTES;
-  // full[S], empty[S], qfull, qempty, tfull[2], tempty[2], drain
-  static constexpr int NBAR = 2 * STAGES + 7;
+  // full[S], empty[S], qfull, qempty, tfull[NBUF], tempty[NBUF], drain
+  static constexpr int NBAR = 2 * STAGES + 3 + 2 * NBUF;
   static constexpr int oTmem = oBar + NBAR * 8;
   static constexpr int oBias = (oTmem + 16 + 15) / 16 * 16;
-  static constexpr int total = oBias + 256 * 4 + 1024;   // + alignment slack
+  static constexpr int BIASB = PASS == 1 ? 4 * 256 * 4 : 0;   // column pass: 4 bias copies
+  static constexpr int total = oBias + BIASB + 1024;            // + alignment slack
+  static_assert(total <= 232448, "fits the shared memory of one CTA");
   static_assert(QBYTES % 1024 == 0 && KBYTES % 1024 == 0, "1024-byte aligned tiles");
 };
 
@@ -85,8 +95,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   uint64_t* qfull = bars + 2 * C::STAGES;
   uint64_t* qempty = qfull + 1;
   uint64_t* tfull = qfull + 2;
-  uint64_t* tempty = qfull + 4;
-  uint64_t* drain = qfull + 6;
+  uint64_t* tempty = tfull + C::NBUF;
+  uint64_t* drain = tempty + C::NBUF;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(dsm + C::oTmem);
   float* sbias = reinterpret_cast<float*>(dsm + C::oBias);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -99,7 +109,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
     for (int s = 0; s < C::STAGES; ++s) { tc::mbar_init(&full[s], 1); tc::mbar_init(&empty[s], 1); }
     tc::mbar_init(qfull, 1);
     tc::mbar_init(qempty, 1);
-    for (int b = 0; b < 2; ++b) { tc::mbar_init(&tfull[b], 1); tc::mbar_init(&tempty[b], 4); }
+    for (int b = 0; b < C::NBUF; ++b) {
+      tc::mbar_init(&tfull[b], 1);
+      tc::mbar_init(&tempty[b], PASS == 0 ? kEpiWarps : 4);
+    }
     tc::mbar_init(drain, 1);
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&tmK);
@@ -167,12 +180,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           ++nq;
           cur = unit;
         }
-        const int b = k & 1, rb = k >> 1;
+        const int b = k % C::NBUF, rb = k / C::NBUF;
         if (rb > 0) ok = tc::mbar_wait(&tempty[b], (uint32_t)((rb - 1) & 1), a.err, 16u);
         if (!ok) break;
         tc::fence_after_sync();
         const uint32_t sQa = tc::saddr(sQ), sKa = tc::saddr(sK + s * C::KBYTES);
-        const uint32_t dcol = tbase + (uint32_t)(b * 256);
+        const uint32_t dcol = tbase + (uint32_t)(b * C::BUFCOLS);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int kb = kk / 4, kin = (kk % 4) * 32;
@@ -200,85 +213,127 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
     }
   } else {
     // ------------------------------------------------------------- epilogue
+    const int e = warp - 2;
     const int sub = warp & 3;                    // tensor-memory lane quarter
     const int row_in = sub * 32 + lane;          // row (pass 0) or key (pass 1) in the tile
     const uint32_t lane_addr = (uint32_t)(sub * 32) << 16;
-    const int ep = threadIdx.x - 64;             // 0 .. 127
-    int cur = -1;
-    for (int it = it0, k = 0; it < it1; ++it, ++k) {
-      const int unit = it / a.tiles, tile = it % a.tiles;
-      if (PASS == 1 && unit != cur) {
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        for (int j = ep; j < 256; j += 128)
-          sbias[j] = j < a.M ? a.rowbias[(size_t)unit * a.M + j] : INFINITY;
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        cur = unit;
-      }
-      const int b = k & 1, rb = k >> 1;
-      // on a failed wait every warp keeps the loop (the named barriers above stay
-      // matched) but stores nothing
-      if (ok) ok = tc::mbar_wait(&tfull[b], (uint32_t)(rb & 1), a.err, 32u);
-      ok = __all_sync(0xffffffffu, ok);
-      tc::fence_after_sync();
-      const uint32_t tcol = tbase + lane_addr + (uint32_t)(b * 256);
-      if (PASS == 0) {
+    if (PASS == 0) {
+      // every tile: warp e reads lane quarter e % 4 and column split e / 4
+      const int split = e >> 2;
+      for (int it = it0, k = 0; it < it1; ++it, ++k) {
+        const int unit = it / a.tiles, tile = it % a.tiles;
+        const int b = k % C::NBUF, rb = k / C::NBUF;
+        if (ok) ok = tc::mbar_wait(&tfull[b], (uint32_t)(rb & 1), a.err, 32u);
+        ok = __all_sync(0xffffffffu, ok);
+        tc::fence_after_sync();
+        const uint32_t tcol = tbase + lane_addr + (uint32_t)(b * C::BUFCOLS);
+        constexpr int HC = C::KROWS / kSplit;     // columns of this split
+        static_assert(HC % 32 == 0, "whole 32-column loads");
+        const int key0 = tile * C::KROWS + split * HC;
+        // only the tiles reaching the observation window need the causal / range mask
+        const bool masked = key0 + HC > a.n - a.alpha;
 #pragma unroll
         for (int mt = 0; mt < QT; ++mt) {
           const int r = mt * 128 + row_in;
           const int pos = a.n - a.alpha + (r % a.alpha);
-          const int key0 = tile * C::KROWS;
+          const int lim = min(a.n - 1, pos) - key0;   // last visible column of this split
           float m = -INFINITY, ssum = 0.f;
-          for (int c0 = 0; c0 < C::KROWS; c0 += 32) {
-            float v[32];
-            tc::tmem_ld32(tcol + (uint32_t)(mt * C::KROWS + c0), v);
-            const bool full_valid = key0 + c0 + 31 < a.n - a.alpha;
-            float cm = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int key = key0 + c0 + j;
-              float x = v[j] * a.sl2;
-              if (!full_valid && (key >= a.n || key > pos)) x = -INFINITY;
-              v[j] = x;
-              cm = fmaxf(cm, x);
+          for (int c0 = 0; c0 < HC; c0 += 32) {
+            float v[32];
+            tc::tmem_ld32(tcol + (uint32_t)(mt * C::KROWS + split * HC + c0), v);
+            if (masked) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = (c0 + j <= lim) ? v[j] : -INFINITY;
             }
+            float mx[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mx[j] = fmaxf(fmaxf(v[j], v[j + 8]), fmaxf(v[j + 16], v[j + 24]));
+            const float cm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             if (cm != -INFINITY) {
-              if (cm > m) {
-                ssum = (m == -INFINITY) ? 0.f : ssum * exp2f(m - cm);
-                m = cm;
+              const float cms = cm * a.sl2;
+              if (cms > m) {
+                ssum = (m == -INFINITY) ? 0.f : ssum * exp2f(m - cms);
+                m = cms;
               }
-              float t = 0.f;
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
-                float e;
-                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(v[j] - m));
-                t += e;
+                float x = fmaf(v[j], a.sl2, -m);
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(v[j]) : "f"(x));
               }
-              ssum += t;
-            }
-          }
-          if (ok && r < a.M) a.stats[((size_t)unit * a.M + r) * a.tiles + tile] = make_float2(m, ssum);
-        }
-      } else {
-        const int MP = (a.M + 15) / 16 * 16;
-        float acc = 0.f;
-        for (int c0 = 0; c0 < MP; c0 += 32) {
-          float v[32];
-          tc::tmem_ld32(tcol + (uint32_t)c0, v);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (c0 + j < a.M) {
-              float e;
-              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fmaf(v[j], a.sl2, -sbias[c0 + j])));
-              acc += e;
+              for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+                for (int j = 0; j < w; ++j) v[j] += v[j + w];
+              ssum += v[0];
             }
           }
+          if (ok && r < a.M)
+            a.stats[((size_t)unit * a.M + r) * (kSplit * a.tiles) + kSplit * tile + split] =
+                make_float2(m, ssum);
         }
-        const int key = tile * C::KROWS + row_in;
-        if (ok && key < a.ns) a.scores[(size_t)unit * a.ns + key] = acc;
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&tempty[b]);
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tempty[b]);
+    } else {
+      // group gi = e / 4 (four warps, one per lane quarter) takes the tiles k with
+      // k % NBUF == gi, all MP columns: no data crosses warps
+      const int gi = e >> 2;
+      const int MP = (a.M + 15) / 16 * 16;
+      float* gbias = sbias + gi * 256;           // this group's negated row normalisers
+      int cur = -1;
+      if (gi < C::NBUF) {
+        for (int it = it0 + gi, k = gi; it < it1; it += C::NBUF, k += C::NBUF) {
+          const int unit = it / a.tiles, tile = it % a.tiles;
+          if (unit != cur) {
+            asm volatile("bar.sync %0, 128;" :: "r"(1 + gi) : "memory");
+            for (int j = sub * 32 + lane; j < 256; j += 128)
+              gbias[j] = j < a.M ? -a.rowbias[(size_t)unit * a.M + j] : -INFINITY;
+            asm volatile("bar.sync %0, 128;" :: "r"(1 + gi) : "memory");
+            cur = unit;
+          }
+          const int b = gi, rb = k / C::NBUF;
+          if (ok) ok = tc::mbar_wait(&tfull[b], (uint32_t)(rb & 1), a.err, 32u);
+          ok = __all_sync(0xffffffffu, ok);
+          tc::fence_after_sync();
+          const uint32_t tcol = tbase + lane_addr + (uint32_t)(b * C::BUFCOLS);
+          float acc = 0.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < MP; c0 += 32) {
+            float v[32];
+            tc::tmem_ld32(tcol + (uint32_t)c0, v);
+            const float4* nb4 = reinterpret_cast<const float4*>(gbias + c0);
+            if (c0 + 32 <= a.M) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 4) {
+                const float4 nb = nb4[j / 4];
+                v[j] = fmaf(v[j], a.sl2, nb.x);
+                v[j + 1] = fmaf(v[j + 1], a.sl2, nb.y);
+                v[j + 2] = fmaf(v[j + 2], a.sl2, nb.z);
+                v[j + 3] = fmaf(v[j + 3], a.sl2, nb.w);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                v[j] = (c0 + j < a.M) ? fmaf(v[j], a.sl2, gbias[c0 + j]) : -INFINITY;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(v[j]) : "f"(v[j]));
+#pragma unroll
+            for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+              for (int j = 0; j < w; ++j) v[j] += v[j + w];
+            acc += v[0];
+          }
+          const int key = tile * C::KROWS + row_in;
+          if (ok && key < a.ns) a.scores[(size_t)unit * a.ns + key] = acc;
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&tempty[b]);
+        }
+      }
     }
   }
 
@@ -375,7 +430,7 @@ cudaError_t run_passes(const kvc_dims& d, const __nv_bfloat16* q_obs, const __nv
   const int tiles0 = a.tiles;
   e = qt == 1 ? launch_pass<D, 0, 1>(mk, mq, a, stream) : launch_pass<D, 0, 2>(mk, mq, a, stream);
   if (e != cudaSuccess) return e;
-  e = launch_score_combine(stats, tiles0, M, units, rowbias, stream);
+  e = launch_score_combine(stats, kSplit * tiles0, M, units, rowbias, stream);
   if (e != cudaSuccess) return e;
   // per-key column sums over the scored keys
   a.tiles = (a.ns + 127) / 128;
