@@ -33,11 +33,16 @@
 //     o_c = sum_t (p_t S_t,gc) code_tc + sum_t p_t Z_t,gc.
 // Both code sums run on the tensor cores (mma m16n8k16, fp16 operands, fp32
 // accumulate): codes are unpacked in registers to exact fp16 integers, and the
-// fp16 operand products (q_c S_c, p_t S_t) are split into hi + lo fp16 parts that
-// occupy separate rows of the 16-row operand (rows 0..g-1 hi, g..2g-1 lo), so the
-// rounding of the operand does not limit accuracy. The zero-point sums are small
-// extra tensor-core products (q against the warp's groups' key zeros; p against
-// the value zeros). The window runs the same flow on bf16 operands.
+// fp16 operand products (q_c S_c, p_t S_t) are split into hi + lo fp16 parts in
+// adjacent columns of the 8-column operand (column 2h hi, 2h + 1 lo for head h),
+// so the rounding of the operand does not limit accuracy. The key zero-point sums
+// are one small extra product per chunk (q against the chunk's groups' key zeros).
+// The value zero-point sums are products of the zero-points (every row of a channel
+// group carrying Z_t) against hi/lo(p), accumulated into the same registers as the
+// code sums of the same 16 tokens: the two terms nearly cancel (the code term is
+// about +range/2 times the weight, the zero term about -range/2 times it), so
+// keeping them apart would leave a small result as the difference of two large
+// fp32 sums over all tokens. The window runs the same flow on bf16 operands.
 #include <algorithm>
 #include <utility>
 
@@ -226,7 +231,6 @@ struct WarpState {
   float m[NH];                 // running max of the raw logits (head 4u + tid)
   float l[NH];                 // lane-partial sum of the weights
   float o[NH][D / 16][4];      // value accumulators: rows = channels, columns = (head, part)
-  float cz[NH][4];             // value zero-point sums: rows = channel groups
 };
 
 template <int D, int GQ>
@@ -240,8 +244,6 @@ __device__ __forceinline__ void state_init(WarpState<D, GQ>& st) {
     for (int i = 0; i < D / 16; ++i)
 #pragma unroll
       for (int e = 0; e < 4; ++e) st.o[u][i][e] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) st.cz[u][e] = 0.f;
   }
 }
 
@@ -295,8 +297,6 @@ __device__ __forceinline__ void softmax_update(WarpState<D, GQ>& st,
       for (int i = 0; i < D / 16; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) st.o[u][i][e] *= corr;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) st.cz[u][e] *= corr;
       st.m[u] = mnew;
     }
     const float msl = (st.m[u] == -INFINITY) ? 0.f : st.m[u] * sl2;
@@ -440,17 +440,20 @@ __device__ void packed_warp(WarpState<D, GQ>& st, const QRegs<D, GQ>& qr, const 
 #pragma unroll
         for (int gc = 0; gc < NGC; ++gc)
           S[r][gc] = __half2float(vs[vs_index(16 * K + gid + 8 * r, gc, NGC)]);
-      // zero-point sums: rows = channel groups (A = zeros, token pairs), B = hi/lo(p)
-      const uint32_t az0 = gid < NGC ? vz[(8 * K + tid) * NGC + gid] : 0u;
-      const uint32_t az2 = gid < NGC ? vz[(8 * K + 4 + tid) * NGC + gid] : 0u;
+      // zero-point term: every row (channel) of a channel group carries the zero-points
+      // Z_t of the k (token) pair, against B = hi/lo(p). It goes into the same
+      // accumulator right next to the code term of the same tokens, so the two
+      // (which nearly cancel) never build up separately.
+      uint32_t bz0[NH], bz1[NH];
 #pragma unroll
       for (int u = 0; u < NH; ++u) {
-        const uint32_t bz0 = movm_t(split_f16(x[u][K][0]));
-        const uint32_t bz1 = movm_t(split_f16(x[u][K][1]));
-        mma_f16(st.cz[u], az0, 0u, az2, 0u, bz0, bz1);
+        bz0[u] = movm_t(split_f16(x[u][K][0]));
+        bz1[u] = movm_t(split_f16(x[u][K][1]));
       }
       static_for<NGC>([&](auto GC_) {
         constexpr int GC = decltype(GC_)::value;
+        const uint32_t z0 = vz[(8 * K + tid) * NGC + GC];
+        const uint32_t z1 = vz[(8 * K + 4 + tid) * NGC + GC];
 #pragma unroll
         for (int u = 0; u < NH; ++u) {
           const uint32_t b0 = movm_t(split_f16(x[u][K][0] * S[0][GC]));
@@ -459,6 +462,7 @@ __device__ void packed_warp(WarpState<D, GQ>& st, const QRegs<D, GQ>& qr, const 
             constexpr int MV = 2 * GC + decltype(H_)::value;
             uint32_t a[4];
             value_afrag<BITS, MV, K>(vw, a);
+            mma_f16(st.o[u][MV], z0, z0, z1, z1, bz0[u], bz1[u]);
             mma_f16(st.o[u][MV], a[0], a[1], a[2], a[3], b0, b1);
           });
         }
@@ -592,7 +596,7 @@ __device__ __forceinline__ int snake_unit(int k, int i, int P) {
 // folded in) as one deposit: m[GQ], l[GQ], o[GQ][D].
 template <int D, int GQ>
 __device__ void warp_deposit(WarpState<D, GQ>& st, float* dep, float sl2) {
-  constexpr int NGC = D / 32, NH = n_tiles<GQ>();
+  constexpr int NH = n_tiles<GQ>();
   const int lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
   float* dm = dep;
   float* dl = dep + GQ;
@@ -604,15 +608,11 @@ __device__ void warp_deposit(WarpState<D, GQ>& st, float* dep, float sl2) {
     l += __shfl_xor_sync(0xffffffffu, l, 4);
     l += __shfl_xor_sync(0xffffffffu, l, 8);
     l += __shfl_xor_sync(0xffffffffu, l, 16);
-    float z[NGC];
-    const float zl = st.cz[u][0] + st.cz[u][1];   // channel group gid, head h
-#pragma unroll
-    for (int gc = 0; gc < NGC; ++gc) z[gc] = __shfl_sync(0xffffffffu, zl, gc * 4 + tid);
     if (h < GQ) {
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
-        dout[h * D + 16 * mt + gid] = st.o[u][mt][0] + st.o[u][mt][1] + z[mt / 2];
-        dout[h * D + 16 * mt + gid + 8] = st.o[u][mt][2] + st.o[u][mt][3] + z[mt / 2];
+        dout[h * D + 16 * mt + gid] = st.o[u][mt][0] + st.o[u][mt][1];
+        dout[h * D + 16 * mt + gid + 8] = st.o[u][mt][2] + st.o[u][mt][3];
       }
       if (gid == 0) {
         dm[h] = st.m[u] == -INFINITY ? -INFINITY : st.m[u] * sl2;
