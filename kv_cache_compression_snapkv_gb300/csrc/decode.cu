@@ -429,44 +429,49 @@ __device__ void packed_warp(WarpState<D, GQ>& st, const QRegs<D, GQ>& qr, const 
         vw[4 * i] = w4.x; vw[4 * i + 1] = w4.y; vw[4 * i + 2] = w4.z; vw[4 * i + 3] = w4.w;
       }
     }
-    const __half* vs = reinterpret_cast<const __half*>(blk + off_vscale(D, BITS));
+    const uint32_t* vs = reinterpret_cast<const uint32_t*>(blk + off_vscale(D, BITS));
     const uint32_t* vz = reinterpret_cast<const uint32_t*>(blk + off_vzero(D, BITS));
     static_for<2>([&](auto KS_) {
       constexpr int K = decltype(KS_)::value;
-      // scales of this lane's tokens 16K + gid and 16K + gid + 8, all channel groups
-      float S[2][NGC];
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int gc = 0; gc < NGC; ++gc)
-          S[r][gc] = __half2float(vs[vs_index(16 * K + gid + 8 * r, gc, NGC)]);
-      // zero-point term: every row (channel) of a channel group carries the zero-points
-      // Z_t of the k (token) pair, against B = hi/lo(p). It goes into the same
-      // accumulator right next to the code term of the same tokens, so the two
-      // (which nearly cancel) never build up separately.
-      uint32_t bz0[NH], bz1[NH];
+      // scales of this lane's tokens (16K + gid, 16K + gid + 8) for every channel group
+      uint32_t S2[NGC];
+      if constexpr (NGC == 4) {
+        const uint4 v4 = *reinterpret_cast<const uint4*>(vs + (K * 8 + gid) * NGC);
+        S2[0] = v4.x; S2[1] = v4.y; S2[2] = v4.z; S2[3] = v4.w;
+      } else {
+        const uint2 v2 = *reinterpret_cast<const uint2*>(vs + (K * 8 + gid) * NGC);
+        S2[0] = v2.x; S2[1] = v2.y;
+      }
 #pragma unroll
       for (int u = 0; u < NH; ++u) {
-        bz0[u] = movm_t(split_f16(x[u][K][0]));
-        bz1[u] = movm_t(split_f16(x[u][K][1]));
-      }
-      static_for<NGC>([&](auto GC_) {
-        constexpr int GC = decltype(GC_)::value;
-        const uint32_t z0 = vz[(8 * K + tid) * NGC + GC];
-        const uint32_t z1 = vz[(8 * K + 4 + tid) * NGC + GC];
-#pragma unroll
-        for (int u = 0; u < NH; ++u) {
-          const uint32_t b0 = movm_t(split_f16(x[u][K][0] * S[0][GC]));
-          const uint32_t b1 = movm_t(split_f16(x[u][K][1] * S[1][GC]));
+        // p of the two tokens as fp16 pairs hi (ph) + lo (pl), p = ph + pl
+        const float p0 = x[u][K][0], p1 = x[u][K][1];
+        const __half2 ph = __floats2half2_rn(p0, p1);
+        const float2 phf = __half22float2(ph);
+        const __half2 pl = __floats2half2_rn(p0 - phf.x, p1 - phf.y);
+        // zero-point term operand: (hi, lo) of p per token
+        const uint32_t bz0 = movm_t(__byte_perm(h2u(ph), h2u(pl), 0x5410));
+        const uint32_t bz1 = movm_t(__byte_perm(h2u(ph), h2u(pl), 0x7632));
+        static_for<NGC>([&](auto GC_) {
+          constexpr int GC = decltype(GC_)::value;
+          const uint32_t z0 = vz[(8 * K + tid) * NGC + GC];
+          const uint32_t z1 = vz[(8 * K + 4 + tid) * NGC + GC];
+          // (hi, lo) of p * S: hi = fp16(ph S), lo = fp16(pl S + (ph S - hi)), the
+          // remainder of the fp16 product exact through the fused multiply-add
+          const __half2 s2 = u2h(S2[GC]);
+          const __half2 hi = __hmul2(ph, s2);
+          const __half2 lo = __hfma2(pl, s2, __hfma2(ph, s2, __hneg2(hi)));
+          const uint32_t b0 = movm_t(__byte_perm(h2u(hi), h2u(lo), 0x5410));
+          const uint32_t b1 = movm_t(__byte_perm(h2u(hi), h2u(lo), 0x7632));
           static_for<2>([&](auto H_) {
             constexpr int MV = 2 * GC + decltype(H_)::value;
             uint32_t a[4];
             value_afrag<BITS, MV, K>(vw, a);
-            mma_f16(st.o[u][MV], z0, z0, z1, z1, bz0[u], bz1[u]);
+            mma_f16(st.o[u][MV], z0, z0, z1, z1, bz0, bz1);
             mma_f16(st.o[u][MV], a[0], a[1], a[2], a[3], b0, b1);
           });
-        }
-      });
+        });
+      }
     });
   }
 }
@@ -655,15 +660,28 @@ __device__ void merge_deposits(float* dep, unsigned mask, float* __restrict__ o)
     for (int w = 0; w < NW; ++w) s += dep[w * DEPW + h] * (mask >> w & 1u ? dep[w * DEPW + GQ + h] : 0.f);
     L[h] = s;
   }
-  for (int e = lane; e < GQ * D; e += 32) {
-    const int h = e / D;
-    float acc = 0.f;
-    for (int w = 0; w < NW; ++w)
-      if (mask >> w & 1u) acc += dep[w * DEPW + h] * dep[w * DEPW + 2 * GQ + e];
+  // each lane owns E outputs; the deposits are walked in the outer loop so the E
+  // accumulations are independent (their shared-memory loads overlap)
+  constexpr int E = GQ * D / 32;
+  float acc[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) acc[i] = 0.f;
+  for (int w = 0; w < NW; ++w) {
+    if (!(mask >> w & 1u)) continue;
+    const float* dw = dep + w * DEPW;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const int e = lane + 32 * i;
+      acc[i] += dw[e / D] * dw[2 * GQ + e];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int e = lane + 32 * i, h = e / D;
     float Lh = 0.f;
 #pragma unroll
     for (int hh = 0; hh < GQ; ++hh) Lh = hh == h ? L[hh] : Lh;
-    o[e] = Lh > 0.f ? acc / Lh : 0.f;
+    o[e] = Lh > 0.f ? acc[i] / Lh : 0.f;
   }
 }
 

@@ -58,8 +58,12 @@ __host__ __device__ constexpr int vperm(int c, int D) {
 __host__ __device__ constexpr int vsz_index(int t, int gc, int ngc) {
   return ((t >> 1) * ngc + gc) * 2 + (t & 1);
 }
-// Index of the value scale of (token t, channel group gc): token-major.
-__host__ __device__ constexpr int vs_index(int t, int gc, int ngc) { return t * ngc + gc; }
+// Index of the value scale of (token t, channel group gc): tokens t and t + 8 of
+// a 16-token half (same gc) form one half2, and the half2 of all channel groups of
+// one (half, t % 8) are adjacent.
+__host__ __device__ constexpr int vs_index(int t, int gc, int ngc) {
+  return (((t >> 4) * 8 + (t & 7)) * ngc + gc) * 2 + ((t >> 3) & 1);
+}
 
 // Bytes of one 32-token group block.
 __host__ __device__ constexpr int block_bytes(int D, int bits) { return 8 * D * (bits + 1); }
