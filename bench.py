@@ -33,7 +33,7 @@ UNIT = "tokens/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", type=int, default=2)
@@ -84,7 +84,7 @@ class ClockSampler:
                 self.f = open(self.path, "w")
                 self.proc = subprocess.Popen(
                     ["nvidia-smi", "-i", str(index), f"--query-gpu={self.QUERY}",
-                     "--format=csv,noheader,nounits", "-lms", "200"],
+                     "--format=csv,noheader,nounits", "-lms", "50"],
                     stdout=self.f, stderr=subprocess.DEVNULL)
             except Exception:
                 self.proc = None
