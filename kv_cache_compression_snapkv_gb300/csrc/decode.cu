@@ -565,17 +565,20 @@ struct DecCfg {
   static constexpr int DEPW = GQ * (D + 2);                // floats of one deposit: m, l, o
   static constexpr int QB = GQ * D * 2;                    // bytes of one unit's queries
   static constexpr int kQRing = 4;                         // query ring entries
+  // Two deposit buffers (by unit parity): a warp leaving unit k waits, before it
+  // deposits, for the merge of unit k - 2 (it may already compute unit k + 1).
+  static constexpr int NDEP = 2;
   static constexpr int bytes(int nw) {
-    return nw * 2 * SLOT + 2 * nw * DEPW * 4 + kQRing * QB + (2 * nw + kQRing) * 8 + 64 +
+    return nw * 2 * SLOT + NDEP * nw * DEPW * 4 + 16 + kQRing * QB + (2 * nw + kQRing) * 8 + 64 +
            KVC_MAX_LAUNCH_LAYERS * (int)sizeof(DecLayer);
   }
-  static constexpr int pick(int nw) { return (nw <= 4 || bytes(nw) <= 220 * 1024) ? nw : pick(nw - 1); }
+  static constexpr int pick(int nw) { return (nw <= 4 || bytes(nw) <= 224 * 1024) ? nw : pick(nw - 1); }
   static constexpr int NW = pick(GQ > 4 ? 8 : 12);           // warps per CTA
   static constexpr int kThreadsC = NW * 32;
   // byte offsets inside dynamic shared memory
   static constexpr int oRing = 0;
   static constexpr int oDep = oRing + NW * 2 * SLOT;
-  static constexpr int oQ = oDep + 2 * NW * DEPW * 4;
+  static constexpr int oQ = (oDep + NDEP * NW * DEPW * 4 + 15) / 16 * 16;
   static constexpr int oBars = oQ + kQRing * QB;
   static constexpr int oCtl = oBars + (2 * NW + kQRing) * 8;
   static constexpr int oLay = oCtl + 64;
@@ -653,13 +656,14 @@ __device__ void merge_deposits(float* dep, unsigned mask, float* __restrict__ o)
     if (idx < NW * GQ) dep[w * DEPW + h] = f[i];   // unused warps get weight 0
   }
   __syncwarp();
+  // lane h < GQ sums head h's weighted l over the deposits; the sums are shuffled out
+  float Lh_lane = 0.f;
+  if (lane < GQ)
+    for (int w = 0; w < NW; ++w)
+      if (mask >> w & 1u) Lh_lane += dep[w * DEPW + lane] * dep[w * DEPW + GQ + lane];
   float L[GQ];
 #pragma unroll
-  for (int h = 0; h < GQ; ++h) {
-    float s = 0.f;
-    for (int w = 0; w < NW; ++w) s += dep[w * DEPW + h] * (mask >> w & 1u ? dep[w * DEPW + GQ + h] : 0.f);
-    L[h] = s;
-  }
+  for (int h = 0; h < GQ; ++h) L[h] = __shfl_sync(0xffffffffu, Lh_lane, h);
   // each lane owns E outputs; the deposits are walked in the outer loop so the E
   // accumulations are independent (their shared-memory loads overlap)
   constexpr int E = GQ * D / 32;
@@ -702,16 +706,6 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
   const int P_ = gridDim.x, cta = blockIdx.x;
   const int total_units = P.n_layers * P.units;
 
-  // layer table into shared memory (independent loads), barriers, control words
-  if (threadIdx.x < P.n_layers) lay[threadIdx.x] = P.L[threadIdx.x];
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 2 * NW + QR; ++i)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" :: "r"(smem_u32(&cbar[i])) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    for (int p = 0; p < 2; ++p) { ctl.count[p] = 0u; ctl.mask[p] = 0u; ctl.gen[p] = 0u; }
-  }
-  __syncthreads();
-
   // the CTA's units: k = 0, 1, ... while snake_unit(k) < total_units
   auto unit_of = [&](int k) { return snake_unit(k, cta, P_); };
   auto chunks_of = [&](int g) { const DecLayer& L = lay[g / P.units]; return L.wchunks + L.pchunks; };
@@ -724,8 +718,17 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
                  :: "r"(smem_u32(b)), "r"((uint32_t)C::QB) : "memory");
     bulk_g2s(qring + (k % QR) * GQ * D, q + (size_t)g * GQ * D, (uint32_t)C::QB, b);
   };
-  if (threadIdx.x == 0)
+  // barriers and control words, then the first units' queries (their addresses
+  // need no layer table); the layer table into shared memory meanwhile
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2 * NW + QR; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" :: "r"(smem_u32(&cbar[i])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    for (int p = 0; p < 2; ++p) { ctl.count[p] = 0u; ctl.mask[p] = 0u; ctl.gen[p] = 0u; }
     for (int k = 0; k < QR; ++k) q_copy(k);
+  }
+  if (threadIdx.x < P.n_layers) lay[threadIdx.x] = P.L[threadIdx.x];
+  __syncthreads();
 
   // this warp's chunk stream: positions w, w + NW, ... of the CTA's chunk list
   struct Cursor { int k, base, g, n; };   // unit k of the CTA, first list position, unit, chunks
@@ -777,16 +780,16 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
   const int units_per_layer = P.units;
 
   auto deposit = [&](int k) {   // hand over unit k's state; the last depositor merges
-    const int par = k & 1;
+    const int par = k % C::NDEP;
     const Cursor& cu = cur;   // (unused: expected count from unit k itself)
     (void)cu;
     const int g = unit_of(k);
     const unsigned expect = (unsigned)min(NW, chunks_of(g));
-    // the slot of this parity is free once unit k - 2 is merged
+    // the deposit buffer of unit k is free once unit k - NDEP is merged
     if (lane == 0) {
       bool ready = false;
       for (unsigned it = 0; it < kWaitLimit && !ready; ++it)
-        ready = *reinterpret_cast<volatile unsigned*>(&ctl.gen[par]) == (unsigned)(k >> 1);
+        ready = *reinterpret_cast<volatile unsigned*>(&ctl.gen[par]) == (unsigned)(k / C::NDEP);
       if (!ready) { atomicOr(P.err, 2u); ok = false; }
     }
     ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
