@@ -268,17 +268,19 @@ kvc_status kvc_scores_layer(kvc_cache* cache, float* scores, float* pooled, void
  *   KVC_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading this library holds
  *   until exit. All calls share it (it keeps the last call's contents; every
  *   value a call reads is written by that call first), so calls that overlap on
- *   the GPU race: serialize them. The first call on a device looks up the
- *   array's device address; make it before any stream capture.
- *   Scratch needed: B*H*(4*ceil(n/128)+4)*g*alpha*8 + B*H*g*alpha*4 +
- *   B*H*(n-alpha)*4 bytes (+ the same again for scores when `scores` is NULL),
- *   each part rounded up to 256 bytes.
+ *   the GPU race: serialize them. A second static array, zero at load, holds
+ *   the scoring launch's 1 + B*H counters (B*H <= 8192); every launch leaves
+ *   them at zero. The first call on a device looks up the device addresses;
+ *   make it before any stream capture.
+ *   Scratch needed: B*H*(4*ceil(n/128)+4)*g*alpha*8 + B*H*(n-alpha)*4 bytes
+ *   (+ the same again for scores when `scores` is NULL), each part rounded up
+ *   to 256 bytes.
  *   q_obs: device bf16 [B][Hq][alpha][d]; k: device bf16 [B][H][n][d];
  *   kept:  device int32 [B][H][min(budget, n - alpha)] (written, ascending);
  *   scores: optional device fp32 [B][H][n - alpha] (written when not NULL).
  *   Only the fields n_layers..pool_kernel of dims are read.
  *   Errors: KVC_E_ARG, KVC_E_SHAPE, KVC_E_CAPACITY (the sizes need more than
- *   the static scratch; nothing is enqueued), KVC_E_CUDA.
+ *   the static scratch, or B*H > 8192; nothing is enqueued), KVC_E_CUDA.
  * ------------------------------------------------------------------------- */
 #define KVC_NOALLOC_SCRATCH_BYTES (32u << 20)
 kvc_status kvc_select_noalloc(const kvc_dims* dims, int32_t budget, const void* q_obs,

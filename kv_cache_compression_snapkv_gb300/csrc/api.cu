@@ -133,13 +133,13 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
   if (ok && scoring) {
     const int M = g * d.obs_window;
     c->stats_elems = (size_t)units * kvc::score_stat_chunks(d.prompt_len) * M;
-    c->rowstat_elems = (size_t)units * M;
     c->score_elems = (size_t)units * ns;
     c->stats = static_cast<float2*>(dev_alloc(c, c->stats_elems * 8));
-    c->rowstat = static_cast<float2*>(dev_alloc(c, c->rowstat_elems * 8));
+    c->gsync = static_cast<unsigned*>(dev_alloc(c, (units + 1) * 4));
     c->scores = static_cast<float*>(dev_alloc(c, c->score_elems * 4));
     c->pooled = static_cast<float*>(dev_alloc(c, c->score_elems * 4));
-    ok = c->stats && c->rowstat && c->scores && c->pooled;
+    ok = c->stats && c->gsync && c->scores && c->pooled &&
+         cudaMemset(c->gsync, 0, (units + 1) * 4) == cudaSuccess;
   }
   // kept positions are stored for selective layers (keep-all layers are the identity)
   if (ok) {

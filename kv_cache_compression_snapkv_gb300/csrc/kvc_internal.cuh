@@ -190,7 +190,7 @@ struct kvc_cache {
   int32_t* kept = nullptr;    size_t kept_elems = 0;
   // scratch
   float2* stats = nullptr;    size_t stats_elems = 0;  // scoring partial row stats
-  float2* rowstat = nullptr;  size_t rowstat_elems = 0;
+  unsigned* gsync = nullptr;  // scoring counters, 1 + B*H words (zero between launches)
   float* scores = nullptr;
   float* pooled = nullptr;    size_t score_elems = 0;
   unsigned* err = nullptr;     // device error word (bounded waits that gave up)
@@ -224,15 +224,15 @@ cudaError_t launch_decode(const kvc_cache* c, int layer_begin, int layer_count,
 cudaError_t launch_export(const kvc_cache* c, int layer, const kvc_export* dst,
                           cudaStream_t stream);
 // Scoring on the tensor cores (row statistics, their merge into row normalisers,
-// per-key column sums); err may be NULL.
+// per-key column sums) in one cooperative launch. gsync: 1 + B*H words of device
+// memory that are zero before the launch and are zero again after it; err may be
+// NULL.
 cudaError_t launch_score_tc(const kvc_dims& d, const __nv_bfloat16* q_obs,
-                            const __nv_bfloat16* k, float2* stats, float* rowbias, float* scores,
+                            const __nv_bfloat16* k, float2* stats, unsigned* gsync, float* scores,
                             unsigned* err, cudaStream_t stream);
-cudaError_t launch_score_combine(const float2* stats, int nch, int M, int units, float* rowbias,
-                                 cudaStream_t stream);
 // Selection launches with explicit scratch (allocation-free entry point).
 cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
-                              const __nv_bfloat16* k, float2* stats, float* rowbias,
+                              const __nv_bfloat16* k, float2* stats, unsigned* gsync,
                               float* scores, cudaStream_t stream);
 cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float* pooled,
                                   int32_t* kept_out, int k_sel, cudaStream_t stream);
@@ -242,8 +242,9 @@ cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float*
 constexpr int kDecGroupsPerChunk = 2;
 constexpr int kDecSlotsPerChunk = 16;
 
-// Scoring: entries of the per-row statistics kept for a prompt of n keys (up to
-// four column splits per key tile of at least 128 keys).
+// Scoring: partial row statistics kept per (unit, row) for a prompt of n keys
+// (at most four epilogue groups in each CTA that owns one of the ceil(n/128) key
+// tiles).
 inline size_t score_stat_chunks(int n) { return 4 * (size_t)((n + 127) / 128) + 4; }
 
 }  // namespace kvc

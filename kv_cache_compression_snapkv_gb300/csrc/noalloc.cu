@@ -6,8 +6,8 @@
 // or latency-critical loops where a cudaMalloc (which may synchronize the device
 // and can fail under fragmentation) is not acceptable. kvc_select_noalloc gives
 // them the prefill selection without any allocation: the caller passes inputs
-// and outputs, and the intermediate buffers (per-chunk row statistics, per-row
-// normalisers, scores, pooled scores) live in one file-scope static device array
+// and outputs, and the intermediate buffers (partial row statistics, scores,
+// pooled scores) live in one file-scope static device array
 // of fixed size, KVC_NOALLOC_SCRATCH_BYTES.
 //
 // Properties of that array:
@@ -17,6 +17,9 @@
 //     to be cleared;
 //   * calls whose work overlaps on the GPU (different streams, or devices
 //     sharing a context) race on it: serialize them.
+// A second static array, zero at load, holds the scoring launch's counters (one
+// per (sequence, kv head) plus one); each launch leaves them at zero again, and it
+// bounds B*H at kMaxUnits.
 // In host code the array's name is only a host-side stand-in, not a device
 // address, so its device address is looked up once per device
 // (cudaGetSymbolAddress, with that device current) on the first call made on
@@ -31,25 +34,32 @@ constexpr size_t kScratchBytes = KVC_NOALLOC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_select_scratch[kScratchBytes];
+constexpr int kMaxUnits = 8192;
+static __device__ unsigned g_select_sync[1 + kMaxUnits] = {0u};
 
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+void* g_sync_addr[kMaxDevices] = {};
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-kvc_status scratch_for_current_device(void** out) {
+kvc_status scratch_for_current_device(void** out, unsigned** sync) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_E_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || !p) {
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || !p ||
+        cudaGetSymbolAddress(&q, g_select_sync) != cudaSuccess || !q) {
       cudaGetLastError();
       return KVC_E_CUDA;
     }
     g_scratch_addr[dev] = p;
+    g_sync_addr[dev] = q;
   }
   *out = g_scratch_addr[dev];
+  *sync = static_cast<unsigned*>(g_sync_addr[dev]);
   return KVC_OK;
 }
 
@@ -70,29 +80,29 @@ extern "C" kvc_status kvc_select_noalloc(const kvc_dims* dims, int32_t budget, c
   if (d.pool_kernel < 1 || d.pool_kernel % 2 == 0) return KVC_E_ARG;
 
   const size_t units = (size_t)d.batch * d.n_kv_heads;
+  if (units > (size_t)kMaxUnits) return KVC_E_CAPACITY;
   const size_t M = (size_t)g * d.obs_window;
   const size_t ns = (size_t)d.prompt_len - d.obs_window;
   const size_t nch = kvc::score_stat_chunks(d.prompt_len);
   const size_t stats_b = align256(units * nch * M * sizeof(float2));
-  const size_t bias_b = align256(units * M * sizeof(float));
   const size_t score_b = align256(units * ns * sizeof(float));
-  const size_t need = stats_b + bias_b + (scores ? 0 : score_b) + score_b;
+  const size_t need = stats_b + (scores ? 0 : score_b) + score_b;
   if (need > kScratchBytes) return KVC_E_CAPACITY;   // larger than the static scratch
 
   void* base = nullptr;
-  kvc_status st = scratch_for_current_device(&base);
+  unsigned* gsync = nullptr;
+  kvc_status st = scratch_for_current_device(&base, &gsync);
   if (st != KVC_OK) return st;
   unsigned char* p = static_cast<unsigned char*>(base);
   float2* stats = reinterpret_cast<float2*>(p);
-  float* rowbias = reinterpret_cast<float*>(p + stats_b);
-  float* pooled = reinterpret_cast<float*>(p + stats_b + bias_b);
-  float* sc = scores ? scores : reinterpret_cast<float*>(p + stats_b + bias_b + score_b);
+  float* pooled = reinterpret_cast<float*>(p + stats_b);
+  float* sc = scores ? scores : reinterpret_cast<float*>(p + stats_b + score_b);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int k_sel = (size_t)budget < ns ? budget : (int)ns;
   cudaError_t e = kvc::launch_score_into(d, static_cast<const __nv_bfloat16*>(q_obs),
-                                         static_cast<const __nv_bfloat16*>(k), stats, rowbias,
-                                         sc, s);
+                                         static_cast<const __nv_bfloat16*>(k), stats, gsync, sc,
+                                         s);
   if (e == cudaSuccess) e = kvc::launch_pool_topk_into(d, sc, pooled, kept, k_sel, s);
   if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? KVC_E_OOM : KVC_E_CUDA;
   return KVC_OK;

@@ -1,29 +1,35 @@
-// score_tc.cu -- observation-window scores on the 5th-generation tensor cores.
+// score_tc.cu -- observation-window scores on the 5th-generation tensor cores, one
+// cooperative persistent launch per layer.
 //
 // PyramidKV: Dynamic KV Cache Compression based on Pyramidal Information
 // Funneling, §4.2.2 "KV Cache Selection": every prompt key i < n - alpha is scored
 // by the attention the last alpha ("instruction") tokens pay it; MiniKV §2 eq. (1):
-// A = softmax(Q K^T / sqrt(d)). Per (sequence, kv head) the rows are the alpha
+// A = softmax(Q K^T / sqrt(d)). Per unit (sequence, kv head) the rows are the alpha
 // observation queries of each of the g query heads sharing the kv head (M = g *
 // alpha rows, M <= 256); a row at prompt position p sees keys 0..p (causal); each
 // row is normalised over all the keys it sees, then rows are summed per key.
 //
-// Two passes over the keys, each a persistent warp-specialised kernel:
-//   warp 0      TMA producer: key tiles into a ring of shared-memory stages, the
-//               unit's observation queries into their own buffer;
-//   warp 1      allocates tensor memory and issues the tcgen05 MMAs (one thread);
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulators (one row or key per
-//               thread) and the softmax arithmetic.
-//   Row-stats pass:  D[row][key] = Q_obs . K_tile^T (M = 128 rows per MMA tile, N =
-//               256 keys, or 128 keys when M = 256); each thread owns one row and
-//               keeps an online (max, sum of exp2) over the tile's keys, written
-//               per (row, tile); a small kernel merges them into b_r = max +
-//               log2(sum) per row.
-//   Column pass: D[key][row] = K_tile . Q_obs^T (M = 128 keys, N = M rows rounded
-//               up to 16); each thread owns one key and sums exp2(l * log2(e)/sqrt(d)
-//               - b_r) over the rows: the per-key score.
-// Both reductions stay inside a thread. Accumulators are double-buffered in tensor
-// memory so the epilogue of one tile overlaps the MMAs of the next.
+// Keys are cut into tiles of 128. Units are taken in batches whose keys fit in
+// L2; per batch, two phases over the batch's key tiles:
+//   row-stats phase  D[row][key] = Q_obs . K_tile^T (M = 128 rows per MMA, N = 128
+//                    keys); each epilogue thread owns one row and keeps an online
+//                    (max, sum of exp2) of the scaled logits over the tiles its group
+//                    handles; at the end of a unit the groups' partials are merged in
+//                    shared memory, one partial per (unit, CTA) is written and the
+//                    unit's arrival counter is raised;
+//   column phase     D[key][row] = K_tile . Q_obs^T (M = 128 keys, N = M rows
+//                    rounded up to 16); once every CTA owning row-stats tiles of the
+//                    unit has arrived (epilogue warps only wait: the producer and MMA
+//                    warps already run ahead), the row normaliser b_r = max +
+//                    log2(sum) is merged from the row's partials, and each thread owns one key and
+//                    sums exp2(l * log2(e)/sqrt(d) - b_r) over the rows: the key's
+//                    score. These key tiles were read moments before: they come
+//                    from L2.
+// Roles: warp 0 TMA producer (key tiles into a ring of shared-memory stages, the
+// unit's observation queries into their own buffers), warp 1 tensor-memory owner
+// and MMA issuer (one thread), warps 2..17 epilogue in groups, one accumulator
+// buffer per group (4 groups of 4 warps, or 2 groups of 8 when M > 128).
+// Every wait is bounded; a wait that gives up sets a bit of the error word.
 #include <algorithm>
 #include <cudaTypedefs.h>
 
@@ -33,35 +39,42 @@
 namespace kvc {
 namespace {
 
-constexpr int kEpiWarps = 16;                      // four per tensor-memory lane quarter
-constexpr int kSplit = kEpiWarps / 4;              // column splits of a tile
+constexpr int kEpiWarps = 16;
 constexpr int kTcThreads = 64 + 32 * kEpiWarps;    // producer, MMA, epilogue warps
 constexpr int kTmemCols = 512;
+constexpr int kSmemLimit = 232448;                 // opt-in shared memory per CTA
+constexpr long long kBatchKeyBytes = 80ll << 20;   // keys of one batch: well inside L2
 
-template <int D, int PASS, int QT>
+enum : unsigned { kErrProducer = 8u, kErrMma = 16u, kErrEpilogue = 32u, kErrUnit = 64u };
+
+template <int D, int QT>
 struct TcCfg {
-  static constexpr int KB = D / 64;                     // 64-element K blocks
-  static constexpr int QROWS = QT * 128;                 // staged query rows
-  static constexpr int KROWS = PASS == 0 ? (QT == 1 ? 256 : 128) : 128;   // keys per tile
+  static constexpr int KB = D / 64;                // 64-element K blocks
+  static constexpr int QROWS = QT * 128;           // staged query rows
+  static constexpr int KROWS = 128;                // keys per tile
   static constexpr int QBYTES = QROWS * D * 2;
   static constexpr int KBYTES = KROWS * D * 2;
-  // as many key stages as shared memory holds: the bytes in flight per SM set the
-  // DRAM throughput a pass reaches
-  static constexpr int STAGES = PASS == 0 ? (QT == 1 ? 3 : 5) : (QT == 1 ? 5 : 4);
-  // tensor-memory accumulator buffers: two of 256 columns for the row-stats pass,
-  // four of 128 columns for the column pass (two of 256 when M > 128)
-  static constexpr int NBUF = (PASS == 1 && QT == 1) ? 4 : 2;
-  static constexpr int BUFCOLS = 512 / NBUF;
+  static constexpr int NG = 4 / QT;                // epilogue groups = accumulator buffers
+  static constexpr int BUFCOLS = kTmemCols / NG;   // 128 * QT columns each
+  static constexpr int GW = kEpiWarps / NG;        // warps per group
+  static constexpr int GT = 32 * GW;               // threads per group (= rows it can own)
+  static constexpr int QBUF = QT == 1 ? 2 : 1;     // query buffers
+  static constexpr int TAIL = NG * GT * 4 + NG * 2 * 128 * 4 + NG * GT * 8 + 64 * 8 + 16 + 1024;
+  static constexpr int FIT = (kSmemLimit - QBUF * QBYTES - TAIL) / KBYTES;
+  static constexpr int STAGES = FIT > 8 ? 8 : FIT;   // key stages: bytes in flight per SM
   static constexpr int oQ = 0;
-  static constexpr int oK = QBYTES;
+  static constexpr int oK = QBUF * QBYTES;
   static constexpr int oBar = oK + STAGES * KBYTES;
-  // full[S], empty[S], qfull, qempty, tfull[NBUF], tempty[NBUF], drain
-  static constexpr int NBAR = 2 * STAGES + 3 + 2 * NBUF;
+  // full[S], empty[S], qfull[QBUF], qempty[QBUF], tfull[NG], tempty[NG], drain
+  static constexpr int NBAR = 2 * STAGES + 2 * QBUF + 2 * NG + 1;
   static constexpr int oTmem = oBar + NBAR * 8;
-  static constexpr int oBias = (oTmem + 16 + 15) / 16 * 16;
-  static constexpr int BIASB = PASS == 1 ? 4 * 256 * 4 : 0;   // column pass: 4 bias copies
-  static constexpr int total = oBias + BIASB + 1024;            // + alignment slack
-  static_assert(total <= 232448, "fits the shared memory of one CTA");
+  static constexpr int oBias = (oTmem + 16 + 15) / 16 * 16;   // [NG][GT] negated b_r
+  static constexpr int oPart = oBias + NG * GT * 4;           // [NG][2][128] column halves
+  static constexpr int oRow = oPart + NG * 2 * 128 * 4;       // [NG][GT] group row partials
+  static constexpr int total = oRow + NG * GT * 8 + 1024;     // + alignment slack
+  static_assert(STAGES >= 2, "at least two key stages");
+  static_assert(NBAR <= 64, "barrier area");
+  static_assert(total <= kSmemLimit, "fits the shared memory of one CTA");
   static_assert(QBYTES % 1024 == 0 && KBYTES % 1024 == 0, "1024-byte aligned tiles");
 };
 
@@ -70,20 +83,69 @@ struct TcArgs {
   int ns;         // scored keys (n - alpha)
   int alpha;
   int M;          // rows per unit (g * alpha)
+  int MP;         // M rounded up to 16 (N of the column-phase MMA)
   int units;
-  int tiles;      // tiles per unit
+  int ubatch;     // units per batch
+  int tiles0;     // key tiles per unit, row-stats phase (all n keys)
+  int tiles1;     // key tiles per unit, column phase (the ns scored keys)
+  int smax;       // partial slots per (unit, row)
   float sl2;      // log2(e) / sqrt(d)
-  float2* stats;  // row-stats pass: [unit][row][tile]
-  const float* rowbias;   // column pass: [unit][row]
-  float* scores;          // column pass: [unit][ns]
+  float2* stats;  // [unit][slot][row] partial (max, sum), one slot per CTA
+  float* scores;  // [unit][ns]
+  unsigned* gsync;  // [0] CTAs done, [1 + unit] arrivals; all zero between launches
   unsigned* err;
 };
 
-template <int D, int PASS, int QT>
+// Items [b, e) of `total` that CTA c of G owns, and the owner of item i.
+struct Slice { long long b, e; };
+__device__ __forceinline__ Slice slice_of(long long total, int c, int G) {
+  return {total * c / G, total * (c + 1) / G};
+}
+__device__ __forceinline__ int owner_of(long long i, long long total, int G) {
+  return (int)(((i + 1) * G + total - 1) / total) - 1;
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait until `*cnt` reaches `target` (acquire). One thread per group.
+__device__ bool wait_count(const unsigned* cnt, unsigned target, unsigned* err) {
+  if (ld_acquire(cnt) >= target) return true;
+  const unsigned long long t0 = tc::gtimer();
+  while (ld_acquire(cnt) < target) {
+    if (tc::gtimer() - t0 > tc::kWaitNs) {
+      if (err) atomicOr(err, kErrUnit);
+      return false;
+    }
+  }
+  return true;
+}
+// Count one arrival; the writes this CTA made before (ordered by a barrier with
+// this thread) are visible to a thread whose acquire load sees the count.
+__device__ __forceinline__ void arrive_release(unsigned* cnt) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(cnt) : "memory");
+}
+
+// (max, sum) merge of two partials of exp2 sums: M = max, S = s_a 2^(m_a - M) + ...
+__device__ __forceinline__ float2 merge_ms(float2 p, float2 q) {
+  if (q.y <= 0.f) return p;
+  if (p.y <= 0.f) return q;
+  const float m = fmaxf(p.x, q.x);
+  return make_float2(m, fmaf(p.y, exp2f(p.x - m), q.y * exp2f(q.x - m)));
+}
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
+
+template <int D, int QT>
 __global__ void __launch_bounds__(kTcThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                 const TcArgs a) {
-  using C = TcCfg<D, PASS, QT>;
+  using C = TcCfg<D, QT>;
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
                                             ~uintptr_t(1023));
@@ -93,25 +155,24 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* qfull = bars + 2 * C::STAGES;
-  uint64_t* qempty = qfull + 1;
-  uint64_t* tfull = qfull + 2;
-  uint64_t* tempty = tfull + C::NBUF;
-  uint64_t* drain = tempty + C::NBUF;
+  uint64_t* qempty = qfull + C::QBUF;
+  uint64_t* tfull = qempty + C::QBUF;
+  uint64_t* tempty = tfull + C::NG;
+  uint64_t* drain = tempty + C::NG;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(dsm + C::oTmem);
   float* sbias = reinterpret_cast<float*>(dsm + C::oBias);
+  float* spart = reinterpret_cast<float*>(dsm + C::oPart);
+  float2* srow = reinterpret_cast<float2*>(dsm + C::oRow);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const long long total = (long long)a.units * a.tiles;
-  const int it0 = (int)(blockIdx.x * total / gridDim.x);
-  const int it1 = (int)((blockIdx.x + 1) * total / gridDim.x);
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int nbatch = (a.units + a.ubatch - 1) / a.ubatch;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) { tc::mbar_init(&full[s], 1); tc::mbar_init(&empty[s], 1); }
-    tc::mbar_init(qfull, 1);
-    tc::mbar_init(qempty, 1);
-    for (int b = 0; b < C::NBUF; ++b) {
+    for (int q = 0; q < C::QBUF; ++q) { tc::mbar_init(&qfull[q], 1); tc::mbar_init(&qempty[q], 1); }
+    for (int b = 0; b < C::NG; ++b) {
       tc::mbar_init(&tfull[b], 1);
-      tc::mbar_init(&tempty[b], PASS == 0 ? kEpiWarps : 4);
+      tc::mbar_init(&tempty[b], C::GW);
     }
     tc::mbar_init(drain, 1);
     tc::fence_mbar_init();
@@ -131,219 +192,304 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
-      int cur = -1, nq = 0, issued = 0;
-      for (int it = it0, k = 0; it < it1 && ok; ++it, ++k) {
-        const int unit = it / a.tiles, tile = it % a.tiles;
-        if (unit != cur) {
-          if (nq > 0) ok = tc::mbar_wait(qempty, (uint32_t)((nq - 1) & 1), a.err, 8u);
-          if (!ok) break;
-          tc::mbar_expect_tx(qfull, (uint32_t)C::QBYTES);
-          for (int kb = 0; kb < C::KB; ++kb)
-            for (int qt = 0; qt < QT; ++qt)
-              tc::tma_load_2d(sQ + kb * C::QROWS * 128 + qt * 128 * 128, &tmQ, kb * 64,
-                              unit * a.M + qt * 128, qfull);
-          ++nq;
-          cur = unit;
+      int k = 0, nq = 0, qkey = -1;
+      for (int j = 0; j < nbatch && ok; ++j) {
+        const int u0 = j * a.ubatch, nu = min(a.ubatch, a.units - u0);
+        for (int ph = 0; ph < 2 && ok; ++ph) {
+          const int tiles = ph ? a.tiles1 : a.tiles0;
+          const Slice sl = slice_of((long long)nu * tiles, cta, G);
+          for (long long i = sl.b; i < sl.e && ok; ++i, ++k) {
+            const int unit = u0 + (int)(i / tiles), tile = (int)(i % tiles);
+            if (unit * 2 + ph != qkey) {
+              const int qb = nq % C::QBUF;
+              if (nq >= C::QBUF)
+                ok = tc::mbar_wait(&qempty[qb], (uint32_t)((nq / C::QBUF - 1) & 1), a.err,
+                                   kErrProducer);
+              if (!ok) break;
+              tc::mbar_expect_tx(&qfull[qb], (uint32_t)C::QBYTES);
+              uint8_t* q = sQ + qb * C::QBYTES;
+              for (int kb = 0; kb < C::KB; ++kb)
+                for (int qt = 0; qt < QT; ++qt)
+                  tc::tma_load_2d(q + kb * C::QROWS * 128 + qt * 128 * 128, &tmQ, kb * 64,
+                                  unit * a.M + qt * 128, &qfull[qb]);
+              ++nq;
+              qkey = unit * 2 + ph;
+            }
+            const int s = k % C::STAGES, round = k / C::STAGES;
+            if (round > 0)
+              ok = tc::mbar_wait(&empty[s], (uint32_t)((round - 1) & 1), a.err, kErrProducer);
+            if (!ok) break;
+            tc::mbar_expect_tx(&full[s], (uint32_t)C::KBYTES);
+            uint8_t* dst = sK + s * C::KBYTES;
+            for (int kb = 0; kb < C::KB; ++kb)
+              tc::tma_load_2d(dst + kb * C::KROWS * 128, &tmK, kb * 64,
+                              unit * a.n + tile * C::KROWS, &full[s]);
+          }
         }
-        const int s = k % C::STAGES, round = k / C::STAGES;
-        if (round > 0) ok = tc::mbar_wait(&empty[s], (uint32_t)((round - 1) & 1), a.err, 8u);
-        if (!ok) break;
-        tc::mbar_expect_tx(&full[s], (uint32_t)C::KBYTES);
-        uint8_t* dst = sK + s * C::KBYTES;
-        for (int kb = 0; kb < C::KB; ++kb)
-          for (int r = 0; r < C::KROWS / 128; ++r)
-            tc::tma_load_2d(dst + kb * C::KROWS * 128 + r * 128 * 128, &tmK, kb * 64,
-                            unit * a.n + tile * C::KROWS + r * 128, &full[s]);
-        issued = k + 1;
       }
-      // every copy this thread issued has landed before the CTA can leave (in the
-      // normal case the MMA thread already waited for all of them)
-      for (int k = std::max(0, issued - C::STAGES); k < issued; ++k)
-        tc::mbar_wait(&full[k % C::STAGES], (uint32_t)((k / C::STAGES) & 1), a.err, 8u);
-      if (nq > 0) tc::mbar_wait(qfull, (uint32_t)((nq - 1) & 1), a.err, 8u);
+      // every copy issued here has landed before the CTA can leave (normally the
+      // MMA thread already waited for all of them)
+      for (int kk = max(0, k - C::STAGES); kk < k; ++kk)
+        tc::mbar_wait(&full[kk % C::STAGES], (uint32_t)((kk / C::STAGES) & 1), a.err,
+                      kErrProducer);
+      for (int q = max(0, nq - C::QBUF); q < nq; ++q)
+        tc::mbar_wait(&qfull[q % C::QBUF], (uint32_t)((q / C::QBUF) & 1), a.err, kErrProducer);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
-      constexpr uint32_t idesc = PASS == 0 ? tc::idesc_bf16_f32(128, C::KROWS) : 0u;
-      const int MP = (a.M + 15) / 16 * 16;
-      const uint32_t idesc1 = tc::idesc_bf16_f32(128, MP);
-      int cur = -1, nq = 0;
-      for (int it = it0, k = 0; it < it1 && ok; ++it, ++k) {
-        const int unit = it / a.tiles;
-        const int s = k % C::STAGES, round = k / C::STAGES;
-        ok = tc::mbar_wait(&full[s], (uint32_t)(round & 1), a.err, 16u);
-        if (!ok) break;
-        if (unit != cur) {
-          ok = tc::mbar_wait(qfull, (uint32_t)(nq & 1), a.err, 16u);
-          if (!ok) break;
-          ++nq;
-          cur = unit;
-        }
-        const int b = k % C::NBUF, rb = k / C::NBUF;
-        if (rb > 0) ok = tc::mbar_wait(&tempty[b], (uint32_t)((rb - 1) & 1), a.err, 16u);
-        if (!ok) break;
-        tc::fence_after_sync();
-        const uint32_t sQa = tc::saddr(sQ), sKa = tc::saddr(sK + s * C::KBYTES);
-        const uint32_t dcol = tbase + (uint32_t)(b * C::BUFCOLS);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int kb = kk / 4, kin = (kk % 4) * 32;
-          if (PASS == 0) {
-#pragma unroll
-            for (int mt = 0; mt < QT; ++mt) {
-              const uint64_t ad = tc::sw128_desc(sQa + kb * C::QROWS * 128 + mt * 128 * 128 + kin);
-              const uint64_t bd = tc::sw128_desc(sKa + kb * C::KROWS * 128 + kin);
-              tc::mma_bf16(dcol + mt * C::KROWS, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      constexpr uint32_t idesc0 = tc::idesc_bf16_f32(128, 128);
+      const uint32_t idesc1 = tc::idesc_bf16_f32(128, a.MP);
+      int k = 0, nq = 0, qkey = -1, qb = 0;
+      for (int j = 0; j < nbatch && ok; ++j) {
+        const int u0 = j * a.ubatch, nu = min(a.ubatch, a.units - u0);
+        for (int ph = 0; ph < 2 && ok; ++ph) {
+          const int tiles = ph ? a.tiles1 : a.tiles0;
+          const Slice sl = slice_of((long long)nu * tiles, cta, G);
+          for (long long i = sl.b; i < sl.e && ok; ++i, ++k) {
+            const int unit = u0 + (int)(i / tiles);
+            const int s = k % C::STAGES, round = k / C::STAGES;
+            ok = tc::mbar_wait(&full[s], (uint32_t)(round & 1), a.err, kErrMma);
+            if (!ok) break;
+            if (unit * 2 + ph != qkey) {
+              qb = nq % C::QBUF;
+              ok = tc::mbar_wait(&qfull[qb], (uint32_t)((nq / C::QBUF) & 1), a.err, kErrMma);
+              if (!ok) break;
+              ++nq;
+              qkey = unit * 2 + ph;
             }
-          } else {
-            const uint64_t ad = tc::sw128_desc(sKa + kb * C::KROWS * 128 + kin);
-            const uint64_t bd = tc::sw128_desc(sQa + kb * C::QROWS * 128 + kin);
-            tc::mma_bf16(dcol, ad, bd, idesc1, kk > 0 ? 1u : 0u);
+            const int b = k % C::NG, rb = k / C::NG;
+            if (rb > 0) ok = tc::mbar_wait(&tempty[b], (uint32_t)((rb - 1) & 1), a.err, kErrMma);
+            if (!ok) break;
+            tc::fence_after_sync();
+            const uint32_t sQa = tc::saddr(sQ + qb * C::QBYTES);
+            const uint32_t sKa = tc::saddr(sK + s * C::KBYTES);
+            const uint32_t dcol = tbase + (uint32_t)(b * C::BUFCOLS);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const int kb = kk / 4, kin = (kk % 4) * 32;
+              if (ph == 0) {
+#pragma unroll
+                for (int mt = 0; mt < QT; ++mt) {
+                  const uint64_t ad =
+                      tc::sw128_desc(sQa + kb * C::QROWS * 128 + mt * 128 * 128 + kin);
+                  const uint64_t bd = tc::sw128_desc(sKa + kb * C::KROWS * 128 + kin);
+                  tc::mma_bf16(dcol + mt * 128, ad, bd, idesc0, kk > 0 ? 1u : 0u);
+                }
+              } else {
+                const uint64_t ad = tc::sw128_desc(sKa + kb * C::KROWS * 128 + kin);
+                const uint64_t bd = tc::sw128_desc(sQa + kb * C::QROWS * 128 + kin);
+                tc::mma_bf16(dcol, ad, bd, idesc1, kk > 0 ? 1u : 0u);
+              }
+            }
+            tc::mma_commit(&empty[s]);
+            tc::mma_commit(&tfull[b]);
+            if (i + 1 == sl.e || (i + 1) / tiles != i / tiles) tc::mma_commit(&qempty[qb]);
           }
         }
-        tc::mma_commit(&empty[s]);
-        tc::mma_commit(&tfull[b]);
-        const bool last_of_unit = (it + 1 >= it1) || ((it + 1) / a.tiles != unit);
-        if (last_of_unit) tc::mma_commit(qempty);
       }
       // every MMA issued here has completed before tensor memory is released
       tc::mma_commit(drain);
-      tc::mbar_wait(drain, 0u, a.err, 16u);
+      tc::mbar_wait(drain, 0u, a.err, kErrMma);
     }
   } else {
     // ------------------------------------------------------------- epilogue
     const int e = warp - 2;
+    const int g = e / C::GW, we = e % C::GW;     // group, warp within the group
     const int sub = warp & 3;                    // tensor-memory lane quarter
-    const int row_in = sub * 32 + lane;          // row (pass 0) or key (pass 1) in the tile
+    const int h = we >> 2;                       // row half (two halves when M > 128)
+    const int gt = we * 32 + lane;               // thread within the group
     const uint32_t lane_addr = (uint32_t)(sub * 32) << 16;
-    if (PASS == 0) {
-      // every tile: warp e reads lane quarter e % 4 and column split e / 4
-      const int split = e >> 2;
-      for (int it = it0, k = 0; it < it1; ++it, ++k) {
-        const int unit = it / a.tiles, tile = it % a.tiles;
-        const int b = k % C::NBUF, rb = k / C::NBUF;
-        if (ok) ok = tc::mbar_wait(&tfull[b], (uint32_t)(rb & 1), a.err, 32u);
-        ok = __all_sync(0xffffffffu, ok);
-        tc::fence_after_sync();
-        const uint32_t tcol = tbase + lane_addr + (uint32_t)(b * C::BUFCOLS);
-        constexpr int HC = C::KROWS / kSplit;     // columns of this split
-        static_assert(HC % 32 == 0, "whole 32-column loads");
-        const int key0 = tile * C::KROWS + split * HC;
-        // only the tiles reaching the observation window need the causal / range mask
-        const bool masked = key0 + HC > a.n - a.alpha;
+    float* gbias = sbias + g * C::GT;
+    __shared__ int s_bad[4];                     // a group's wait gave up
+    if (gt == 0) s_bad[g] = 0;
+    int k = 0;
+    for (int j = 0; j < nbatch; ++j) {
+      const int u0 = j * a.ubatch, nu = min(a.ubatch, a.units - u0);
+      const long long tot0 = (long long)nu * a.tiles0;
+      // ---------------------------------------------------- row-stats phase
+      {
+        const Slice sl = slice_of(tot0, cta, G);
+        const int r = h * 128 + sub * 32 + lane;              // the row this thread owns
+        const int pos = a.n - a.alpha + (r % a.alpha);       // its prompt position
+        long long i = sl.b;
+        while (i < sl.e) {
+          const int ul = (int)(i / a.tiles0);
+          const long long iend = min(sl.e, (long long)(ul + 1) * a.tiles0);
+          float m = -INFINITY, z = 0.f;
+          for (; i < iend; ++i, ++k) {
+            if (k % C::NG != g) continue;
+            const int tile = (int)(i % a.tiles0);
+            if (ok) ok = tc::mbar_wait(&tfull[g], (uint32_t)((k / C::NG) & 1), a.err, kErrEpilogue);
+            ok = __all_sync(0xffffffffu, ok);
+            tc::fence_after_sync();
+            const uint32_t tcol = tbase + lane_addr + (uint32_t)(g * C::BUFCOLS + h * 128);
+            const int key0 = tile * C::KROWS;
+            // only tiles reaching the observation window need the causal / range mask
+            const bool masked = key0 + C::KROWS > a.n - a.alpha;
+            const int lim = min(a.n - 1, pos) - key0;        // last visible column
+#pragma unroll 1
+            for (int c0 = 0; c0 < C::KROWS; c0 += 32) {
+              float v[32];
+              tc::tmem_ld32(tcol + (uint32_t)c0, v);
+              if (masked) {
 #pragma unroll
-        for (int mt = 0; mt < QT; ++mt) {
-          const int r = mt * 128 + row_in;
-          const int pos = a.n - a.alpha + (r % a.alpha);
-          const int lim = min(a.n - 1, pos) - key0;   // last visible column of this split
-          float m = -INFINITY, ssum = 0.f;
-#pragma unroll
-          for (int c0 = 0; c0 < HC; c0 += 32) {
-            float v[32];
-            tc::tmem_ld32(tcol + (uint32_t)(mt * C::KROWS + split * HC + c0), v);
-            if (masked) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = (c0 + j <= lim) ? v[j] : -INFINITY;
-            }
-            float mx[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) mx[j] = fmaxf(fmaxf(v[j], v[j + 8]), fmaxf(v[j + 16], v[j + 24]));
-            const float cm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            if (cm != -INFINITY) {
-              const float cms = cm * a.sl2;
-              if (cms > m) {
-                ssum = (m == -INFINITY) ? 0.f : ssum * exp2f(m - cms);
-                m = cms;
+                for (int jj = 0; jj < 32; ++jj) v[jj] = (c0 + jj <= lim) ? v[jj] : -INFINITY;
               }
+              float mx[8];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                float x = fmaf(v[j], a.sl2, -m);
-                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(v[j]) : "f"(x));
+              for (int jj = 0; jj < 8; ++jj)
+                mx[jj] = fmaxf(fmaxf(v[jj], v[jj + 8]), fmaxf(v[jj + 16], v[jj + 24]));
+              const float cm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+              if (cm != -INFINITY) {
+                const float cms = cm * a.sl2;
+                if (cms > m) {
+                  z = (m == -INFINITY) ? 0.f : z * exp2f(m - cms);
+                  m = cms;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                  const float x = fmaf(v[jj], a.sl2, -m);
+                  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(v[jj]) : "f"(x));
+                }
+#pragma unroll
+                for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+                  for (int jj = 0; jj < w; ++jj) v[jj] += v[jj + w];
+                z += v[0];
               }
-#pragma unroll
-              for (int w = 16; w > 0; w >>= 1)
-#pragma unroll
-                for (int j = 0; j < w; ++j) v[j] += v[j + w];
-              ssum += v[0];
             }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&tempty[g]);
           }
-          if (ok && r < a.M)
-            a.stats[((size_t)unit * a.M + r) * (kSplit * a.tiles) + kSplit * tile + split] =
-                make_float2(m, ssum);
+          // the groups' partials of the unit (a group without a tile of it holds the
+          // empty partial) merge into this CTA's partial, then the unit's counter
+          // counts the CTA in
+          srow[g * C::GT + r] = make_float2(m, z);
+          named_bar(5, 32 * kEpiWarps);
+          const int te = e * 32 + lane;
+          if (te < a.M) {
+            float2 p = srow[te];
+#pragma unroll
+            for (int gg = 1; gg < C::NG; ++gg) p = merge_ms(p, srow[gg * C::GT + te]);
+            const int cf = owner_of((long long)ul * a.tiles0, tot0, G);
+            a.stats[((size_t)(u0 + ul) * a.smax + (cta - cf)) * a.M + te] = p;
+          }
+          named_bar(5, 32 * kEpiWarps);
+          if (te == 0) arrive_release(a.gsync + 1 + u0 + ul);
         }
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&tempty[b]);
       }
-    } else {
-      // group gi = e / 4 (four warps, one per lane quarter) takes the tiles k with
-      // k % NBUF == gi, all MP columns: no data crosses warps
-      const int gi = e >> 2;
-      const int MP = (a.M + 15) / 16 * 16;
-      float* gbias = sbias + gi * 256;           // this group's negated row normalisers
-      int cur = -1;
-      if (gi < C::NBUF) {
-        for (int it = it0 + gi, k = gi; it < it1; it += C::NBUF, k += C::NBUF) {
-          const int unit = it / a.tiles, tile = it % a.tiles;
-          if (unit != cur) {
-            asm volatile("bar.sync %0, 128;" :: "r"(1 + gi) : "memory");
-            for (int j = sub * 32 + lane; j < 256; j += 128)
-              gbias[j] = j < a.M ? -a.rowbias[(size_t)unit * a.M + j] : -INFINITY;
-            asm volatile("bar.sync %0, 128;" :: "r"(1 + gi) : "memory");
-            cur = unit;
+      // ------------------------------------------------------- column phase
+      {
+        const Slice sl = slice_of((long long)nu * a.tiles1, cta, G);
+        const int key_in = sub * 32 + lane;                   // the key this thread owns
+        const int cbeg = h * 128, cend = min(a.MP, cbeg + 128);
+        int cur = -1;
+        for (long long i = sl.b; i < sl.e; ++i, ++k) {
+          if (k % C::NG != g) continue;
+          const int ul = (int)(i / a.tiles1), tile = (int)(i % a.tiles1);
+          if (ul != cur) {
+            // b_r of the unit's rows, merged from the partials of every CTA owning
+            // row-stats tiles of the unit, once all of them have arrived
+            const int cf = owner_of((long long)ul * a.tiles0, tot0, G);
+            const int cl = owner_of((long long)(ul + 1) * a.tiles0 - 1, tot0, G);
+            const int nct = cl - cf + 1;
+            named_bar(1 + g, C::GT);
+            if (gt == 0 && ok && !wait_count(a.gsync + 1 + u0 + ul, (unsigned)nct, a.err))
+              s_bad[g] = 1;
+            named_bar(1 + g, C::GT);
+            ok = ok && s_bad[g] == 0;
+            float nb = -INFINITY;
+            if (gt < a.M) {
+              const float2* st = a.stats + (size_t)(u0 + ul) * a.smax * a.M + gt;
+              // all loads of a round in flight at once: one L2 round trip per 24 CTAs
+              float2 p = make_float2(-INFINITY, 0.f);
+              for (int s0 = 0; s0 < nct; s0 += 24) {
+                float2 v[24];
+#pragma unroll
+                for (int q = 0; q < 24; ++q)
+                  v[q] = s0 + q < nct ? __ldcg(st + (size_t)(s0 + q) * a.M)
+                                      : make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int q = 0; q < 24; ++q) p = merge_ms(p, v[q]);
+              }
+              nb = -(p.x + log2f(p.y));
+            }
+            gbias[gt] = nb;
+            named_bar(1 + g, C::GT);
+            cur = ul;
           }
-          const int b = gi, rb = k / C::NBUF;
-          if (ok) ok = tc::mbar_wait(&tfull[b], (uint32_t)(rb & 1), a.err, 32u);
+          if (ok) ok = tc::mbar_wait(&tfull[g], (uint32_t)((k / C::NG) & 1), a.err, kErrEpilogue);
           ok = __all_sync(0xffffffffu, ok);
           tc::fence_after_sync();
-          const uint32_t tcol = tbase + lane_addr + (uint32_t)(b * C::BUFCOLS);
+          const uint32_t tcol = tbase + lane_addr + (uint32_t)(g * C::BUFCOLS);
           float acc = 0.f;
 #pragma unroll 1
-          for (int c0 = 0; c0 < MP; c0 += 32) {
+          for (int c0 = cbeg; c0 < cend; c0 += 32) {
             float v[32];
             tc::tmem_ld32(tcol + (uint32_t)c0, v);
             const float4* nb4 = reinterpret_cast<const float4*>(gbias + c0);
-            if (c0 + 32 <= a.M) {
+            if (c0 + 32 <= cend) {
 #pragma unroll
-              for (int j = 0; j < 32; j += 4) {
-                const float4 nb = nb4[j / 4];
-                v[j] = fmaf(v[j], a.sl2, nb.x);
-                v[j + 1] = fmaf(v[j + 1], a.sl2, nb.y);
-                v[j + 2] = fmaf(v[j + 2], a.sl2, nb.z);
-                v[j + 3] = fmaf(v[j + 3], a.sl2, nb.w);
+              for (int jj = 0; jj < 32; jj += 4) {
+                const float4 nb = nb4[jj / 4];
+                v[jj] = fmaf(v[jj], a.sl2, nb.x);
+                v[jj + 1] = fmaf(v[jj + 1], a.sl2, nb.y);
+                v[jj + 2] = fmaf(v[jj + 2], a.sl2, nb.z);
+                v[jj + 3] = fmaf(v[jj + 3], a.sl2, nb.w);
               }
             } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                v[j] = (c0 + j < a.M) ? fmaf(v[j], a.sl2, gbias[c0 + j]) : -INFINITY;
+              for (int jj = 0; jj < 32; ++jj)
+                v[jj] = (c0 + jj < cend) ? fmaf(v[jj], a.sl2, gbias[c0 + jj]) : -INFINITY;
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(v[j]) : "f"(v[j]));
+            for (int jj = 0; jj < 32; ++jj)
+              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(v[jj]) : "f"(v[jj]));
 #pragma unroll
             for (int w = 16; w > 0; w >>= 1)
 #pragma unroll
-              for (int j = 0; j < w; ++j) v[j] += v[j + w];
+              for (int jj = 0; jj < w; ++jj) v[jj] += v[jj + w];
             acc += v[0];
           }
-          const int key = tile * C::KROWS + row_in;
-          if (ok && key < a.ns) a.scores[(size_t)unit * a.ns + key] = acc;
           tc::fence_before_sync();
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&tempty[b]);
+          if (lane == 0) tc::mbar_arrive(&tempty[g]);
+          const int key = tile * C::KROWS + key_in;
+          if (QT == 1) {
+            if (ok && key < a.ns) a.scores[(size_t)(u0 + ul) * a.ns + key] = acc;
+          } else {
+            // the two row halves of the group meet in shared memory (two buffers by
+            // tile parity: a half is at most one tile ahead of the other)
+            float* part = spart + (g * 2 + ((k / C::NG) & 1)) * 128;
+            if (h == 1) part[key_in] = acc;
+            named_bar(1 + g, C::GT);
+            if (h == 0 && ok && key < a.ns)
+              a.scores[(size_t)(u0 + ul) * a.ns + key] = acc + part[key_in];
+          }
         }
       }
     }
   }
 
   // teardown: every MMA this CTA issued has completed once the epilogue consumed
-  // its last tile; on an error path, drain before releasing tensor memory
+  // its last tile; on an error path the MMA thread drained before this point
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tbase, kTmemCols);
+  }
+  // the last CTA to finish returns the counters to zero for the next launch
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.gsync, 1u) == (unsigned)G - 1) {
+      for (int u = 0; u < a.units; ++u) a.gsync[1 + u] = 0u;
+      a.gsync[0] = 0u;
+      __threadfence();
+    }
   }
 }
 
@@ -375,36 +521,52 @@ cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, int d) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int PASS, int QT>
-cudaError_t launch_pass(const CUtensorMap& mk, const CUtensorMap& mq, const TcArgs& a,
-                        cudaStream_t stream) {
-  using C = TcCfg<D, PASS, QT>;
-  static int n_sm[64] = {};
+template <int D, int QT>
+cudaError_t launch_fused(const CUtensorMap& mk, const CUtensorMap& mq, const TcArgs& a,
+                         cudaStream_t stream) {
+  using C = TcCfg<D, QT>;
+  static int max_ctas[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorInvalidDevice;
-  if (!n_sm[dev]) {
-    e = cudaFuncSetAttribute(score_tc_kernel<D, PASS, QT>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::total);
+  if (!max_ctas[dev]) {
+    e = cudaFuncSetAttribute(score_tc_kernel<D, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::total);
     if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    int n_sm = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    n_sm[dev] = n;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_tc_kernel<D, QT>, kTcThreads,
+                                                      C::total);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    max_ctas[dev] = n_sm * per_sm;
   }
-  const long long items = (long long)a.units * a.tiles;
-  const int grid = (int)std::min<long long>(n_sm[dev], items);
+  // every CTA owns row-stats tiles of the first (largest) batch
+  const long long items0 = (long long)std::min(a.ubatch, a.units) * a.tiles0;
+  const int grid = (int)std::min<long long>(max_ctas[dev], items0);
   if (grid < 1) return cudaSuccess;
-  score_tc_kernel<D, PASS, QT><<<grid, kTcThreads, C::total, stream>>>(mk, mq, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = C::total;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: waits across CTAs are safe
+  at[0].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, score_tc_kernel<D, QT>, mk, mq, a);
+  if (e != cudaSuccess) return e;
   count_launches(1);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 template <int D>
-cudaError_t run_passes(const kvc_dims& d, const __nv_bfloat16* q_obs, const __nv_bfloat16* k,
-                       float2* stats, float* rowbias, float* scores, unsigned* err,
-                       cudaStream_t stream) {
+cudaError_t run_fused(const kvc_dims& d, const __nv_bfloat16* q_obs, const __nv_bfloat16* k,
+                      float2* stats, unsigned* gsync, float* scores, unsigned* err,
+                      cudaStream_t stream) {
   const int units = d.batch * d.n_kv_heads;
   const int n = d.prompt_len, alpha = d.obs_window;
   const int M = (d.n_q_heads / d.n_kv_heads) * alpha;
@@ -417,36 +579,32 @@ cudaError_t run_passes(const kvc_dims& d, const __nv_bfloat16* q_obs, const __nv
   a.ns = n - alpha;
   a.alpha = alpha;
   a.M = M;
+  a.MP = (M + 15) / 16 * 16;
   a.units = units;
+  const long long unit_bytes = (long long)n * D * 2;
+  const long long nb = std::max(1ll, ((long long)units * unit_bytes + kBatchKeyBytes - 1) /
+                                         kBatchKeyBytes);
+  a.ubatch = (int)((units + nb - 1) / nb);
+  a.tiles0 = (n + 127) / 128;
+  a.tiles1 = (a.ns + 127) / 128;
+  a.smax = (int)score_stat_chunks(n);
   a.sl2 = 1.4426950408889634f / sqrtf((float)D);
   a.stats = stats;
-  a.rowbias = rowbias;
   a.scores = scores;
+  a.gsync = gsync;
   a.err = err;
-  // row statistics over all n keys
-  const int qt = M > 128 ? 2 : 1;
-  const int kr0 = qt == 1 ? 256 : 128;
-  a.tiles = (n + kr0 - 1) / kr0;
-  const int tiles0 = a.tiles;
-  e = qt == 1 ? launch_pass<D, 0, 1>(mk, mq, a, stream) : launch_pass<D, 0, 2>(mk, mq, a, stream);
-  if (e != cudaSuccess) return e;
-  e = launch_score_combine(stats, kSplit * tiles0, M, units, rowbias, stream);
-  if (e != cudaSuccess) return e;
-  // per-key column sums over the scored keys
-  a.tiles = (a.ns + 127) / 128;
-  const int qt1 = (M + 15) / 16 * 16 > 128 ? 2 : 1;
-  return qt1 == 1 ? launch_pass<D, 1, 1>(mk, mq, a, stream) : launch_pass<D, 1, 2>(mk, mq, a, stream);
+  return M > 128 ? launch_fused<D, 2>(mk, mq, a, stream) : launch_fused<D, 1>(mk, mq, a, stream);
 }
 
 }  // namespace
 
-// Scores of one layer on the tensor cores: stats, row normalisers and the per-key
-// column sums (the same contract as the warp-level path).
+// Scores of one layer on the tensor cores: row statistics, their merge into row
+// normalisers and the per-key column sums, in one launch.
 cudaError_t launch_score_tc(const kvc_dims& d, const __nv_bfloat16* q_obs, const __nv_bfloat16* k,
-                            float2* stats, float* rowbias, float* scores, unsigned* err,
+                            float2* stats, unsigned* gsync, float* scores, unsigned* err,
                             cudaStream_t stream) {
-  if (d.head_dim == 128) return run_passes<128>(d, q_obs, k, stats, rowbias, scores, err, stream);
-  if (d.head_dim == 64) return run_passes<64>(d, q_obs, k, stats, rowbias, scores, err, stream);
+  if (d.head_dim == 128) return run_fused<128>(d, q_obs, k, stats, gsync, scores, err, stream);
+  if (d.head_dim == 64) return run_fused<64>(d, q_obs, k, stats, gsync, scores, err, stream);
   return cudaErrorInvalidValue;
 }
 
