@@ -5,9 +5,9 @@
 // values per token over 32 consecutive channels; zero-point = group min,
 // scale = (max - min) / (2^b - 1); both stored as fp16 (round to nearest even).
 // Codes use the stored fp16 values: code = rint((x - Z) / S) clamped to
-// [0, 2^b - 1], evaluated with explicit IEEE round-to-nearest fp32 subtract and
-// divide (no contraction, no reciprocal), round-half-to-even conversion;
-// S == 0 gives code 0. MiniKV Algorithm 1 (decoding): new tokens go to a 16-bit
+// [0, 2^b - 1], the IEEE round-to-nearest fp32 subtract and divide (no
+// contraction) and round-half-to-even conversion; S == 0 gives code 0 (the divide
+// is taken through the reciprocal wherever that gives the same code). MiniKV Algorithm 1 (decoding): new tokens go to a 16-bit
 // buffer that is quantized as it fills; here the oldest 32 tokens are quantized
 // as one group whenever the window reaches R tokens.
 #include "quant_device.cuh"

@@ -7,7 +7,8 @@
 // scale = (max - min) / (2^b - 1), both stored as fp16 (round to nearest even).
 // Codes use the stored fp16 values: code = rint((x - Z) / S) clamped to
 // [0, 2^b - 1], with explicit IEEE round-to-nearest fp32 subtract and divide (no
-// contraction, no reciprocal) and round-half-to-even conversion; S == 0 gives 0.
+// contraction) and round-half-to-even conversion; S == 0 gives 0. The divide is
+// taken through the reciprocal where that provably gives the same code.
 #pragma once
 
 #include "kvc_internal.cuh"
@@ -15,18 +16,30 @@
 namespace kvc {
 
 __device__ __forceinline__ void group_params(float lo, float hi, int bits, __half& S, __half& Z,
-                                             float& Sf, float& Zf) {
+                                             float& Sf, float& Zf, float& rS) {
   const float rng = __fsub_rn(hi, lo);
   const float s32 = __fdiv_rn(rng, (float)((1 << bits) - 1));
   S = __float2half_rn(s32);
   Z = __float2half_rn(lo);
   Sf = __half2float(S);
   Zf = __half2float(Z);
+  rS = Sf == 0.f ? 0.f : __frcp_rn(Sf);
 }
 
-__device__ __forceinline__ int quant_code(float x, float Zf, float Sf, int bits) {
+// code = rint((x - Z) / S) with the quotient first rounded to fp32 (IEEE
+// division), clamped to [0, 2^b - 1]; S == 0 gives 0. Evaluated as (x - Z) * rS,
+// rS the correctly rounded reciprocal of S: that product and the rounded quotient
+// each lie within 2^-24 (relative) of the exact quotient plus one rounding, so they
+// differ by less than 2^-22 |q|, and their nearest integers agree unless the
+// product lies within that distance of a half-integer. There (margin 2^-18 |q|)
+// the division itself is evaluated, so every code equals the division's.
+__device__ __forceinline__ int quant_code(float x, float Zf, float Sf, float rS, int bits) {
   if (Sf == 0.f) return 0;
-  const float q = __fdiv_rn(__fsub_rn(x, Zf), Sf);
+  const float d = __fsub_rn(x, Zf);
+  float q = __fmul_rn(d, rS);
+  const float fr = __fsub_rn(q, floorf(q));
+  if (fabsf(__fsub_rn(fr, 0.5f)) <= 3.814697265625e-06f * fmaxf(1.f, fabsf(q)))
+    q = __fdiv_rn(d, Sf);
   const int c = __float2int_rn(q);
   const int top = (1 << bits) - 1;
   return c < 0 ? 0 : (c > top ? top : c);
@@ -85,24 +98,24 @@ __device__ void quantize_block(GroupSmem<D, NT>& s, uint8_t* __restrict__ blk) {
     float lo = s.klo[0][g], hi = s.khi[0][g];
 #pragma unroll
     for (int p = 1; p < NP; ++p) { lo = fminf(lo, s.klo[p][g]); hi = fmaxf(hi, s.khi[p][g]); }
-    __half S, Z; float Sf, Zf;
-    group_params(lo, hi, BITS, S, Z, Sf, Zf);
+    __half S, Z; float Sf, Zf, rS;
+    group_params(lo, hi, BITS, S, Z, Sf, Zf, rS);
 #pragma unroll
     for (int t = 0; t < PER; ++t)
       s.kc[part * PER + t][g] =
-          (uint8_t)quant_code(__bfloat162float(s.k[part * PER + t][g]), Zf, Sf, BITS);
+          (uint8_t)quant_code(__bfloat162float(s.k[part * PER + t][g]), Zf, Sf, rS, BITS);
     if (part == 0) { kS[kperm(g, D)] = S; kZ[kperm(g, D)] = Z; }
   }
   if (act) {
     float lo = s.vlo[0][g], hi = s.vhi[0][g];
 #pragma unroll
     for (int p = 1; p < NP; ++p) { lo = fminf(lo, s.vlo[p][g]); hi = fmaxf(hi, s.vhi[p][g]); }
-    __half S, Z; float Sf, Zf;
-    group_params(lo, hi, BITS, S, Z, Sf, Zf);
+    __half S, Z; float Sf, Zf, rS;
+    group_params(lo, hi, BITS, S, Z, Sf, Zf, rS);
 #pragma unroll
     for (int j = 0; j < PER; ++j)
       s.vc[vt][vgc * KVC_GROUP + part * PER + j] =
-          (uint8_t)quant_code(__bfloat162float(vrow[j]), Zf, Sf, BITS);
+          (uint8_t)quant_code(__bfloat162float(vrow[j]), Zf, Sf, rS, BITS);
     if (part == 0) { vS[vs_index(vt, vgc, NGC)] = S; vZ[vsz_index(vt, vgc, NGC)] = Z; }
   }
   __syncthreads();

@@ -205,10 +205,11 @@ pool_topk_kernel(const float* __restrict__ scores, float* __restrict__ pooled, i
 // One thread-block cluster of kCluster CTAs per (sequence, kv head). CTA r pools
 // and selects over its segment [r * seg, (r + 1) * seg) of the scores (staged in
 // shared memory with a halo of (w - 1) / 2 on each side). Each radix pass builds a
-// 256-bin histogram per CTA; the CTAs read each other's histograms through
-// distributed shared memory after one cluster barrier, so every CTA takes the same
-// decision. The ordered compaction adds the (greater, equal) counts of the
-// preceding CTAs of the cluster.
+// 256-bin histogram per CTA (per-warp histograms, then summed); the CTAs read each other's histograms through distributed shared
+// memory after one cluster barrier, so every CTA takes the same decision and also
+// learns, per CTA, how many of its elements the pass already decided "kept" (bins
+// above the selected one): the ordered compaction needs no further exchange. The
+// passes stop early once the selected bin is kept whole.
 constexpr int kCluster = 8;
 constexpr int kCThreads = 256;
 constexpr int kCWarps = kCThreads / 32;
@@ -218,10 +219,11 @@ struct ClusterSmem {
   unsigned whist[kCWarps][256];   // per-warp histograms of the current pass
   unsigned hist[2][256];          // this CTA's histogram, by pass parity (read remotely)
   unsigned total[256];            // the cluster's histogram
-  unsigned cnt[2];                // (greater, equal) counts of this segment (read remotely)
+  unsigned red[kCWarps][kCluster];
+  unsigned gtc[kCluster];         // per CTA: elements decided kept by the bins above
+  unsigned eqc[kCluster];         // per CTA: elements in the final selected bin
   unsigned warp_gt[kCWarps], warp_eq[kCWarps];
-  unsigned base_gt, base_eq;
-  unsigned sel_bin, krem;
+  unsigned sel_bin, krem, done;
 };
 
 __device__ __forceinline__ unsigned cluster_rank() {
@@ -241,23 +243,26 @@ __device__ __forceinline__ unsigned ld_cluster_u32(const unsigned* p, unsigned r
   return v;
 }
 
-__global__ void __launch_bounds__(kCThreads)
-pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ pooled, int ns,
-                         int w, int k_sel, int32_t* __restrict__ kept) {
-  __shared__ ClusterSmem s;
-  extern __shared__ __align__(16) float dyn[];
+// Dynamic shared memory of the selection for a segment of `seg` and pool radius hw.
+__host__ __device__ inline size_t select_smem_floats(int seg, int hw) {
+  return (size_t)((seg + 2 * hw + 4 + 3) / 4 * 4) + seg;
+}
+
+// Pool and select within the cluster; CTA `rank` writes the kept positions of its
+// segment to out (ascending, ranks offset by the preceding CTAs). No remote
+// shared-memory access remains when it returns; the caller ends with a cluster
+// barrier before any CTA of the cluster exits.
+__device__ void cluster_pool_select(ClusterSmem& s, float* dyn, const float* __restrict__ sc,
+                                    float* __restrict__ pg, int32_t* __restrict__ out, int ns,
+                                    int w, int k_sel) {
   const unsigned rank = cluster_rank();
-  const int unit = blockIdx.x / kCluster;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seg = (ns + kCluster - 1) / kCluster;
   const int i0 = min(ns, (int)rank * seg), i1 = min(ns, i0 + seg);
   const int n_loc = i1 - i0;
   const int hw = (w - 1) / 2;
-  const float* sc = scores + (size_t)unit * ns;
-  float* pg = pooled + (size_t)unit * ns;
-  int32_t* out = kept + (size_t)unit * k_sel;
-  float* sx = dyn;                    // scores of [i0 - hw, i1 + hw) (-inf outside the row)
-  float* pl = dyn + seg + 2 * hw;     // pooled scores of [i0, i1)
+  float* sx = dyn;                                          // [i0 - hw, i1 + hw), -inf outside
+  float* pl = dyn + (seg + 2 * hw + 4 + 3) / 4 * 4;          // pooled scores of [i0, i1)
 
   // 1. stage the segment with its halo: every element an independent 4-byte
   //    asynchronous copy (all in flight at once); -inf outside the row
@@ -273,26 +278,47 @@ pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ p
   }
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
   __syncthreads();
-  // 2. max-pool (window clipped to the row: the halo outside it is -inf)
-  for (int t = threadIdx.x; t < n_loc; t += kCThreads) {
-    float m = sx[t + hw];
-    for (int d = 0; d < 2 * hw + 1; ++d) m = fmaxf(m, sx[t + d]);
-    pl[t] = m;
-    pg[i0 + t] = m;
+  // 2. max-pool, four outputs per thread: the windows of outputs t0..t0+3 share
+  //    their middle [t0 + 3, t0 + 2hw]; reads past the halo only feed outputs past
+  //    the segment, which are not written
+  for (int q = threadIdx.x; 4 * q < n_loc; q += kCThreads) {
+    const int t0 = 4 * q;
+    float m[4];
+    if (hw == 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m[j] = sx[t0 + j];
+    } else {
+      float core = -INFINITY;
+      for (int d = 3; d <= 2 * hw; ++d) core = fmaxf(core, sx[t0 + d]);
+      const float a0 = sx[t0], a1 = sx[t0 + 1], a2 = sx[t0 + 2];
+      const float b1 = sx[t0 + 2 * hw + 1], b2 = sx[t0 + 2 * hw + 2], b3 = sx[t0 + 2 * hw + 3];
+      m[0] = fmaxf(core, fmaxf(a0, fmaxf(a1, a2)));
+      m[1] = fmaxf(core, fmaxf(a1, fmaxf(a2, b1)));
+      m[2] = fmaxf(core, fmaxf(a2, fmaxf(b1, b2)));
+      m[3] = fmaxf(core, fmaxf(b1, fmaxf(b2, b3)));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (t0 + j < n_loc) { pl[t0 + j] = m[j]; pg[i0 + t0 + j] = m[j]; }
   }
   if (k_sel >= ns) {   // everything is kept
     for (int t = threadIdx.x; t < n_loc; t += kCThreads) out[i0 + t] = i0 + t;
     return;
   }
   if (k_sel <= 0) return;
-  if (threadIdx.x == 0) s.krem = (unsigned)k_sel;
-  __syncthreads();
+  if (threadIdx.x == 0) { s.krem = (unsigned)k_sel; s.done = 0u; }
 
   // 3. radix select of the k-th largest pooled score (fp32 bits: scores are >= 0)
   unsigned prefix = 0, mask = 0;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = threadIdx.x; i < kCWarps * 256; i += kCThreads) (&s.whist[0][0])[i] = 0u;
+  unsigned gacc[kCluster];         // this thread's bin: per CTA, counts of bins above the selection
+  unsigned v[kCluster];
+#pragma unroll
+  for (int r = 0; r < kCluster; ++r) gacc[r] = 0u;
+  int shift = 24;
+  for (int pass = 0; pass < 4; ++pass, shift -= 8) {
+    unsigned* h = s.hist[pass & 1];
+#pragma unroll
+    for (int ww = 0; ww < kCWarps; ++ww) s.whist[ww][threadIdx.x] = 0u;   // 256 bins
     __syncthreads();
     for (int t = threadIdx.x; t < n_loc; t += kCThreads) {
       const unsigned u = __float_as_uint(pl[t]);
@@ -300,22 +326,20 @@ pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ p
     }
     __syncthreads();
     {
-      const int b = threadIdx.x;   // kCThreads == 256 bins
-      unsigned h = 0;
+      unsigned hb = 0;
 #pragma unroll
-      for (int ww = 0; ww < kCWarps; ++ww) h += s.whist[ww][b];
-      s.hist[pass & 1][b] = h;
+      for (int ww = 0; ww < kCWarps; ++ww) hb += s.whist[ww][threadIdx.x];
+      h[threadIdx.x] = hb;
     }
     cluster_sync_all();   // every CTA's histogram of this pass is complete
     {
       const int b = threadIdx.x;
-      unsigned v[kCluster];
 #pragma unroll
-      for (int r = 0; r < kCluster; ++r) v[r] = ld_cluster_u32(&s.hist[pass & 1][b], (unsigned)r);
-      unsigned h = 0;
+      for (int r = 0; r < kCluster; ++r) v[r] = ld_cluster_u32(&h[b], (unsigned)r);
+      unsigned tot = 0;
 #pragma unroll
-      for (int r = 0; r < kCluster; ++r) h += v[r];
-      s.total[b] = h;
+      for (int r = 0; r < kCluster; ++r) tot += v[r];
+      s.total[b] = tot;
     }
     __syncthreads();
     if (warp == 0) {
@@ -335,51 +359,72 @@ pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ p
       if (suf >= krem && above < krem) {
         unsigned cum = above;
         for (int b = 8 * lane + 7; b >= 8 * lane; --b) {
-          const unsigned h = s.total[b];
-          if (cum + h >= krem) { s.sel_bin = (unsigned)b; s.krem = krem - cum; break; }
-          cum += h;
+          const unsigned hb = s.total[b];
+          if (cum + hb >= krem) {
+            s.sel_bin = (unsigned)b;
+            s.krem = krem - cum;
+            s.done = (cum + hb == krem) ? 1u : 0u;   // the bin is kept whole
+            break;
+          }
+          cum += hb;
         }
       }
     }
     __syncthreads();
-    prefix |= s.sel_bin << shift;
+    const unsigned sel = s.sel_bin;
+    if ((unsigned)threadIdx.x > sel) {
+#pragma unroll
+      for (int r = 0; r < kCluster; ++r) gacc[r] += v[r];
+    }
+    prefix |= sel << shift;
     mask |= 255u << shift;
+    if (s.done || pass == 3) {
+      if ((unsigned)threadIdx.x == sel) {
+#pragma unroll
+        for (int r = 0; r < kCluster; ++r) s.eqc[r] = v[r];
+      }
+      break;
+    }
   }
-  const unsigned tau = prefix, need_eq = s.krem;
+  // tau: the selected value (all 32 bits decided), or, when the passes stopped
+  // early, the lowest value of the selected bin, every element >= tau being kept
+  const unsigned tau = prefix;
+  const bool ge = s.done != 0u;
+  const unsigned need_eq = ge ? 0u : s.krem;
+  // per-CTA counts of the bins above the selection, summed over the block
+#pragma unroll
+  for (int r = 0; r < kCluster; ++r) {
+    unsigned x = gacc[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) s.red[warp][r] = x;
+  }
+  __syncthreads();
+  if (threadIdx.x < kCluster) {
+    unsigned x = 0;
+#pragma unroll
+    for (int ww = 0; ww < kCWarps; ++ww) x += s.red[ww][threadIdx.x];
+    s.gtc[threadIdx.x] = x;
+  }
+  __syncthreads();
+  unsigned base_gt = 0, base_eq = 0;
+  for (unsigned r = 0; r < rank; ++r) { base_gt += s.gtc[r]; base_eq += s.eqc[r]; }
+  if (ge) { base_gt += base_eq; base_eq = 0; }
 
   // 4. ordered compaction: warp w owns the contiguous span [w*span, (w+1)*span) of
-  //    the segment; the counts of the preceding warps and CTAs give the offsets
+  //    the segment; the preceding CTAs' and warps' counts give the offsets
   const int span = (n_loc + kCWarps - 1) / kCWarps;
   const int w0 = min(n_loc, warp * span), w1 = min(n_loc, w0 + span);
   unsigned gt = 0, eq = 0;
   for (int base = w0; base < w1; base += 32) {
     const int t = base + lane;
     const unsigned u = t < w1 ? __float_as_uint(pl[t]) : 0u;
-    gt += __popc(__ballot_sync(0xffffffffu, t < w1 && u > tau));
-    eq += __popc(__ballot_sync(0xffffffffu, t < w1 && u == tau));
+    gt += __popc(__ballot_sync(0xffffffffu, t < w1 && (ge ? u >= tau : u > tau)));
+    eq += __popc(__ballot_sync(0xffffffffu, t < w1 && !ge && u == tau));
   }
   if (lane == 0) { s.warp_gt[warp] = gt; s.warp_eq[warp] = eq; }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    unsigned g = 0, e = 0;
-    for (int ww = 0; ww < kCWarps; ++ww) { g += s.warp_gt[ww]; e += s.warp_eq[ww]; }
-    s.cnt[0] = g;
-    s.cnt[1] = e;
-  }
-  cluster_sync_all();
-  if (warp == 0) {
-    // lanes r < rank read CTA r's counts; warp sums
-    unsigned g = 0, e = 0;
-    if (lane < (int)rank) { g = ld_cluster_u32(&s.cnt[0], (unsigned)lane); e = ld_cluster_u32(&s.cnt[1], (unsigned)lane); }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      g += __shfl_xor_sync(0xffffffffu, g, o);
-      e += __shfl_xor_sync(0xffffffffu, e, o);
-    }
-    if (lane == 0) { s.base_gt = g; s.base_eq = e; }
-  }
-  __syncthreads();
-  unsigned egt = s.base_gt, eeq = s.base_eq;
+  unsigned egt = base_gt, eeq = base_eq;
   for (int ww = 0; ww < warp; ++ww) { egt += s.warp_gt[ww]; eeq += s.warp_eq[ww]; }
   unsigned pos = egt + (eeq < need_eq ? eeq : need_eq);
   unsigned eq_seen = eeq;
@@ -387,7 +432,8 @@ pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ p
   for (int base = w0; base < w1; base += 32) {
     const int t = base + lane;
     const unsigned u = t < w1 ? __float_as_uint(pl[t]) : 0u;
-    const bool is_gt = t < w1 && u > tau, is_eq = t < w1 && u == tau;
+    const bool is_gt = t < w1 && (ge ? u >= tau : u > tau);
+    const bool is_eq = t < w1 && !ge && u == tau;
     const unsigned beq = __ballot_sync(0xffffffffu, is_eq);
     const bool take = is_gt || (is_eq && eq_seen + __popc(beq & lt) < need_eq);
     const unsigned bt = __ballot_sync(0xffffffffu, take);
@@ -398,13 +444,23 @@ pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ p
     pos += __popc(bt);
     eq_seen += __popc(beq);
   }
+}
+
+__global__ void __launch_bounds__(kCThreads)
+pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ pooled, int ns,
+                         int w, int k_sel, int32_t* __restrict__ kept) {
+  __shared__ ClusterSmem s;
+  extern __shared__ __align__(16) float dyn[];
+  const int unit = blockIdx.x / kCluster;
+  cluster_pool_select(s, dyn, scores + (size_t)unit * ns, pooled + (size_t)unit * ns,
+                      kept + (size_t)unit * k_sel, ns, w, k_sel);
   cluster_sync_all();   // no CTA leaves while another may still read its shared memory
 }
 
 cudaError_t launch_topk_cluster(const float* scores, float* pooled, int units, int ns, int w,
                                 int k_sel, int32_t* kept, cudaStream_t stream) {
   const int seg = (ns + kCluster - 1) / kCluster;
-  const size_t sm = (size_t)(2 * seg + (w - 1)) * sizeof(float);
+  const size_t sm = select_smem_floats(seg, (w - 1) / 2) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(pool_topk_cluster_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
