@@ -6,6 +6,8 @@
 #include <cstring>
 #include <new>
 
+#include <mutex>
+
 #include "kvc_internal.cuh"
 
 using kvc::LayerState;
@@ -191,6 +193,26 @@ kvc_status finish_prefill(kvc_cache* c, int layer, int n_kept, const int32_t* ke
 }  // namespace
 
 void kvc::count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+cudaError_t kvc::ensure_smem(const void* kernel, size_t bytes) {
+  struct Entry { const void* kernel; int device; size_t bytes; };
+  static std::mutex mu;
+  static std::vector<Entry> set;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (Entry& x : set)
+    if (x.kernel == kernel && x.device == dev) {
+      if (x.bytes >= bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+      if (e == cudaSuccess) x.bytes = bytes;
+      return e;
+    }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) set.push_back({kernel, dev, bytes});
+  return e;
+}
 
 extern "C" {
 

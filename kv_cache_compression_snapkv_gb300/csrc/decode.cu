@@ -725,8 +725,11 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" :: "r"(smem_u32(&cbar[i])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     for (int p = 0; p < 2; ++p) { ctl.count[p] = 0u; ctl.mask[p] = 0u; ctl.gen[p] = 0u; }
-    for (int k = 0; k < QR; ++k) q_copy(k);
   }
+  pdl_wait();      // the previous kernels' writes (queries, cache) are visible
+  pdl_release();
+  if (threadIdx.x == 0)
+    for (int k = 0; k < QR; ++k) q_copy(k);
   if (threadIdx.x < P.n_layers) lay[threadIdx.x] = P.L[threadIdx.x];
   __syncthreads();
 
@@ -911,9 +914,16 @@ cudaError_t launch_one(const DecParams& P, const kvc_cache* c, const __nv_bfloat
   }
   const int total_units = P.n_layers * P.units;
   const int grid = std::min(n_sm[dev], total_units);
-  decode_kernel<D, BITS, GQ><<<grid, C::kThreadsC, C::total, stream>>>(P, c->packed, c->win_k,
-                                                                       c->win_v, q, out);
-  return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(C::kThreadsC);
+  cfg.dynamicSmemBytes = C::total;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1] = {pdl_attr()};
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, BITS, GQ>, P, c->packed, c->win_k, c->win_v,
+                            q, out);
 }
 
 template <int D, int BITS>

@@ -203,6 +203,28 @@ namespace kvc {
 // Process-wide count of kernels launched by this library (kvc_launch_count).
 void count_launches(int n);
 
+// Raise `kernel`'s dynamic shared-memory limit to at least `bytes` on the current
+// device; the driver call is made only when the limit has to grow.
+cudaError_t ensure_smem(const void* kernel, size_t bytes);
+
+// Programmatic dependent launch. Kernels of this library are launched with the
+// programmatic-stream-serialization attribute: a kernel may be scheduled while the
+// previous kernel of the stream drains, runs its shared-memory set-up, and waits
+// in pdl_wait() (until the previous grids have completed and their writes are
+// visible) before it reads or writes global memory; pdl_release() then lets the
+// next kernel be scheduled early in turn. Without the attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Launch attribute for the above (fills attr, returns it for chaining).
+inline cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 // --------------------------------------------------------------- launch helpers
 // (defined in the .cu files; all enqueue on `stream` and return a CUDA error)
 cudaError_t launch_score(const kvc_cache* c, int layer, const __nv_bfloat16* q_obs,

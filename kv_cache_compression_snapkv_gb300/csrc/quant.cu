@@ -27,6 +27,8 @@ gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
                     uint8_t* __restrict__ packed, int cap_groups, int block_bytes, int R,
                     __nv_bfloat16* __restrict__ win_k, __nv_bfloat16* __restrict__ win_v) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  pdl_wait();      // the selection is complete
+  pdl_release();
   const int j = blockIdx.x, unit = blockIdx.y;
   const int n_groups = n_kept / KVC_GROUP;
   const __nv_bfloat16* K = k + (size_t)unit * n * D;
@@ -75,6 +77,8 @@ append_kernel(AppendParams P, int layer_begin, int units, int R, const __nv_bflo
               const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ win_k,
               __nv_bfloat16* __restrict__ win_v, uint8_t* __restrict__ packed, int block_bytes) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  pdl_wait();      // the previous step's reads of the window are complete
+  pdl_release();
   const int lrel = blockIdx.x / units, unit = blockIdx.x % units;
   const size_t wunit = (size_t)(layer_begin + lrel) * units + unit;
   __nv_bfloat16* wk = win_k + wunit * R * D;
@@ -176,7 +180,7 @@ constexpr size_t group_smem() { return sizeof(GroupSmem<D, kThreads>); }
 
 template <typename Kern>
 static cudaError_t set_smem(Kern kernel, size_t bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  return ensure_smem(reinterpret_cast<const void*>(kernel), bytes);
 }
 
 // Packs the kept tokens' whole groups and writes the initial window (one launch).
@@ -192,9 +196,18 @@ cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* ke
     const size_t sm = group_smem<D>();
     cudaError_t e = set_smem(gather_quant_kernel<D, BITS>, sm);
     if (e != cudaSuccess) return e;
-    gather_quant_kernel<D, BITS><<<dim3(groups + 1, units), kThreads, sm, stream>>>(
-        k, v, kept, n_kept, d.prompt_len, d.obs_window, c->packed + ls.packed_off, ls.cap_groups,
-        c->block_bytes, d.window_len, c->win_k + woff, c->win_v + woff);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(groups + 1, units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sm;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1] = {pdl_attr()};
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gather_quant_kernel<D, BITS>, k, v, kept, n_kept, d.prompt_len,
+                           d.obs_window, c->packed + ls.packed_off, ls.cap_groups,
+                           c->block_bytes, d.window_len, c->win_k + woff, c->win_v + woff);
+    if (e != cudaSuccess) return e;
   });
   count_launches(1);
   return cudaGetLastError();
@@ -223,9 +236,18 @@ cudaError_t launch_append(const kvc_cache* c, int layer_begin, int layer_count,
       const size_t sm = group_smem<D>();
       cudaError_t e = set_smem(append_kernel<D, BITS>, sm);
       if (e != cudaSuccess) return e;
-      append_kernel<D, BITS><<<cnt * units, kThreads, sm, stream>>>(
-          P, layer_begin + base, units, d.window_len, kn, vn, c->win_k, c->win_v, c->packed,
-          c->block_bytes);
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(cnt * units);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = sm;
+      cfg.stream = stream;
+      cudaLaunchAttribute at[1] = {pdl_attr()};
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, append_kernel<D, BITS>, P, layer_begin + base, units,
+                             d.window_len, kn, vn, c->win_k, c->win_v, c->packed,
+                             c->block_bytes);
+      if (e != cudaSuccess) return e;
     });
     count_launches(1);
     const cudaError_t e = cudaGetLastError();

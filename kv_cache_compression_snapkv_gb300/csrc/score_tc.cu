@@ -188,6 +188,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   tc::fence_after_sync();
   const uint32_t tbase = *tmem_holder;
   bool ok = true;
+  pdl_wait();      // the previous kernels' writes (keys, queries, scratch) are visible
+  pdl_release();
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
@@ -552,12 +554,22 @@ cudaError_t launch_fused(const CUtensorMap& mk, const CUtensorMap& mq, const TcA
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = C::total;
   cfg.stream = stream;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: waits across CTAs are safe
   at[0].val.cooperative = 1;
+  at[1] = pdl_attr();
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  // a driver that does not take the dependent-launch attribute on a cooperative
+  // launch gets the plain cooperative launch from then on
+  static bool no_pdl = false;
+  cfg.numAttrs = no_pdl ? 1 : 2;
   e = cudaLaunchKernelEx(&cfg, score_tc_kernel<D, QT>, mk, mq, a);
+  if (e != cudaSuccess && !no_pdl) {
+    cudaGetLastError();
+    no_pdl = true;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, score_tc_kernel<D, QT>, mk, mq, a);
+  }
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaSuccess;

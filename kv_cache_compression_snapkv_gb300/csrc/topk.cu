@@ -452,8 +452,11 @@ pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ p
   __shared__ ClusterSmem s;
   extern __shared__ __align__(16) float dyn[];
   const int unit = blockIdx.x / kCluster;
+  pdl_wait();      // the scores are complete (a no-op on a plain launch)
   cluster_pool_select(s, dyn, scores + (size_t)unit * ns, pooled + (size_t)unit * ns,
                       kept + (size_t)unit * k_sel, ns, w, k_sel);
+  // only now: dependents scheduled earlier would wait on these SMs beside the selection
+  pdl_release();
   cluster_sync_all();   // no CTA leaves while another may still read its shared memory
 }
 
@@ -461,8 +464,7 @@ cudaError_t launch_topk_cluster(const float* scores, float* pooled, int units, i
                                 int k_sel, int32_t* kept, cudaStream_t stream) {
   const int seg = (ns + kCluster - 1) / kCluster;
   const size_t sm = select_smem_floats(seg, (w - 1) / 2) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(pool_topk_cluster_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(pool_topk_cluster_kernel), sm);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units * kCluster);
@@ -475,6 +477,7 @@ cudaError_t launch_topk_cluster(const float* scores, float* pooled, int units, i
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
+  // a plain launch: as a dependent launch the selection ran about twice as long
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, pool_topk_cluster_kernel, scores, pooled, ns, w, k_sel, kept);
   count_launches(1);
@@ -488,8 +491,7 @@ cudaError_t launch_topk(const float* scores, float* pooled, int units, int ns, i
     return launch_topk_cluster(scores, pooled, units, ns, w, k_sel, kept, stream);
   if (ns <= kSmemMax) {
     const size_t sm = (size_t)ns * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(pool_topk_kernel<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(pool_topk_kernel<true>), sm);
     if (e != cudaSuccess) return e;
     pool_topk_kernel<true><<<units, kTopkThreads, sm, stream>>>(scores, pooled, ns, w, k_sel,
                                                                  kept);
