@@ -29,6 +29,11 @@ CASES = {
     "long_needles": (synth.small_spec(5, n_layers=2, batch=1, n_q_heads=8, n_kv_heads=2,
                                       prompt_len=4096, obs_window=64, avg_budget=256,
                                       window_len=128), 130, "score"),
+    # a large budget (4,096 of a 32,768-key prompt kept per head), 4-bit
+    "large_budget": (synth.small_spec(2, n_layers=1, batch=1, n_q_heads=2, n_kv_heads=1,
+                                      head_dim=64, prompt_len=32800, obs_window=32,
+                                      avg_budget=4096, schedule="uniform", bits=4,
+                                      window_len=64), 12, "score"),
     # the GPU given the oracle's selection (storage + decode parity alone)
     "oracle_selection": (synth.small_spec(2, n_layers=2, batch=2, n_q_heads=8, n_kv_heads=2,
                                           prompt_len=1500, obs_window=32, avg_budget=160,
