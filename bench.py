@@ -51,6 +51,24 @@ def rank_info():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def max_over_ranks(values, world, device=None):
+    """Element-wise maximum of `values` (floats) over the ranks of the process group
+    (the slowest rank decides a step's time); identity when world == 1."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(tokens_per_rank, world, dec_ms_max):
+    """Whole-job decode tokens/s: every rank decodes its own replica of the workload
+    (weak scaling), in the slowest rank's time."""
+    return tokens_per_rank * world / (dec_ms_max / 1e3)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -326,14 +344,12 @@ def run_gpu(args):
     att_ms_all = [x for a in atts for x in a]
     att_ms = statistics.mean(att_ms_all)
     step_ms = comp_ms + dec_ms
-    if world > 1:
-        t = torch.tensor([step_ms, dec_ms, comp_ms, att_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, dec_ms, comp_ms, att_ms = [float(v) for v in t.tolist()]
+    step_ms, dec_ms, comp_ms, att_ms = max_over_ranks([step_ms, dec_ms, comp_ms, att_ms], world,
+                                                      device=dev)
 
     hbm, tc, peak_kind = peaks()
     tokens = B * S * world
-    value = tokens / (dec_ms / 1e3)
+    value = job_throughput(B * S, world, dec_ms)
     # decode attention: algorithmic bytes per launch / mean launch duration
     mean_bytes = statistics.mean(dec_bytes)
     dec_gbs = mean_bytes / (att_ms / 1e3) / 1e9
