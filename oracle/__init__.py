@@ -5,6 +5,7 @@ written from the pages' statement of the method:
 
   * budgets.py     per-layer token budgets (uniform / PyramidKV-style linear)
   * snapkv.py      observation-window scores, 1-D max-pooling, per-head top-k
+  * sinks.py       attention-sink + recent-token selection (StreamingLLM-style)
   * quant.py       KIVI-style asymmetric group quantization (keys per channel,
                    values per token), b = 2 or 4 bits, fp16 scale and zero-point
   * cache.py       the compressed cache: prefill selection + quantization, the
@@ -22,6 +23,7 @@ CPU-baseline leg of `bench.py` may import it; the product path never routes here
 """
 from .budgets import plan_budgets
 from .snapkv import window_scores, max_pool, select_topk, snapkv_select
+from .sinks import sinks_window_select
 from .quant import (quantize_group, quantize_keys, quantize_values, dequantize_keys,
                     dequantize_values)
 from .cache import OracleCache
@@ -29,6 +31,7 @@ from .arithmetic import (blog_budget_row, minikv_sizes)
 
 __all__ = [
     "plan_budgets", "window_scores", "max_pool", "select_topk", "snapkv_select",
+    "sinks_window_select",
     "quantize_group", "quantize_keys", "quantize_values", "dequantize_keys",
     "dequantize_values", "OracleCache", "blog_budget_row",
     "minikv_sizes",
