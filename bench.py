@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-sinks", action="store_true",
+                    help="skip the compression pass with the sink + recent selection")
     return ap.parse_args()
 
 
@@ -339,6 +341,24 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
 
+    # the attention-sink + recent-token selection (4 sinks, no scoring): the same
+    # layers compressed with it, outside the timed steps
+    sink_ms = None
+    if not args.no_sinks:
+        cs0, cs1 = ev(), ev()
+        sms = []
+        for i in range(4):
+            K.kvc_cache_reset(cache)
+            cs0.record(stream)
+            for l in range(L):
+                x = prompt[l]
+                K.kvc_prefill_sinks(cache, l, 4, x["k"], x["v"])
+            cs1.record(stream)
+            torch.cuda.synchronize()
+            if i > 0:
+                sms.append(cs0.elapsed_time(cs1))
+        sink_ms = statistics.mean(sms) / L
+
     comp_ms = statistics.mean(comps)
     dec_ms = statistics.mean([sum(a) + sum(b) for a, b in zip(apps, atts)])
     att_ms_all = [x for a in atts for x in a]
@@ -366,6 +386,12 @@ def run_gpu(args):
         comp_flops += 2 * B * Hq * spec.obs_window * spec.prompt_len * D if scored else 0
     t_roof = max(comp_bytes / (hbm * 1e9), comp_flops / (tc * 1e12))
     comp_frac = t_roof / (comp_ms / 1e3)
+    # sink + recent selection: kept rows read, packed groups and window rows written
+    sink_bytes = 0
+    for l in range(L):
+        kept = min(budgets[l], ns)
+        sink_bytes += (B * Hk * kept * D * 2 * 2 + B * Hk * (kept // 32) * block_bytes
+                       + B * Hk * (kept % 32 + spec.obs_window) * D * 2 * 2 * 2)
 
     traffic = profiled_traffic("decode.cu")
     roofline = {"kernel": "decode_kernel (fused append + split-K decode attention, all layers "
@@ -390,6 +416,10 @@ def run_gpu(args):
         "cache_gbs": dec_gbs, "cache_frac_of_hbm": dec_gbs / hbm,
         "decode_attn_us_per_launch": att_ms * 1e3,
         "compress_ms_per_layer": comp_ms / L,
+        "compress_sinks": None if sink_ms is None else {
+            "ms_per_layer": sink_ms, "bytes": sink_bytes,
+            "frac": sink_bytes / (hbm * 1e9) / (sink_ms * L / 1e3),
+            "note": "4 attention sinks + the most recent tokens within each layer's budget"},
         "compress_roofline": {"bytes": comp_bytes, "flops": comp_flops, "t_roof_ms": t_roof * 1e3,
                               "frac": comp_frac},
         "wall_ms_per_step": wall * 1e3,

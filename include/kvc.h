@@ -138,6 +138,26 @@ kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets,
                                 const void* v, kvc_cache** cache, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * kvc_prefill_sinks -- like kvc_prefill_compress with the attention-sink +
+ *   recent-token selection in place of the scored one (blog "KV Cache
+ *   Compression: Eviction and Quantization", "Measured on a real model": the first
+ *   4 tokens plus the most recent ones within the budget; PyramidKV's StreamingLLM
+ *   baseline, the first k - alpha and the last alpha tokens, is n_sinks = k).
+ *   Per (sequence, kv head), with k = min(the layer's budget, n - alpha) and
+ *   s = min(n_sinks, k): positions [0, s) and [n - alpha - (k - s), n - alpha) are
+ *   kept (ascending); whole groups of 32 go to the packed store and the rest,
+ *   then the alpha observation tokens, start the bf16 window, as for every
+ *   selection. No scoring: no observation queries are read. One launch (the
+ *   kept positions are formed and stored, for kvc_export_layer, by the packing
+ *   kernel). The cache must exist (kvc_cache_create or an earlier prefill call).
+ *   n_sinks >= 0.
+ *   Errors: KVC_E_ARG, KVC_E_SHAPE (initial window not shorter than R),
+ *   KVC_E_STATE (layer already compressed), KVC_E_OOM, KVC_E_CUDA.
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_prefill_sinks(kvc_cache* cache, int32_t layer, int32_t n_sinks, const void* k,
+                             const void* v, void* stream);
+
+/* ---------------------------------------------------------------------------
  * kvc_prefill_selected -- like kvc_prefill_compress, but with the kept
  *   positions supplied by the caller instead of scored (any selection policy:
  *   e.g. attention sinks + recent tokens, StreamingLLM-style).

@@ -63,6 +63,7 @@ _SIGS = {
     "kvc_prefill_compress": [ctypes.POINTER(KvcDims), _P, _I, _P, _P, _P,
                              ctypes.POINTER(ctypes.c_void_p), _P],
     "kvc_prefill_selected": [_P, _I, _P, _I, _P, _P, _P],
+    "kvc_prefill_sinks": [_P, _I, _I, _P, _P, _P],
     "kvc_cache_create": [ctypes.POINTER(KvcDims), _P, ctypes.POINTER(ctypes.c_void_p)],
     "kvc_append": [_P, _I, _P, _P, _P],
     "kvc_append_layers": [_P, _I, _I, _P, _P, _P],
@@ -177,6 +178,12 @@ def kvc_prefill_selected(cache: Cache, layer: int, kept, n_kept: int, k, v, stre
                                      _stream(stream)), "kvc_prefill_selected")
 
 
+def kvc_prefill_sinks(cache: Cache, layer: int, n_sinks: int, k, v, stream=None):
+    """Attention-sink + recent-token selection of `layer` (no scoring), then packing."""
+    _check(_lib.kvc_prefill_sinks(cache.handle, layer, n_sinks, _ptr(k), _ptr(v),
+                                  _stream(stream)), "kvc_prefill_sinks")
+
+
 def kvc_append(cache: Cache, layer: int, k_new, v_new, stream=None):
     _check(_lib.kvc_append(cache.handle, layer, _ptr(k_new), _ptr(v_new), _stream(stream)),
            "kvc_append")
@@ -266,7 +273,8 @@ def exported_symbols() -> list:
 
 
 __all__ = ["KvcDims", "KvcError", "Cache", "make_dims", "dims_from_spec", "kvc_plan_budgets",
-           "kvc_cache_create", "kvc_prefill_compress", "kvc_prefill_selected", "kvc_append",
+           "kvc_cache_create", "kvc_prefill_compress", "kvc_prefill_selected", "kvc_prefill_sinks",
+           "kvc_append",
            "kvc_append_layers", "kvc_decode_attn", "kvc_decode_step", "kvc_free",
            "kvc_layer_info_get", "kvc_export_layer", "kvc_scores_layer", "kvc_cache_reset",
            "kvc_launch_count", "kvc_check_device", "kvc_select_noalloc", "LIB_PATH",

@@ -174,11 +174,12 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
 }
 
 kvc_status finish_prefill(kvc_cache* c, int layer, int n_kept, const int32_t* kept,
-                          const void* k, const void* v, cudaStream_t stream) {
+                          const void* k, const void* v, cudaStream_t stream, int sinks = -1,
+                          int32_t* kept_out = nullptr) {
   const auto* K = static_cast<const __nv_bfloat16*>(k);
   const auto* V = static_cast<const __nv_bfloat16*>(v);
   // one launch: whole groups into the packed store plus the initial window
-  cudaError_t e = kvc::launch_gather_quant(c, layer, kept, n_kept, K, V, stream);
+  cudaError_t e = kvc::launch_gather_quant(c, layer, kept, n_kept, K, V, stream, sinks, kept_out);
   if (e != cudaSuccess) return from_cuda(e);
   LayerState& ls = c->L[layer];
   ls.n_kept = n_kept;
@@ -337,6 +338,32 @@ kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets, in
     ls.scored = 0;
   }
   return finish_prefill(c, layer, n_kept, kept, k, v, s);
+}
+
+kvc_status kvc_prefill_sinks(kvc_cache* c, int32_t layer, int32_t n_sinks, const void* k,
+                             const void* v, void* stream) {
+  if (!c || !k || !v || n_sinks < 0) return KVC_E_ARG;
+  if (layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
+  LayerState& ls = c->L[layer];
+  if (ls.prefilled) return KVC_E_STATE;
+  const int ns = c->dims.prompt_len - c->dims.obs_window;
+  const int n_kept = ls.budget < ns ? ls.budget : ns;
+  if (n_kept % KVC_GROUP + c->dims.obs_window >= c->dims.window_len) return KVC_E_SHAPE;
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n_kept >= ns) {                 // the budget keeps every token
+    ls.scored = 0;
+    return finish_prefill(c, layer, n_kept, nullptr, k, v, s);
+  }
+  if (!ls.kept_ptr) {
+    const int units = c->dims.batch * c->dims.n_kv_heads;
+    ls.kept_ptr = static_cast<int32_t*>(dev_alloc(c, (size_t)units * n_kept * 4));
+    if (!ls.kept_ptr) return KVC_E_OOM;
+  }
+  ls.scored = 1;                      // the positions are stored for export
+  return finish_prefill(c, layer, n_kept, nullptr, k, v, s, n_sinks < n_kept ? n_sinks : n_kept,
+                        ls.kept_ptr);
 }
 
 kvc_status kvc_prefill_selected(kvc_cache* c, int32_t layer, const int32_t* kept, int32_t n_kept,

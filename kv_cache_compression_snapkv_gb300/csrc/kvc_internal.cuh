@@ -231,9 +231,12 @@ cudaError_t launch_score(const kvc_cache* c, int layer, const __nv_bfloat16* q_o
                          const __nv_bfloat16* k, cudaStream_t stream);
 cudaError_t launch_pool_topk(const kvc_cache* c, int layer, int32_t* kept_out, int k_sel,
                              cudaStream_t stream);
+// Gather + quantize + pack of the kept tokens: kept[] positions, or (kept == NULL,
+// sinks >= 0) the sink + recent-window positions, stored to kept_out; else all.
 cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* kept, int n_kept,
                                 const __nv_bfloat16* k, const __nv_bfloat16* v,
-                                cudaStream_t stream);
+                                cudaStream_t stream, int sinks = -1,
+                                int32_t* kept_out = nullptr);
 cudaError_t launch_append(const kvc_cache* c, int layer_begin, int layer_count,
                           const __nv_bfloat16* k_new, const __nv_bfloat16* v_new,
                           const int* flush_flags, cudaStream_t stream);

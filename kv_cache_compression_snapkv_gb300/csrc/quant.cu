@@ -19,13 +19,16 @@ constexpr int kThreads = 256;
 
 // --------------------------------------------------------------------- kernels
 // grid.x = group index j within the unit (j == n_groups: the initial window),
-// grid.y = unit (b * H + h)
+// grid.y = unit (b * H + h). Kept position p of the unit is kept[p] when `kept` is
+// given; else, with sinks >= 0, the sink + recent-window position (p < sinks: p;
+// else n - alpha - (n_kept - sinks) + (p - sinks)), also stored to kept_out; else p.
 template <int D, int BITS>
 __global__ void __launch_bounds__(kThreads)
 gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                     const int32_t* __restrict__ kept, int n_kept, int n, int alpha,
                     uint8_t* __restrict__ packed, int cap_groups, int block_bytes, int R,
-                    __nv_bfloat16* __restrict__ win_k, __nv_bfloat16* __restrict__ win_v) {
+                    __nv_bfloat16* __restrict__ win_k, __nv_bfloat16* __restrict__ win_v,
+                    int sinks, int32_t* __restrict__ kept_out) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   pdl_wait();      // the selection is complete
   pdl_release();
@@ -34,6 +37,13 @@ gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
   const __nv_bfloat16* K = k + (size_t)unit * n * D;
   const __nv_bfloat16* V = v + (size_t)unit * n * D;
   const int32_t* kp = kept ? kept + (size_t)unit * n_kept : nullptr;
+  int32_t* ko = kept_out ? kept_out + (size_t)unit * n_kept : nullptr;
+  const int recent0 = n - alpha - (n_kept - sinks);
+  auto index_of = [&](int p) -> int {
+    if (kp) return kp[p];
+    if (sinks >= 0) return p < sinks ? p : recent0 + (p - sinks);
+    return p;
+  };
   if (j == n_groups) {
     // initial window: the kept tokens past the last whole group, then the
     // alpha observation tokens, in ring slots 0 .. W-1
@@ -42,7 +52,8 @@ gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
     __nv_bfloat16* wv = win_v + (size_t)unit * R * D;
     for (int i = threadIdx.x; i < W * D; i += kThreads) {
       const int w = i / D, c = i % D;
-      const int idx = w < tail ? (kp ? kp[n_full + w] : n_full + w) : n - alpha + (w - tail);
+      const int idx = w < tail ? index_of(n_full + w) : n - alpha + (w - tail);
+      if (ko && c == 0 && w < tail) ko[n_full + w] = idx;
       window_store(wk, wv, w, c, D, K[(size_t)idx * D + c], V[(size_t)idx * D + c]);
     }
     return;
@@ -51,7 +62,8 @@ gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
   constexpr int CH = D / 8;   // 16-byte chunks per row
   for (int i = threadIdx.x; i < KVC_GROUP * CH; i += kThreads) {
     const int t = i / CH, ch = i % CH;
-    const int idx = kp ? kp[j * KVC_GROUP + t] : j * KVC_GROUP + t;
+    const int idx = index_of(j * KVC_GROUP + t);
+    if (ko && ch == 0) ko[j * KVC_GROUP + t] = idx;
     *reinterpret_cast<uint4*>(&s.k[t][ch * 8]) =
         __ldg(reinterpret_cast<const uint4*>(K + (size_t)idx * D) + ch);
     *reinterpret_cast<uint4*>(&s.v[t][ch * 8]) =
@@ -186,7 +198,7 @@ static cudaError_t set_smem(Kern kernel, size_t bytes) {
 // Packs the kept tokens' whole groups and writes the initial window (one launch).
 cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* kept, int n_kept,
                                 const __nv_bfloat16* k, const __nv_bfloat16* v,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, int sinks, int32_t* kept_out) {
   const kvc_dims& d = c->dims;
   const LayerState& ls = c->L[layer];
   const int groups = n_kept / KVC_GROUP;
@@ -206,7 +218,8 @@ cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* ke
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gather_quant_kernel<D, BITS>, k, v, kept, n_kept, d.prompt_len,
                            d.obs_window, c->packed + ls.packed_off, ls.cap_groups,
-                           c->block_bytes, d.window_len, c->win_k + woff, c->win_v + woff);
+                           c->block_bytes, d.window_len, c->win_k + woff, c->win_v + woff,
+                           sinks, kept_out);
     if (e != cudaSuccess) return e;
   });
   count_launches(1);

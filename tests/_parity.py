@@ -19,7 +19,7 @@ import numpy as np
 import torch
 
 import synth
-from oracle import OracleCache, snapkv_select
+from oracle import OracleCache, sinks_window_select, snapkv_select
 
 DECODE_RTOL = 2e-3
 TIE_RTOL = 1e-5
@@ -95,8 +95,9 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
               dev="cuda"):
     """Full comparison on a workload the oracle finishes in seconds.
 
-    selection: "score" (GPU scores and selects; the oracle does the same) or
-               "oracle" (the GPU is given the oracle's kept positions).
+    selection: "score" (GPU scores and selects; the oracle does the same),
+               "oracle" (the GPU is given the oracle's kept positions) or
+               ("sinks", s) (both keep s attention sinks + the most recent tokens).
     """
     K = kvc()
     rep = Report()
@@ -115,11 +116,29 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
         bud = budgets[layer]
         oc = OracleCache(B, Hq, Hk, D, spec.bits, spec.group_size, spec.window_len)
         scoring = bud < n - a
-        oc.prefill(k_np, v_np, a, budget=bud if scoring else None, q_obs=q_np,
-                   pool_kernel=spec.pool_kernel)
+        sinks = selection[1] if isinstance(selection, tuple) else None
+        if sinks is not None:
+            sel = sinks_window_select(n - a, bud, sinks)
+            oc.prefill(k_np, v_np, a, kept=[[sel] * Hk for _ in range(B)])
+        else:
+            oc.prefill(k_np, v_np, a, budget=bud if scoring else None, q_obs=q_np,
+                       pool_kernel=spec.pool_kernel)
         kd, vd = x["k"].to(dev), x["v"].to(dev)
         qd = x["q_obs"].to(dev) if "q_obs" in x else None
-        if selection == "oracle" or not scoring:
+        if sinks is not None:
+            if cache is None:
+                cache = K.kvc_cache_create(dims, budgets)
+            K.kvc_prefill_sinks(cache, layer, sinks, kd, vd)
+            ex = K.kvc_export_layer(cache, layer)
+            torch.cuda.synchronize()
+            if scoring:
+                for b in range(B):
+                    for h in range(Hk):
+                        np.testing.assert_array_equal(ex["kept"][b, h].cpu().numpy(),
+                                                      oc.heads[b][h].kept)
+                        rep.kept_compared += 1
+            ok_heads = [(b, h) for b in range(B) for h in range(Hk)]
+        elif selection == "oracle" or not scoring:
             if cache is None:
                 cache = K.kvc_cache_create(dims, budgets)
             nk = len(oc.heads[0][0].kept)

@@ -34,6 +34,10 @@ CASES = {
                                       head_dim=64, prompt_len=32800, obs_window=32,
                                       avg_budget=4096, schedule="uniform", bits=4,
                                       window_len=64), 12, "score"),
+    # attention sinks + recent tokens (no scoring), pyramid budgets over 3 layers
+    "sinks_window": (synth.small_spec(2, n_layers=3, batch=2, n_q_heads=8, n_kv_heads=2,
+                                      prompt_len=1000, obs_window=32, avg_budget=96,
+                                      window_len=64), 40, ("sinks", 4)),
     # the GPU given the oracle's selection (storage + decode parity alone)
     "oracle_selection": (synth.small_spec(2, n_layers=2, batch=2, n_q_heads=8, n_kv_heads=2,
                                           prompt_len=1500, obs_window=32, avg_budget=160,
