@@ -12,8 +12,13 @@
 //   unit = (layer, sequence b, kv head h); its work is cut into chunks of 16
 //   window slots or 2 packed group blocks. There is one CTA per SM; CTA i takes
 //   the units i, 2P-1-i, 2P+i, ... (P CTAs, snake order over units that come
-//   largest first), lays their chunks end to end, and warp w takes chunks w,
-//   w + NW, w + 2 NW, ... of that list. Each warp double-buffers its chunks in
+//   largest first) and lays their chunks end to end. When the CTA's units all fit
+//   in the query ring, warp w takes the w-th of NW contiguous runs of that list
+//   (a unit is split over as few warps as the balance allows, so few partial
+//   states are merged); otherwise warp w takes chunks w, w + NW, w + 2 NW, ...,
+//   which keeps the warps within a few units of each other (a unit's queries are
+//   issued only when the unit QR places before it has been merged). Each warp
+//   double-buffers its chunks in
 //   shared memory with bulk asynchronous copies (cp.async.bulk on per-slot
 //   mbarriers, bounded waits): the copy of its next-but-one chunk is issued as
 //   soon as a slot is read. A warp keeps an online softmax for the g query heads
@@ -564,7 +569,7 @@ struct DecCfg {
   static constexpr int SLOT = warp_buf_bytes<D, BITS>();   // one chunk
   static constexpr int DEPW = GQ * (D + 2);                // floats of one deposit: m, l, o
   static constexpr int QB = GQ * D * 2;                    // bytes of one unit's queries
-  static constexpr int kQRing = 4;                         // query ring entries
+  static constexpr int kQRing = 4;                         // query ring entries (<= 8)
   // Two deposit buffers (by unit parity): a warp leaving unit k waits, before it
   // deposits, for the merge of unit k - 2 (it may already compute unit k + 1).
   static constexpr int NDEP = 2;
@@ -593,7 +598,9 @@ struct DecCtl {
   unsigned count[2];
   unsigned mask[2];
   unsigned gen[2];
+  int qunit[8];      // unit whose queries the ring entry was last issued for
 };
+static_assert(sizeof(DecCtl) <= 64, "control words fit their shared-memory region");
 
 // Unit k of CTA i (snake order): k even -> k*P + i, k odd -> (k+1)*P - 1 - i.
 __device__ __forceinline__ int snake_unit(int k, int i, int P) {
@@ -713,6 +720,7 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
     const int g = unit_of(k);
     if (g >= total_units) return;
     uint64_t* b = &qbar[k % QR];
+    *reinterpret_cast<volatile int*>(&ctl.qunit[k % QR]) = k;
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
                  :: "r"(smem_u32(b)), "r"((uint32_t)C::QB) : "memory");
@@ -725,6 +733,7 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" :: "r"(smem_u32(&cbar[i])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     for (int p = 0; p < 2; ++p) { ctl.count[p] = 0u; ctl.mask[p] = 0u; ctl.gen[p] = 0u; }
+    for (int e = 0; e < 8; ++e) ctl.qunit[e] = -1;
   }
   pdl_wait();      // the previous kernels' writes (queries, cache) are visible
   pdl_release();
@@ -767,27 +776,39 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
     }
   };
 
+  // chunk list positions of this warp: a contiguous run when the CTA's units all
+  // fit in the query ring, else every NW-th position (-1: none left)
+  int n_units = 0, total = 0;
+  for (int k = 0; unit_of(k) < total_units; ++k) { ++n_units; total += chunks_of(unit_of(k)); }
+  const bool blocked = n_units <= QR;
+  const int per = (total + NW - 1) / NW;
+  const int w0 = min(total, warp * per), w1 = min(total, w0 + per);
+  auto position = [&](int n) -> int {
+    if (blocked) return w0 + n < w1 ? w0 + n : -1;
+    return warp + n * NW;   // past the list: advance() fails
+  };
+
   Cursor cur{0, 0, unit_of(0), 0};
   cur.n = cur.g < total_units ? chunks_of(cur.g) : 0;
   Cursor pre = cur;   // cursor of the prefetch stream (runs two chunks ahead)
   // prime the two slots
   for (int s = 0; s < 2; ++s) {
-    const int pos = warp + s * NW;
-    if (advance(pre, pos) && lane == 0) issue(s, pre, pos);
+    const int pos = position(s);
+    if (pos >= 0 && advance(pre, pos) && lane == 0) issue(s, pre, pos);
   }
 
   WarpState<D, GQ> st;
   QRegs<D, GQ> qr;
-  int k_cur = -1;
+  int k_cur = -1, base_cur = 0;   // the warp's current unit and its first list position
   bool ok = true;
   const int units_per_layer = P.units;
 
-  auto deposit = [&](int k) {   // hand over unit k's state; the last depositor merges
+  auto deposit = [&](int k, int base) {   // hand over unit k's state; the last depositor merges
     const int par = k % C::NDEP;
-    const Cursor& cu = cur;   // (unused: expected count from unit k itself)
-    (void)cu;
     const int g = unit_of(k);
-    const unsigned expect = (unsigned)min(NW, chunks_of(g));
+    // depositors: the warps whose positions meet the unit's [base, base + chunks)
+    const unsigned expect = blocked ? (unsigned)((base + chunks_of(g) - 1) / per - base / per + 1)
+                                    : (unsigned)min(NW, chunks_of(g));
     // the deposit buffer of unit k is free once unit k - NDEP is merged
     if (lane == 0) {
       bool ready = false;
@@ -824,18 +845,27 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
   };
 
   for (int n = 0;; ++n) {
-    const int pos = warp + n * NW;
-    if (!advance(cur, pos)) break;
+    const int pos = position(n);
+    if (pos < 0 || !advance(cur, pos)) break;
     const int slot = n & 1;
     if (cur.k != k_cur) {
-      if (k_cur >= 0) deposit(k_cur);
+      if (k_cur >= 0) deposit(k_cur, base_cur);
       if (!ok) break;
       k_cur = cur.k;
+      base_cur = cur.base;
       state_init(st);
-      // this unit's queries (bounded wait on the query ring entry)
+      // this unit's queries: the ring entry must hold this unit's copy (issued once
+      // the unit QR places before it is merged, so the entry's mbarrier is at most
+      // one phase behind), then a bounded wait for that copy
       bool done = false;
+      for (unsigned it = 0; it < kWaitLimit && !done; ++it)
+        done = *reinterpret_cast<volatile int*>(&ctl.qunit[k_cur % QR]) == k_cur;
       const uint32_t qpar = (uint32_t)((k_cur / QR) & 1);
-      for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(&qbar[k_cur % QR], qpar);
+      if (done) {
+        done = false;
+        for (unsigned it = 0; it < kWaitLimit && !done; ++it)
+          done = mbar_try_wait(&qbar[k_cur % QR], qpar);
+      }
       if (!__all_sync(0xffffffffu, done)) { if (lane == 0) atomicOr(P.err, 1u); ok = false; break; }
       load_qregs<D, GQ>(qr, qring + (k_cur % QR) * GQ * D);
     }
@@ -884,13 +914,13 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
       packed_warp<D, BITS, GQ>(st, qr, sbuf, min(kGroupsPerWarp, L.n_groups - g0), P.sl2);
     }
     __syncwarp();   // the slot is read: refill it with the chunk two steps ahead
-    const int npos = warp + (n + 2) * NW;
-    if (advance(pre, npos) && lane == 0) {
+    const int npos = position(n + 2);
+    if (npos >= 0 && advance(pre, npos) && lane == 0) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       issue(slot, pre, npos);
     }
   }
-  if (ok && k_cur >= 0) deposit(k_cur);
+  if (ok && k_cur >= 0) deposit(k_cur, base_cur);
 }
 
 template <int D, int BITS, int GQ>
