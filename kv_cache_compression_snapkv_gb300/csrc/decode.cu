@@ -574,8 +574,7 @@ struct DecCfg {
   // deposits, for the merge of unit k - 2 (it may already compute unit k + 1).
   static constexpr int NDEP = 2;
   static constexpr int bytes(int nw) {
-    return nw * 2 * SLOT + NDEP * nw * DEPW * 4 + 16 + kQRing * QB + (2 * nw + kQRing) * 8 + 64 +
-           KVC_MAX_LAUNCH_LAYERS * (int)sizeof(DecLayer);
+    return nw * 2 * SLOT + NDEP * nw * DEPW * 4 + 16 + kQRing * QB + (2 * nw + kQRing) * 8 + 64;
   }
   static constexpr int pick(int nw) { return (nw <= 4 || bytes(nw) <= 224 * 1024) ? nw : pick(nw - 1); }
   static constexpr int NW = pick(GQ > 4 ? 8 : 12);           // warps per CTA
@@ -586,8 +585,7 @@ struct DecCfg {
   static constexpr int oQ = (oDep + NDEP * NW * DEPW * 4 + 15) / 16 * 16;
   static constexpr int oBars = oQ + kQRing * QB;
   static constexpr int oCtl = oBars + (2 * NW + kQRing) * 8;
-  static constexpr int oLay = oCtl + 64;
-  static constexpr int total = oLay + KVC_MAX_LAUNCH_LAYERS * (int)sizeof(DecLayer);
+  static constexpr int total = oCtl + 64;
   static_assert(SLOT % 16 == 0 && DEPW % 1 == 0 && QB % 16 == 0, "alignment");
   static_assert(oQ % 16 == 0 && oBars % 8 == 0, "alignment");
 };
@@ -708,7 +706,9 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
   uint64_t* cbar = reinterpret_cast<uint64_t*>(dsm + C::oBars);   // [NW][2] chunk slots
   uint64_t* qbar = cbar + 2 * NW;                                 // [QR] query ring
   DecCtl& ctl = *reinterpret_cast<DecCtl*>(dsm + C::oCtl);
-  DecLayer* lay = reinterpret_cast<DecLayer*>(dsm + C::oLay);
+  // layer table read in place from the launch parameters, each read warp-uniform (a
+  // per-thread copy into shared memory made the constant cache serialise)
+  const DecLayer* lay = P.L;
   __nv_bfloat16* qring = reinterpret_cast<__nv_bfloat16*>(dsm + C::oQ);
   const int P_ = gridDim.x, cta = blockIdx.x;
   const int total_units = P.n_layers * P.units;
@@ -726,8 +726,7 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
                  :: "r"(smem_u32(b)), "r"((uint32_t)C::QB) : "memory");
     bulk_g2s(qring + (k % QR) * GQ * D, q + (size_t)g * GQ * D, (uint32_t)C::QB, b);
   };
-  // barriers and control words, then the first units' queries (their addresses
-  // need no layer table); the layer table into shared memory meanwhile
+  // barriers and control words, then the first units' queries
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2 * NW + QR; ++i)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" :: "r"(smem_u32(&cbar[i])) : "memory");
@@ -739,7 +738,6 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
   pdl_release();
   if (threadIdx.x == 0)
     for (int k = 0; k < QR; ++k) q_copy(k);
-  if (threadIdx.x < P.n_layers) lay[threadIdx.x] = P.L[threadIdx.x];
   __syncthreads();
 
   // this warp's chunk stream: positions w, w + NW, ... of the CTA's chunk list
