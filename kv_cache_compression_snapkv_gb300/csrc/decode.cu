@@ -10,7 +10,7 @@
 //
 // Work decomposition (one persistent launch for a range of layers):
 //   unit = (layer, sequence b, kv head h); its work is cut into chunks of 16
-//   window slots or 2 packed group blocks. There is one CTA per SM; CTA i takes
+//   window slots or 1 packed group block. There is one CTA per SM; CTA i takes
 //   the units i, 2P-1-i, 2P+i, ... (P CTAs, snake order over units that come
 //   largest first) and lays their chunks end to end. When the CTA's units all fit
 //   in the query ring, warp w takes the w-th of NW contiguous runs of that list
@@ -71,7 +71,7 @@ struct DecLayer {
   int cap_groups;
   int new_slot;     // ring slot of the token appended in this launch, or -1
   int flush_start;  // ring slot of the oldest token when this launch flushes a group, or -1
-  int wchunks;      // window chunks (16 slots) per unit; packed chunks (2 groups) follow
+  int wchunks;      // window chunks (16 slots) per unit; packed chunks (1 group) follow
   int pchunks;      // packed chunks per unit
   long long packed_off;
 };

@@ -263,8 +263,8 @@ cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float*
                                   int32_t* kept_out, int k_sel, cudaStream_t stream);
 
 // Decode work decomposition: a unit's work is cut into chunks of 16 window slots
-// or 2 packed groups.
-constexpr int kDecGroupsPerChunk = 2;
+// or 1 packed group (fine chunks keep the warps of a CTA evenly loaded).
+constexpr int kDecGroupsPerChunk = 1;
 constexpr int kDecSlotsPerChunk = 16;
 
 // Scoring: partial row statistics kept per (unit, row) for a prompt of n keys
