@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-sinks", action="store_true",
                     help="skip the compression pass with the sink + recent selection")
+    ap.add_argument("--no-exact16", action="store_true",
+                    help="skip the decode launches over a 16-bit (unquantized) cache")
     return ap.parse_args()
 
 
@@ -359,6 +361,41 @@ def run_gpu(args):
                 sms.append(cs0.elapsed_time(cs1))
         sink_ms = statistics.mean(sms) / L
 
+    # 16-bit storage (every kept token exact in the bf16 window), same selection and
+    # budgets: decode launches over the exact cache, outside the timed steps
+    exact16 = None
+    if not args.no_exact16:
+        import dataclasses
+        S16 = min(32, S)
+        R16 = (max(min(b_, spec.prompt_len - spec.obs_window) for b_ in budgets)
+               + spec.obs_window + S16 + 31) // 32 * 32
+        spec16 = dataclasses.replace(spec, bits=16, window_len=R16)
+        dims16 = K.dims_from_spec(spec16, max_new_tokens=S16)
+        cache16 = K.kvc_cache_create(dims16, budgets)
+        for l in range(L):
+            x = prompt[l]
+            K.kvc_prefill_compress(dims16, budgets, l, x.get("q_obs"), x["k"], x["v"],
+                                   cache=cache16)
+        e16 = [(ev(), ev()) for _ in range(S16)]
+        bytes16 = []
+        for t in range(S16):
+            tot = 0
+            for l in range(L):
+                info = K.kvc_layer_info_get(cache16, l)
+                tot += B * Hk * (info["window_tokens"] + 1) * D * 2 * 2
+            bytes16.append(tot + L * B * Hq * D * (2 + 4) + L * B * Hk * D * 2 * 2)
+            flush.max()
+            e16[t][0].record(stream)
+            K.kvc_decode_step(cache16, 0, L, qs[t], kns[t], vns[t], out)
+            e16[t][1].record(stream)
+        torch.cuda.synchronize()
+        us16 = statistics.mean(a.elapsed_time(b) for a, b in e16[3:]) * 1e3
+        b16 = statistics.mean(bytes16[3:])
+        exact16 = {"us_per_launch": us16, "bytes_per_launch": b16,
+                   "gbs": b16 / (us16 * 1e-6) / 1e9, "window_len": R16,
+                   "note": "bits=16: the kept tokens stay exact in the bf16 window"}
+        cache16.close()
+
     comp_ms = statistics.mean(comps)
     dec_ms = statistics.mean([sum(a) + sum(b) for a, b in zip(apps, atts)])
     att_ms_all = [x for a in atts for x in a]
@@ -416,6 +453,8 @@ def run_gpu(args):
         "cache_gbs": dec_gbs, "cache_frac_of_hbm": dec_gbs / hbm,
         "decode_attn_us_per_launch": att_ms * 1e3,
         "compress_ms_per_layer": comp_ms / L,
+        "decode_16bit": None if exact16 is None else dict(
+            exact16, frac=exact16["gbs"] / hbm),
         "compress_sinks": None if sink_ms is None else {
             "ms_per_layer": sink_ms, "bytes": sink_bytes,
             "frac": sink_bytes / (hbm * 1e9) / (sink_ms * L / 1e3),

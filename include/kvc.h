@@ -85,9 +85,14 @@ typedef struct kvc_dims {
   int32_t obs_window;     /* alpha, trailing observation/instruction tokens;       */
                           /*   0 only with KVC_SCHED_NONE budgets (no scoring)     */
   int32_t pool_kernel;    /* w, odd max-pool width (1 = no pooling)                */
-  int32_t bits;           /* 2 or 4                                                */
+  int32_t bits;           /* 2 or 4; or 16: no quantization, every kept token     */
+                          /*   stays exact in the bf16 window (no packed store,    */
+                          /*   no flush); R must then hold the kept, observation   */
+                          /*   and max_new_tokens appended tokens of every layer   */
+                          /*   (with the full budget: plain dense attention)       */
   int32_t group_size;     /* G, quantization group; must be 32                     */
   int32_t window_len;     /* R, bf16 recent window; a multiple of G, 32..1024      */
+                          /*   (up to 65536 with bits == 16)                       */
   int32_t max_new_tokens; /* decode steps the cache is sized for                   */
   kvc_alloc_fn alloc;     /* optional; NULL = cudaMalloc                           */
   kvc_free_fn free;       /* optional; must be set when alloc is                   */

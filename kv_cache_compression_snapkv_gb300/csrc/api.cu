@@ -47,9 +47,11 @@ kvc_status check_dims(const kvc_dims* d) {
   if (d->prompt_len < 1) return KVC_E_SHAPE;
   if (d->obs_window < 0 || d->obs_window >= d->prompt_len) return KVC_E_SHAPE;
   if (d->pool_kernel < 1 || d->pool_kernel % 2 == 0) return KVC_E_ARG;
-  if (d->bits != 2 && d->bits != 4) return KVC_E_ARG;
+  if (d->bits != 2 && d->bits != 4 && d->bits != 16) return KVC_E_ARG;
   if (d->group_size != KVC_GROUP) return KVC_E_ARG;
-  if (d->window_len < KVC_GROUP || d->window_len > 1024 || d->window_len % KVC_GROUP)
+  // 16-bit storage keeps the whole cache in the bf16 window, which may then be long
+  if (d->window_len < KVC_GROUP || d->window_len > (d->bits == 16 ? 65536 : 1024) ||
+      d->window_len % KVC_GROUP)
     return KVC_E_SHAPE;
   if (d->max_new_tokens < 0) return KVC_E_ARG;
   if (d->obs_window >= d->window_len) return KVC_E_SHAPE;
@@ -91,6 +93,14 @@ int kept_cap(const kvc_dims& d, int budget) {
   return budget < ns ? budget : ns;
 }
 
+// The initial window of a layer keeping n_kept tokens fits the ring: the tokens past
+// the last whole group plus the observation tokens (2/4-bit), or, with 16-bit
+// storage (no packed store, no flush), every kept, observation and appended token.
+bool window_fits(const kvc_dims& d, int n_kept) {
+  if (d.bits == 16) return n_kept + d.obs_window + d.max_new_tokens <= d.window_len;
+  return n_kept % KVC_GROUP + d.obs_window < d.window_len;
+}
+
 kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out) {
   kvc_status st = check_dims(dims);
   if (st != KVC_OK) return st;
@@ -103,7 +113,7 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
   for (int l = 0; l < d.n_layers; ++l) {
     if (budgets[l] < 0) return KVC_E_ARG;
     const int nk = kept_cap(d, budgets[l]);
-    if (nk % KVC_GROUP + d.obs_window >= d.window_len) return KVC_E_SHAPE;
+    if (!window_fits(d, nk)) return KVC_E_SHAPE;
     if (nk < ns) scoring = true;
   }
   if (scoring && (d.obs_window < 1 || g * d.obs_window > 256)) return KVC_E_SHAPE;
@@ -112,14 +122,15 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
   if (!c) return KVC_E_OOM;
   c->dims = d;
   c->g = g;
-  c->block_bytes = kvc::block_bytes(d.head_dim, d.bits);
+  c->block_bytes = kvc::block_bytes(d.head_dim, d.bits == 16 ? 2 : d.bits);   // 16-bit: unused
   if (cudaGetDevice(&c->device) != cudaSuccess) { delete c; return KVC_E_CUDA; }
   c->L.resize(d.n_layers);
   size_t packed = 0;
   for (int l = 0; l < d.n_layers; ++l) {
     LayerState& ls = c->L[l];
     ls.budget = kept_cap(d, budgets[l]);
-    ls.cap_groups = ls.budget / KVC_GROUP +
+    ls.cap_groups = d.bits == 16 ? 0 :   // 16-bit storage: everything stays in the window
+                    ls.budget / KVC_GROUP +
                     (KVC_GROUP - 1 + d.obs_window + d.max_new_tokens + KVC_GROUP - 1) / KVC_GROUP + 1;
     ls.packed_off = packed;
     packed += (size_t)units * ls.cap_groups * c->block_bytes;
@@ -182,10 +193,11 @@ kvc_status finish_prefill(kvc_cache* c, int layer, int n_kept, const int32_t* ke
   cudaError_t e = kvc::launch_gather_quant(c, layer, kept, n_kept, K, V, stream, sinks, kept_out);
   if (e != cudaSuccess) return from_cuda(e);
   LayerState& ls = c->L[layer];
+  const bool exact = c->dims.bits == 16;
   ls.n_kept = n_kept;
-  ls.n_groups = n_kept / KVC_GROUP;
+  ls.n_groups = exact ? 0 : n_kept / KVC_GROUP;
   ls.win_start = 0;
-  ls.win_len = n_kept % KVC_GROUP + c->dims.obs_window;
+  ls.win_len = (exact ? n_kept : n_kept % KVC_GROUP) + c->dims.obs_window;
   ls.appended = 0;
   ls.prefilled = 1;
   return KVC_OK;
@@ -348,7 +360,7 @@ kvc_status kvc_prefill_sinks(kvc_cache* c, int32_t layer, int32_t n_sinks, const
   if (ls.prefilled) return KVC_E_STATE;
   const int ns = c->dims.prompt_len - c->dims.obs_window;
   const int n_kept = ls.budget < ns ? ls.budget : ns;
-  if (n_kept % KVC_GROUP + c->dims.obs_window >= c->dims.window_len) return KVC_E_SHAPE;
+  if (!window_fits(c->dims, n_kept)) return KVC_E_SHAPE;
   DeviceGuard dg(c->device);
   if (!dg.ok) return KVC_E_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -375,7 +387,7 @@ kvc_status kvc_prefill_selected(kvc_cache* c, int32_t layer, const int32_t* kept
   const int ns = c->dims.prompt_len - c->dims.obs_window;
   if (n_kept < 0 || n_kept > ns) return KVC_E_ARG;
   if (n_kept > ls.budget) return KVC_E_CAPACITY;
-  if (n_kept % KVC_GROUP + c->dims.obs_window >= c->dims.window_len) return KVC_E_SHAPE;
+  if (!window_fits(c->dims, n_kept)) return KVC_E_SHAPE;
   DeviceGuard dg(c->device);
   if (!dg.ok) return KVC_E_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -408,7 +420,8 @@ kvc_status kvc_append_layers(kvc_cache* c, int32_t layer_begin, int32_t layer_co
   if (!dg.ok) return KVC_E_CUDA;
   const int R = c->dims.window_len;
   std::vector<int> flush(layer_count);
-  for (int i = 0; i < layer_count; ++i) flush[i] = (c->L[layer_begin + i].win_len + 1 == R);
+  for (int i = 0; i < layer_count; ++i)   // 16-bit storage never flushes
+    flush[i] = c->dims.bits != 16 && c->L[layer_begin + i].win_len + 1 == R;
   cudaError_t e = kvc::launch_append(c, layer_begin, layer_count,
                                      static_cast<const __nv_bfloat16*>(k_new),
                                      static_cast<const __nv_bfloat16*>(v_new), flush.data(),
@@ -459,7 +472,8 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t layer_begin, int32_t layer_coun
   if (!dg.ok) return KVC_E_CUDA;
   const int R = c->dims.window_len;
   std::vector<int> flush(layer_count);
-  for (int i = 0; i < layer_count; ++i) flush[i] = (c->L[layer_begin + i].win_len + 1 == R);
+  for (int i = 0; i < layer_count; ++i)   // 16-bit storage never flushes
+    flush[i] = c->dims.bits != 16 && c->L[layer_begin + i].win_len + 1 == R;
   // one launch: append (+ flush of the oldest group) and attention for every layer
   cudaError_t e = kvc::launch_decode_step(c, layer_begin, layer_count,
                                           static_cast<const __nv_bfloat16*>(q),

@@ -1024,10 +1024,13 @@ cudaError_t launch_common(const kvc_cache* c, int layer_begin, int layer_count,
     const __nv_bfloat16* qb = q + (size_t)base * units * c->g * D;
     float* ob = out + (size_t)base * units * c->g * D;
     cudaError_t e;
-    if (D == 128 && d.bits == 2) e = launch_g<128, 2>(P, c, qb, ob, stream);
-    else if (D == 128 && d.bits == 4) e = launch_g<128, 4>(P, c, qb, ob, stream);
-    else if (D == 64 && d.bits == 2) e = launch_g<64, 2>(P, c, qb, ob, stream);
-    else if (D == 64 && d.bits == 4) e = launch_g<64, 4>(P, c, qb, ob, stream);
+    // 16-bit storage has no packed groups (everything is in the window): any packed
+    // instantiation serves it
+    const int bits = d.bits == 16 ? 2 : d.bits;
+    if (D == 128 && bits == 2) e = launch_g<128, 2>(P, c, qb, ob, stream);
+    else if (D == 128 && bits == 4) e = launch_g<128, 4>(P, c, qb, ob, stream);
+    else if (D == 64 && bits == 2) e = launch_g<64, 2>(P, c, qb, ob, stream);
+    else if (D == 64 && bits == 4) e = launch_g<64, 4>(P, c, qb, ob, stream);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
     count_launches(1);

@@ -18,8 +18,10 @@ namespace {
 constexpr int kThreads = 256;
 
 // --------------------------------------------------------------------- kernels
-// grid.x = group index j within the unit (j == n_groups: the initial window),
-// grid.y = unit (b * H + h). Kept position p of the unit is kept[p] when `kept` is
+// grid.x = group index j within the unit (j < n_pack), then one CTA per 32 rows of
+// the initial window (j >= n_pack); grid.y = unit (b * H + h). n_pack is the number
+// of whole groups of kept tokens (0 with 16-bit storage: every kept token then
+// starts in the window). Kept position p of the unit is kept[p] when `kept` is
 // given; else, with sinks >= 0, the sink + recent-window position (p < sinks: p;
 // else n - alpha - (n_kept - sinks) + (p - sinks)), also stored to kept_out; else p.
 template <int D, int BITS>
@@ -28,12 +30,12 @@ gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
                     const int32_t* __restrict__ kept, int n_kept, int n, int alpha,
                     uint8_t* __restrict__ packed, int cap_groups, int block_bytes, int R,
                     __nv_bfloat16* __restrict__ win_k, __nv_bfloat16* __restrict__ win_v,
-                    int sinks, int32_t* __restrict__ kept_out) {
+                    int sinks, int32_t* __restrict__ kept_out, int n_pack) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   pdl_wait();      // the selection is complete
   pdl_release();
   const int j = blockIdx.x, unit = blockIdx.y;
-  const int n_groups = n_kept / KVC_GROUP;
+  const int n_groups = n_pack;
   const __nv_bfloat16* K = k + (size_t)unit * n * D;
   const __nv_bfloat16* V = v + (size_t)unit * n * D;
   const int32_t* kp = kept ? kept + (size_t)unit * n_kept : nullptr;
@@ -44,13 +46,14 @@ gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
     if (sinks >= 0) return p < sinks ? p : recent0 + (p - sinks);
     return p;
   };
-  if (j == n_groups) {
+  if (j >= n_groups) {
     // initial window: the kept tokens past the last whole group, then the
-    // alpha observation tokens, in ring slots 0 .. W-1
+    // alpha observation tokens, in ring slots 0 .. W-1 (rows [32 wj, 32 wj + 32) here)
     const int n_full = n_groups * KVC_GROUP, tail = n_kept - n_full, W = tail + alpha;
+    const int wj = j - n_groups, w0 = wj * KVC_GROUP, w1 = min(W, w0 + KVC_GROUP);
     __nv_bfloat16* wk = win_k + (size_t)unit * R * D;
     __nv_bfloat16* wv = win_v + (size_t)unit * R * D;
-    for (int i = threadIdx.x; i < W * D; i += kThreads) {
+    for (int i = w0 * D + threadIdx.x; i < w1 * D; i += kThreads) {
       const int w = i / D, c = i % D;
       const int idx = w < tail ? index_of(n_full + w) : n - alpha + (w - tail);
       if (ko && c == 0 && w < tail) ko[n_full + w] = idx;
@@ -201,15 +204,18 @@ cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* ke
                                 cudaStream_t stream, int sinks, int32_t* kept_out) {
   const kvc_dims& d = c->dims;
   const LayerState& ls = c->L[layer];
-  const int groups = n_kept / KVC_GROUP;
+  const bool exact = d.bits == 16;   // 16-bit storage: no packed groups, all in the window
+  const int groups = exact ? 0 : n_kept / KVC_GROUP;
+  const int win_rows = n_kept - groups * KVC_GROUP + d.obs_window;
+  const int win_ctas = (win_rows + KVC_GROUP - 1) / KVC_GROUP;
   const int units = d.batch * d.n_kv_heads;
   const size_t woff = (size_t)layer * units * d.window_len * d.head_dim;
-  KVC_DISPATCH_DB(d.head_dim, d.bits, {
+  KVC_DISPATCH_DB(d.head_dim, exact ? 2 : d.bits, {
     const size_t sm = group_smem<D>();
     cudaError_t e = set_smem(gather_quant_kernel<D, BITS>, sm);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(groups + 1, units);
+    cfg.gridDim = dim3(groups + (win_ctas > 0 ? win_ctas : 1), units);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = sm;
     cfg.stream = stream;
@@ -219,7 +225,7 @@ cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* ke
     e = cudaLaunchKernelEx(&cfg, gather_quant_kernel<D, BITS>, k, v, kept, n_kept, d.prompt_len,
                            d.obs_window, c->packed + ls.packed_off, ls.cap_groups,
                            c->block_bytes, d.window_len, c->win_k + woff, c->win_v + woff,
-                           sinks, kept_out);
+                           sinks, kept_out, groups);
     if (e != cudaSuccess) return e;
   });
   count_launches(1);
@@ -275,7 +281,7 @@ cudaError_t launch_export(const kvc_cache* c, int layer, const kvc_export* dst,
   const LayerState& ls = c->L[layer];
   const int units = d.batch * d.n_kv_heads;
   const size_t woff = (size_t)layer * units * d.window_len * d.head_dim;
-  KVC_DISPATCH_DB(d.head_dim, d.bits, {
+  KVC_DISPATCH_DB(d.head_dim, d.bits == 16 ? 2 : d.bits, {   // 16-bit: window only
     export_kernel<D, BITS><<<dim3(ls.n_groups + 1, units), kThreads, 0, stream>>>(
         c->packed + ls.packed_off, ls.cap_groups, ls.n_groups, c->block_bytes, c->win_k + woff,
         c->win_v + woff, d.window_len, ls.win_start, ls.win_len, *dst);
