@@ -214,6 +214,7 @@ constexpr int kCluster = 8;
 constexpr int kCThreads = 256;
 constexpr int kCWarps = kCThreads / 32;
 constexpr int kMaxSeg = 24 * 1024;   // elements per CTA (two fp32 copies in shared memory)
+constexpr size_t kOnePerSm = 120 * 1024;   // dynamic shared memory that leaves room for one CTA
 
 struct ClusterSmem {
   unsigned whist[kCWarps][256];   // per-warp histograms of the current pass
@@ -452,7 +453,7 @@ pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ p
   __shared__ ClusterSmem s;
   extern __shared__ __align__(16) float dyn[];
   const int unit = blockIdx.x / kCluster;
-  pdl_wait();      // the scores are complete (a no-op on a plain launch)
+  pdl_wait();      // the scores are complete
   cluster_pool_select(s, dyn, scores + (size_t)unit * ns, pooled + (size_t)unit * ns,
                       kept + (size_t)unit * k_sel, ns, w, k_sel);
   // only now: dependents scheduled earlier would wait on these SMs beside the selection
@@ -463,7 +464,11 @@ pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ p
 cudaError_t launch_topk_cluster(const float* scores, float* pooled, int units, int ns, int w,
                                 int k_sel, int32_t* kept, cudaStream_t stream) {
   const int seg = (ns + kCluster - 1) / kCluster;
-  const size_t sm = select_smem_floats(seg, (w - 1) / 2) * sizeof(float);
+  // a dependent launch (its set-up overlaps the scoring launch's end); the shared
+  // memory is padded so that one CTA fits an SM: scheduled early, the CTAs would
+  // otherwise pack several to an SM as the scoring CTAs leave, and run far slower
+  size_t sm = select_smem_floats(seg, (w - 1) / 2) * sizeof(float);
+  if (sm < kOnePerSm) sm = kOnePerSm;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(pool_topk_cluster_kernel), sm);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -471,14 +476,14 @@ cudaError_t launch_topk_cluster(const float* scores, float* pooled, int units, i
   cfg.blockDim = dim3(kCThreads);
   cfg.dynamicSmemBytes = sm;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attr();
   cfg.attrs = attr;
-  // a plain launch: as a dependent launch the selection ran about twice as long
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, pool_topk_cluster_kernel, scores, pooled, ns, w, k_sel, kept);
   count_launches(1);
   if (e != cudaSuccess) return e;
