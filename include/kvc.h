@@ -119,6 +119,27 @@ kvc_status kvc_plan_budgets(const kvc_dims* dims, kvc_schedule schedule,
                             int32_t* budgets_out);
 
 /* ---------------------------------------------------------------------------
+ * kvc_plan_budgets_weighted -- per-layer token budgets in proportion to given
+ *   positive weights (host only, no device work). MiniKV §4.2 "Layer-Specific
+ *   Selectivity", the variance policies: Var-prop (weights = the layers'
+ *   variance scores, see kvc_score_variance) and Var-inv (weights = their
+ *   inverses). Budgets are whole groups of G tokens; every layer gets one group
+ *   and the remaining n_layers * avg_budget / G - n_layers groups are shared in
+ *   proportion to the weights: each weight is scaled to the integer
+ *   q_l = max(1, rint(w_l / max(w) * 2^30)), layer l's quota is
+ *   spare * q_l / sum(q), quotas are floored and the leftover groups go one each
+ *   to the largest remainders (ties to the lower layer), so the budgets sum to
+ *   exactly n_layers * avg_budget. Every budget is finally clipped to
+ *   prompt_len - obs_window.
+ *   weights:     host array of n_layers doubles (read).
+ *   budgets_out: host array of n_layers int32 (written).
+ *   Errors: KVC_E_ARG (null pointer, a weight not positive and finite,
+ *   avg_budget not a positive multiple of G), KVC_E_SHAPE (invalid dims).
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_plan_budgets_weighted(const kvc_dims* dims, int32_t avg_budget,
+                                     const double* weights, int32_t* budgets_out);
+
+/* ---------------------------------------------------------------------------
  * kvc_prefill_compress -- compress one layer's prompt into the cache.
  *   PyramidKV §4.2.2; MiniKV §4.1, §4.4 and Algorithm 1 (prefill part).
  *   If *cache is NULL a cache is created for `dims` and `budgets` (host,
@@ -275,6 +296,17 @@ typedef struct kvc_export {
 
 kvc_status kvc_export_layer(kvc_cache* cache, int32_t layer, const kvc_export* dst,
                             void* stream);
+
+/* kvc_score_variance -- the variance score of the last scored layer (MiniKV
+ * §4.2, Figure 7: the variance of cumulated attention), per (sequence, kv head):
+ * the population variance, over the prompt_len - obs_window selectable
+ * positions, of the selection scores (before pooling), accumulated in fp64 and
+ * written as fp32 to var_out (device, [B][H]). The mean over (B, H) is the
+ * layer's weight for Var-prop / Var-inv budgets. One launch on `stream`. Only
+ * valid right after kvc_prefill_compress of a scoring layer (the scratch is
+ * reused by the next one). Errors: KVC_E_ARG (null pointer), KVC_E_STATE (no
+ * layer scored yet), KVC_E_CUDA. */
+kvc_status kvc_score_variance(kvc_cache* cache, float* var_out, void* stream);
 
 /* kvc_scores_layer -- copy the last scored layer's selection scores (fp32,
  * device [B][H][prompt_len - obs_window]) and pooled scores (same shape);

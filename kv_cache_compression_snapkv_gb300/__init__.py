@@ -60,6 +60,7 @@ _I = ctypes.c_int32
 _S = ctypes.c_int
 _SIGS = {
     "kvc_plan_budgets": [ctypes.POINTER(KvcDims), _S, _I, _I, _P],
+    "kvc_plan_budgets_weighted": [ctypes.POINTER(KvcDims), _I, _P, _P],
     "kvc_prefill_compress": [ctypes.POINTER(KvcDims), _P, _I, _P, _P, _P,
                              ctypes.POINTER(ctypes.c_void_p), _P],
     "kvc_prefill_selected": [_P, _I, _P, _I, _P, _P, _P],
@@ -73,6 +74,7 @@ _SIGS = {
     "kvc_layer_info_get": [_P, _I, ctypes.POINTER(KvcLayerInfo)],
     "kvc_export_layer": [_P, _I, ctypes.POINTER(KvcExport), _P],
     "kvc_scores_layer": [_P, _P, _P, _P],
+    "kvc_score_variance": [_P, _P, _P],
     "kvc_cache_reset": [_P],
     "kvc_select_noalloc": [ctypes.POINTER(KvcDims), _I, _P, _P, _P, _P, _P],
     "kvc_check_device": [_P, _P],
@@ -130,6 +132,18 @@ def kvc_plan_budgets(dims: KvcDims, schedule: str, avg_budget: int,
     out = (ctypes.c_int32 * dims.n_layers)()
     _check(_lib.kvc_plan_budgets(ctypes.byref(dims), SCHED[schedule], avg_budget, pyramid_depth,
                                  out), "kvc_plan_budgets")
+    return list(out)
+
+
+def kvc_plan_budgets_weighted(dims: KvcDims, avg_budget: int, weights: Sequence[float]) -> list:
+    """Budgets in proportion to per-layer weights (Var-prop: the layers' variance
+    scores; Var-inv: their inverses)."""
+    if len(weights) != dims.n_layers:
+        raise ValueError("need one weight per layer")
+    w = (ctypes.c_double * dims.n_layers)(*[float(x) for x in weights])
+    out = (ctypes.c_int32 * dims.n_layers)()
+    _check(_lib.kvc_plan_budgets_weighted(ctypes.byref(dims), avg_budget, w, out),
+           "kvc_plan_budgets_weighted")
     return list(out)
 
 
@@ -247,6 +261,13 @@ def kvc_scores_layer(cache: Cache, scores=None, pooled=None, stream=None):
            "kvc_scores_layer")
 
 
+def kvc_score_variance(cache: Cache, var_out, stream=None):
+    """Per-(sequence, kv head) variance of the last scored layer's selection
+    scores into var_out (device fp32 [B][H])."""
+    _check(_lib.kvc_score_variance(cache.handle, _ptr(var_out), _stream(stream)),
+           "kvc_score_variance")
+
+
 def kvc_cache_reset(cache: Cache):
     _check(_lib.kvc_cache_reset(cache.handle), "kvc_cache_reset")
 
@@ -277,5 +298,6 @@ __all__ = ["KvcDims", "KvcError", "Cache", "make_dims", "dims_from_spec", "kvc_p
            "kvc_append",
            "kvc_append_layers", "kvc_decode_attn", "kvc_decode_step", "kvc_free",
            "kvc_layer_info_get", "kvc_export_layer", "kvc_scores_layer", "kvc_cache_reset",
+           "kvc_plan_budgets_weighted", "kvc_score_variance",
            "kvc_launch_count", "kvc_check_device", "kvc_select_noalloc", "LIB_PATH",
            "exported_symbols"]

@@ -3,6 +3,7 @@
 // orchestration of the device kernels. No device arithmetic happens here.
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <new>
 
@@ -309,6 +310,47 @@ kvc_status kvc_plan_budgets(const kvc_dims* dims, kvc_schedule schedule, int32_t
   return KVC_OK;
 }
 
+kvc_status kvc_plan_budgets_weighted(const kvc_dims* dims, int32_t avg_budget,
+                                     const double* weights, int32_t* budgets_out) {
+  kvc_status st = check_dims(dims);
+  if (st != KVC_OK) return st;
+  if (!weights || !budgets_out) return KVC_E_ARG;
+  const int L = dims->n_layers, G = dims->group_size;
+  if (avg_budget <= 0 || avg_budget % G) return KVC_E_ARG;
+  double wmax = 0.0;
+  for (int l = 0; l < L; ++l) {
+    if (!std::isfinite(weights[l]) || !(weights[l] > 0.0)) return KVC_E_ARG;
+    wmax = std::max(wmax, weights[l]);
+  }
+  // integer weights q_l = max(1, rint(w_l / max(w) * 2^30)), round half to even
+  std::vector<long long> q(L);
+  unsigned __int128 qsum = 0;
+  for (int l = 0; l < L; ++l) {
+    q[l] = std::max(1LL, (long long)std::nearbyint((weights[l] / wmax) * 1073741824.0));
+    qsum += (unsigned __int128)q[l];
+  }
+  // one group per layer, the spare groups shared by largest remainder (ties to
+  // the lower layer)
+  const long long total = (long long)L * (avg_budget / G), spare = total - L;
+  std::vector<long long> units(L);
+  std::vector<unsigned __int128> rem(L);
+  long long used = 0;
+  for (int l = 0; l < L; ++l) {
+    const unsigned __int128 num = (unsigned __int128)spare * (unsigned __int128)q[l];
+    units[l] = 1 + (long long)(num / qsum);
+    rem[l] = num % qsum;
+    used += units[l];
+  }
+  std::vector<int> order(L);
+  for (int l = 0; l < L; ++l) order[l] = l;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return rem[a] > rem[b]; });
+  for (long long i = 0; i < total - used && i < L; ++i) units[order[i]] += 1;
+  const int ns = dims->prompt_len - dims->obs_window;
+  for (int l = 0; l < L; ++l)
+    budgets_out[l] = (int32_t)std::min<long long>(units[l] * G, (long long)ns);
+  return KVC_OK;
+}
+
 kvc_status kvc_cache_create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** cache) {
   if (!cache) return KVC_E_ARG;
   *cache = nullptr;
@@ -536,6 +578,17 @@ kvc_status kvc_export_layer(kvc_cache* c, int32_t layer, const kvc_export* dst, 
   DeviceGuard dg(c->device);
   if (!dg.ok) return KVC_E_CUDA;
   return from_cuda(kvc::launch_export(c, layer, dst, static_cast<cudaStream_t>(stream)));
+}
+
+kvc_status kvc_score_variance(kvc_cache* c, float* var_out, void* stream) {
+  if (!c || !var_out) return KVC_E_ARG;
+  if (c->last_scored_layer < 0 || !c->scores) return KVC_E_STATE;
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  const kvc_dims& d = c->dims;
+  return from_cuda(kvc::launch_score_variance(c->scores, d.batch * d.n_kv_heads,
+                                              d.prompt_len - d.obs_window, var_out,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 kvc_status kvc_scores_layer(kvc_cache* c, float* scores, float* pooled, void* stream) {

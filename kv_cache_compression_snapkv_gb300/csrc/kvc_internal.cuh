@@ -259,6 +259,9 @@ cudaError_t launch_score_tc(const kvc_dims& d, const __nv_bfloat16* q_obs,
 cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
                               const __nv_bfloat16* k, float2* stats, unsigned* gsync,
                               float* scores, cudaStream_t stream);
+// Population variance of each of `units` rows of m scores (fp32 out, one per row).
+cudaError_t launch_score_variance(const float* scores, int units, int m, float* var,
+                                  cudaStream_t stream);
 cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float* pooled,
                                   int32_t* kept_out, int k_sel, cudaStream_t stream);
 

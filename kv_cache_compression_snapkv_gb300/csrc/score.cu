@@ -1,5 +1,5 @@
 // score.cu -- entry points of the scoring launch (score_tc.cu): the cache's own
-// scratch, or scratch given explicitly.
+// scratch, or scratch given explicitly; and the variance of a layer's scores.
 //
 // PyramidKV: Dynamic KV Cache Compression based on Pyramidal Information
 // Funneling, §4.2.2 "KV Cache Selection"; MiniKV §2 eq. (1).
@@ -19,6 +19,52 @@ cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
                               const __nv_bfloat16* k, float2* stats, unsigned* gsync,
                               float* scores, cudaStream_t stream) {
   return launch_score_tc(d, q_obs, k, stats, gsync, scores, nullptr, stream);
+}
+
+namespace {
+
+// Sum of v over the block, identical in every thread (each thread adds the
+// per-warp partial sums in the same order). Callable repeatedly: the first
+// barrier keeps a previous call's readers ahead of this call's writers.
+__device__ double block_sum(double v, double* red) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  double t = 0.0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+  return t;
+}
+
+// MiniKV §4.2 "Layer-Specific Selectivity" (the variance policy) and Figure 7:
+// the variance score of cumulated attention. One CTA per (sequence, kv head):
+// population variance of its m selection scores, two passes (mean, then squared
+// deviations) accumulated in fp64.
+constexpr int kVarThreads = 256;
+__global__ void __launch_bounds__(kVarThreads) score_variance_kernel(
+    const float* __restrict__ scores, int m, float* __restrict__ var) {
+  __shared__ double red[kVarThreads / 32];
+  const float* row = scores + (size_t)blockIdx.x * m;
+  double acc = 0.0;
+  for (int i = threadIdx.x; i < m; i += kVarThreads) acc += (double)row[i];
+  const double mean = block_sum(acc, red) / m;
+  double acc2 = 0.0;
+  for (int i = threadIdx.x; i < m; i += kVarThreads) {
+    const double dv = (double)row[i] - mean;
+    acc2 += dv * dv;
+  }
+  const double v = block_sum(acc2, red) / m;
+  if (threadIdx.x == 0) var[blockIdx.x] = (float)v;
+}
+
+}  // namespace
+
+cudaError_t launch_score_variance(const float* scores, int units, int m, float* var,
+                                  cudaStream_t stream) {
+  if (units <= 0 || m <= 0) return cudaSuccess;
+  score_variance_kernel<<<units, kVarThreads, 0, stream>>>(scores, m, var);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 }  // namespace kvc

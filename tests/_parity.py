@@ -92,18 +92,20 @@ def decode_error(o_gpu, o_ora):
 
 
 def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=True,
-              dev="cuda"):
+              dev="cuda", budgets=None):
     """Full comparison on a workload the oracle finishes in seconds.
 
     selection: "score" (GPU scores and selects; the oracle does the same),
                "oracle" (the GPU is given the oracle's kept positions) or
                ("sinks", s) (both keep s attention sinks + the most recent tokens).
+    budgets: per-layer budgets to use instead of the spec's schedule.
     """
     K = kvc()
     rep = Report()
     layers = list(range(spec.n_layers)) if layers is None else layers
     dims = K.dims_from_spec(spec, max_new_tokens=steps)
-    budgets = K.kvc_plan_budgets(dims, spec.schedule, spec.avg_budget, spec.pyramid_depth)
+    if budgets is None:
+        budgets = K.kvc_plan_budgets(dims, spec.schedule, spec.avg_budget, spec.pyramid_depth)
     n, a = spec.prompt_len, spec.obs_window
     B, Hk, Hq, D = spec.batch, spec.n_kv_heads, spec.n_q_heads, spec.head_dim
     cache = None

@@ -3,6 +3,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -85,3 +86,39 @@ def test_null_handles(kvc):
     assert lib.kvc_free(None) == 0
     lib.kvc_status_string.restype = ctypes.c_char_p
     assert lib.kvc_status_string(6) == b"capacity exceeded"
+
+
+@pytest.mark.parametrize("L,avg,n,alpha,seed,sigma", [
+    (32, 512, 32768, 32, 0, 1.0), (32, 1024, 131072, 64, 1, 0.5), (7, 96, 500, 16, 2, 2.0),
+    (40, 128, 32768, 32, 3, 1.0), (5, 512, 300, 16, 4, 1.0), (1, 64, 1000, 8, 5, 1.0),
+    (32, 512, 32768, 32, 6, 8.0)])
+def test_weighted_planner_matches_oracle(kvc, L, avg, n, alpha, seed, sigma):
+    """Var-prop / Var-inv budgets: the C planner equals the oracle's on the same
+    doubles (exact integers), including weights spanning many decades."""
+    from oracle import plan_budgets_weighted, variance_weights
+    dims = kvc.make_dims(L, 1, 8, 8, 128, n, alpha, 7, 2, 32, 128, 16)
+    var = list(np.random.default_rng(seed).lognormal(0.0, sigma, L))
+    for policy in ("var-prop", "var-inv"):
+        w = variance_weights(var, policy)
+        assert kvc.kvc_plan_budgets_weighted(dims, avg, w) == \
+            plan_budgets_weighted(L, avg, w, 32, max_budget=n - alpha)
+
+
+def test_weighted_planner_rounding_ties(kvc):
+    """Weights whose scaled values land on exact halves and equal remainders."""
+    from oracle import plan_budgets_weighted
+    dims = kvc.make_dims(4, 1, 8, 8, 128, 100000, 32, 7, 2, 32, 128, 16)
+    for w in ([1.0, 1.0, 1.0, 1.0], [3.0, 1.0, 1.0, 1.0], [1.0, 2.0 ** -31, 2.0 ** -31, 1.0],
+              [1.0, 1.5 * 2.0 ** -30, 2.5 * 2.0 ** -30, 0.75]):
+        for avg in (32, 64, 96, 1024):
+            assert kvc.kvc_plan_budgets_weighted(dims, avg, w) == \
+                plan_budgets_weighted(4, avg, w, 32, max_budget=100000 - 32), (w, avg)
+
+
+def test_weighted_planner_rejects(kvc):
+    dims = kvc.make_dims(3, 1, 8, 8, 128, 1000, 16, 7, 2, 32, 128, 16)
+    for w, avg in (([1.0, 0.0, 1.0], 64), ([1.0, float("nan"), 1.0], 64),
+                   ([1.0, -1.0, 1.0], 64), ([1.0, 1.0, 1.0], 48)):
+        with pytest.raises(kvc.KvcError) as e:
+            kvc.kvc_plan_budgets_weighted(dims, avg, w)
+        assert e.value.status == 1
