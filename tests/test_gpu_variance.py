@@ -68,10 +68,12 @@ def test_variance_budgets_end_to_end(policy):
     layer_var = [float(v.mean()) for v, _, _ in prof]
     w = variance_weights(layer_var, policy)
     dims = K.dims_from_spec(SPEC, max_new_tokens=30)
-    budgets = K.kvc_plan_budgets_weighted(dims, SPEC.avg_budget, w)
+    avg = 320          # 10 groups a layer: enough spare groups for the shares to differ
+    budgets = K.kvc_plan_budgets_weighted(dims, avg, w)
     ns = SPEC.prompt_len - SPEC.obs_window
-    assert budgets == plan_budgets_weighted(SPEC.n_layers, SPEC.avg_budget, w,
-                                            SPEC.group_size, max_budget=ns)
+    assert budgets == plan_budgets_weighted(SPEC.n_layers, avg, w, SPEC.group_size,
+                                            max_budget=ns)
+    assert sum(budgets) == SPEC.n_layers * avg and len(set(budgets)) > 1
     print(policy, "layer variances", [f"{v:.3g}" for v in layer_var], "budgets", budgets)
     rep = run_small(SPEC, 30, selection="score", budgets=budgets)
     assert rep.decode_checked > 0 and rep.decode_err <= DECODE_RTOL
