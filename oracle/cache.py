@@ -37,6 +37,7 @@ from typing import List, Optional
 import numpy as np
 
 from .quant import quantize_keys, quantize_values, dequantize_keys, dequantize_values
+from .acumul import acumul_select
 from .snapkv import snapkv_select
 
 
@@ -101,12 +102,15 @@ class OracleCache:
     # ------------------------------------------------------------------ prefill
     def prefill(self, k: np.ndarray, v: np.ndarray, obs_window: int,
                 budget: Optional[int] = None, q_obs: Optional[np.ndarray] = None,
-                pool_kernel: int = 7, kept: Optional[List[List[np.ndarray]]] = None):
+                pool_kernel: int = 7, kept: Optional[List[List[np.ndarray]]] = None,
+                q_full: Optional[np.ndarray] = None):
         """Select, quantize and place the prompt.
 
         k, v: [B][Hkv][n][d] (exact bf16 values). q_obs: [B][Hq][alpha][d].
         Selection: `kept` if given (ascending indices in [0, n - alpha) per (b, h)),
-        else the observation-window top-`budget` when budget < n - alpha, else all.
+        else the top-`budget` when budget < n - alpha -- of the full-prompt
+        cumulated attention when `q_full` ([B][Hq][n][d], every prompt query) is
+        given, else of the observation-window score -- else all.
         """
         B, Hk, n, d = k.shape
         a = obs_window
@@ -118,6 +122,11 @@ class OracleCache:
             for h in range(Hk):
                 if kept is not None:
                     idx = np.asarray(kept[b][h], dtype=np.int64)
+                elif budget is not None and budget < n - a and q_full is not None:
+                    qg = q_full[b, h * self.gqa:(h + 1) * self.gqa].astype(np.float64)
+                    idx, s, p = acumul_select(qg, k[b, h].astype(np.float64), budget, a,
+                                              pool_kernel)
+                    self.scores[b][h], self.pooled[b][h] = s, p
                 elif budget is not None and budget < n - a:
                     if q_obs is None:
                         raise ValueError("scoring needs the observation queries")

@@ -1,0 +1,135 @@
+"""Pins the oracle's full-prompt cumulated attention (MiniKV §4.3 "selective
+flash-attention", Figure 9: column sums of the un-normalised FlashAttention
+tiles, key blocks visited in order with a running row maximum)."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle.acumul import acumul_scores, acumul_select
+
+
+def _hand_case():
+    """d = 1, every query 1, keys 0, ln 2, ln 4: S_ij = k_j (scale 1/sqrt(1))."""
+    q = np.ones((1, 3, 1))
+    k = np.array([[0.0], [math.log(2.0)], [math.log(4.0)]])
+    return q, k
+
+
+@pytest.mark.parametrize("key_block,want", [
+    # one key per block: each new key is the row's running maximum, so every
+    # visible entry is exp(0) = 1 and A[j] counts the rows i >= j
+    (1, [3.0, 2.0, 1.0]),
+    # blocks {0, 1}, {2}: row 0 -> A0 += 1; row 1 (max ln2) -> A0 += 1/2, A1 += 1;
+    # row 2: first block (max ln2) -> A0 += 1/2, A1 += 1, then key 2 alone -> A2 += 1
+    (2, [2.0, 2.0, 1.0]),
+    # one block: each row uses its full maximum (row 1: ln2, row 2: ln4)
+    # A0 = 1 + 1/2 + 1/4, A1 = 1 + 1/2, A2 = 1
+    (3, [1.75, 1.5, 1.0]),
+    (128, [1.75, 1.5, 1.0]),
+])
+def test_hand_computed_example(key_block, want):
+    q, k = _hand_case()
+    np.testing.assert_allclose(acumul_scores(q, k, key_block), want, rtol=1e-15, atol=0)
+
+
+@pytest.mark.parametrize("n,g,block", [(1, 1, 128), (200, 1, 128), (300, 3, 64), (129, 2, 128),
+                                       (77, 4, 1)])
+def test_identical_keys_count_rows(n, g, block):
+    """All logits of a row equal: every visible entry is 1, so A[j] = g (n - j)
+    whatever the blocking."""
+    rng = np.random.default_rng(n)
+    q = rng.standard_normal((g, n, 16))
+    k = np.tile(rng.standard_normal(16), (n, 1))
+    np.testing.assert_allclose(acumul_scores(q, k, block), g * (n - np.arange(n)), rtol=1e-13)
+
+
+def test_dominant_first_key_makes_blocking_irrelevant():
+    """Key 0 carries every row's maximum: the running maximum is final from the
+    first block on, so every block size gives the same A_cumul."""
+    rng = np.random.default_rng(5)
+    n, d, g = 400, 32, 2
+    q = rng.standard_normal((g, n, d))
+    k = rng.standard_normal((n, d))
+    k[0] = 0.0
+    q[:, :, 0] = 1.0
+    k[0, 0] = 40.0          # logit 40 / sqrt(32) ~ 7 above every other
+    k[1:, 0] = 0.0
+    ref = acumul_scores(q, k, n)
+    for block in (1, 7, 64, 128):
+        np.testing.assert_allclose(acumul_scores(q, k, block), ref, rtol=1e-12)
+
+
+def test_blocked_at_least_unblocked_and_bounded():
+    """A running maximum never exceeds the final one, so each blocked entry is at
+    least the unblocked one; every entry is at most 1, so A[j] <= g (n - j)."""
+    rng = np.random.default_rng(7)
+    n, d, g = 513, 64, 2
+    q = rng.standard_normal((g, n, d)) * 2.0
+    k = rng.standard_normal((n, d))
+    full = acumul_scores(q, k, n)
+    blk = acumul_scores(q, k, 128)
+    assert np.all(blk >= full * (1 - 1e-12))
+    assert np.any(blk > full * (1 + 1e-6))          # the blocking does matter here
+    assert np.all(blk <= g * (n - np.arange(n)) * (1 + 1e-12))
+
+
+def test_last_column_and_first_block_of_a_row():
+    """Only the last row sees the last key, with its full row maximum:
+    A[n-1] = sum_h exp(S_{n-1,n-1} - max_j S_{n-1,j})."""
+    rng = np.random.default_rng(9)
+    n, d, g = 300, 16, 3
+    q = rng.standard_normal((g, n, d))
+    k = rng.standard_normal((n, d))
+    want = 0.0
+    for h in range(g):
+        s = k @ q[h, n - 1] / math.sqrt(d)
+        want += math.exp(s[n - 1] - s.max())
+    assert acumul_scores(q, k, 128)[n - 1] == pytest.approx(want, rel=1e-13)
+
+
+def test_gqa_heads_add_and_prefix_monotone():
+    rng = np.random.default_rng(11)
+    n, d = 260, 32
+    q = rng.standard_normal((2, n, d))
+    k = rng.standard_normal((n, d))
+    both = acumul_scores(q, k)
+    np.testing.assert_allclose(both, acumul_scores(q[:1], k) + acumul_scores(q[1:], k),
+                               rtol=1e-13)
+    # a longer prompt only adds rows: A over the first 200 positions can only grow
+    short = acumul_scores(q[:, :200], k[:200])
+    assert np.all(both[:200] >= short * (1 - 1e-13))
+
+
+def test_selection_keeps_planted_heavy_hitters():
+    """Queries share a direction u (as the synthetic workloads' queries do); keys
+    planted along u draw every later row's attention and must be kept."""
+    rng = np.random.default_rng(13)
+    n, d, g, alpha = 600, 32, 2, 16
+    u = rng.standard_normal(d)
+    u /= np.linalg.norm(u)
+    q = rng.standard_normal((g, n, d)) + 2.0 * u
+    k = rng.standard_normal((n, d)) * 0.3
+    hitters = [5, 123, 321, 480]
+    k[hitters] = 6.0 * u
+    idx, s, p = acumul_select(q, k, 32, alpha)
+    assert len(s) == n - alpha and np.array_equal(s, p)    # width 1: no pooling
+    assert len(idx) == 32 and np.all(np.diff(idx) > 0)
+    assert set(hitters) <= set(idx.tolist())
+
+
+def test_cache_prefill_with_full_prompt_queries():
+    """OracleCache keeps, per (sequence, kv head), the A_cumul heavy hitters when
+    given every prompt query, and places them as for any selection."""
+    from oracle import OracleCache
+    rng = np.random.default_rng(17)
+    B, Hq, Hk, n, d, alpha = 1, 4, 2, 300, 32, 16
+    q = rng.standard_normal((B, Hq, n, d))
+    k = rng.standard_normal((B, Hk, n, d))
+    v = rng.standard_normal((B, Hk, n, d))
+    oc = OracleCache(B, Hq, Hk, d, 2, 32, 64)
+    oc.prefill(k, v, alpha, budget=64, q_full=q, pool_kernel=1)
+    for h in range(Hk):
+        want, _, _ = acumul_select(q[0, 2 * h:2 * h + 2], k[0, h], 64, alpha)
+        np.testing.assert_array_equal(oc.heads[0][h].kept, want)
+        assert oc.n_packed() == 64 and len(oc.heads[0][h].win_k) == alpha
