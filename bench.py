@@ -47,6 +47,8 @@ def parse():
                     help="skip the compression pass with the sink + recent selection")
     ap.add_argument("--no-exact16", action="store_true",
                     help="skip the decode launches over a 16-bit (unquantized) cache")
+    ap.add_argument("--no-acumul", action="store_true",
+                    help="skip the compression pass scored by the full-prompt cumulated attention")
     return ap.parse_args()
 
 
@@ -361,6 +363,34 @@ def run_gpu(args):
                 sms.append(cs0.elapsed_time(cs1))
         sink_ms = statistics.mean(sms) / L
 
+    # selection by the full-prompt cumulated attention (every prompt query, un-normalised
+    # column sums): the first two layers compressed with it, outside the timed steps
+    acumul = None
+    if not args.no_acumul:
+        LA = min(2, L)
+        qfull = [synth.prompt_queries(spec, l, device=dev) for l in range(LA)]
+        ca0, ca1 = ev(), ev()
+        ams = []
+        for i in range(4):
+            K.kvc_cache_reset(cache)
+            ca0.record(stream)
+            for l in range(LA):
+                x = prompt[l]
+                K.kvc_prefill_acumul(cache, l, qfull[l], x["k"], x["v"])
+            ca1.record(stream)
+            torch.cuda.synchronize()
+            if i > 0:
+                ams.append(ca0.elapsed_time(ca1))
+        a_ms = statistics.mean(ams) / LA
+        # the method's flops: q.k over every causal (query, key) pair of every query head
+        a_flops = 2 * D * B * Hq * spec.prompt_len * (spec.prompt_len + 1) // 2
+        acumul = {"ms_per_layer": a_ms, "flops": a_flops, "layers": LA,
+                  "tflops": a_flops / (a_ms / 1e3) / 1e12,
+                  "note": "selection by MiniKV's full-prompt cumulated attention (key blocks of "
+                          "128, running row maxima); two MMAs per tile (S and S^T) on the "
+                          "tensor cores"}
+        del qfull
+
     # 16-bit storage (every kept token exact in the bf16 window), same selection and
     # budgets: decode launches over the exact cache, outside the timed steps
     exact16 = None
@@ -455,6 +485,8 @@ def run_gpu(args):
         "compress_ms_per_layer": comp_ms / L,
         "decode_16bit": None if exact16 is None else dict(
             exact16, frac=exact16["gbs"] / hbm),
+        "compress_acumul": None if acumul is None else dict(
+            acumul, frac=acumul["tflops"] / tc),
         "compress_sinks": None if sink_ms is None else {
             "ms_per_layer": sink_ms, "bytes": sink_bytes,
             "frac": sink_bytes / (hbm * 1e9) / (sink_ms * L / 1e3),

@@ -164,6 +164,31 @@ kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets,
                                 const void* v, kvc_cache** cache, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * kvc_prefill_acumul -- like kvc_prefill_compress with MiniKV's full-prompt
+ *   cumulated attention as the selection score (MiniKV §4.3 "selective
+ *   flash-attention", Figure 9; Algorithm 1, prefill). Per (sequence, kv head),
+ *   every prompt query of each of the g query heads sharing the kv head attends
+ *   causally to the prompt keys; keys are visited in blocks of 128 from the
+ *   first on, each row keeps a running maximum m over the blocks seen so far,
+ *   and exp(q.k/sqrt(d) - m) is added into the key's score -- rows are never
+ *   normalised. Scores of positions [0, n - alpha) then go through the same
+ *   max-pool (width pool_kernel; 1 leaves them unchanged) and per-head top-k as
+ *   kvc_prefill_compress, and the kept tokens are stored the same way.
+ *   The cache must exist (kvc_cache_create or an earlier prefill call).
+ *   q_full: device bf16 [batch][n_q_heads][prompt_len][head_dim], every prompt
+ *           query (may be NULL when the layer's budget keeps every token).
+ *   k, v:   device bf16 [batch][n_kv_heads][prompt_len][head_dim].
+ *   Needs 128 % (n_q_heads / n_kv_heads) == 0 and n_q_heads / n_kv_heads <= 16.
+ *   The scores stay readable through kvc_scores_layer / kvc_score_variance until
+ *   the next scoring call. Atomic additions make the scores' last bits depend on
+ *   timing.
+ *   Errors: KVC_E_ARG, KVC_E_SHAPE (group size, or initial window not shorter
+ *   than R), KVC_E_STATE (layer already compressed), KVC_E_CUDA.
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_prefill_acumul(kvc_cache* cache, int32_t layer, const void* q_full, const void* k,
+                              const void* v, void* stream);
+
+/* ---------------------------------------------------------------------------
  * kvc_prefill_sinks -- like kvc_prefill_compress with the attention-sink +
  *   recent-token selection in place of the scored one (blog "KV Cache
  *   Compression: Eviction and Quantization", "Measured on a real model": the first

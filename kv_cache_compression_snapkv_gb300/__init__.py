@@ -65,6 +65,7 @@ _SIGS = {
                              ctypes.POINTER(ctypes.c_void_p), _P],
     "kvc_prefill_selected": [_P, _I, _P, _I, _P, _P, _P],
     "kvc_prefill_sinks": [_P, _I, _I, _P, _P, _P],
+    "kvc_prefill_acumul": [_P, _I, _P, _P, _P, _P],
     "kvc_cache_create": [ctypes.POINTER(KvcDims), _P, ctypes.POINTER(ctypes.c_void_p)],
     "kvc_append": [_P, _I, _P, _P, _P],
     "kvc_append_layers": [_P, _I, _I, _P, _P, _P],
@@ -198,6 +199,13 @@ def kvc_prefill_sinks(cache: Cache, layer: int, n_sinks: int, k, v, stream=None)
                                   _stream(stream)), "kvc_prefill_sinks")
 
 
+def kvc_prefill_acumul(cache: Cache, layer: int, q_full, k, v, stream=None):
+    """Selection of `layer` by MiniKV's full-prompt cumulated attention (every
+    prompt query, un-normalised column sums), then packing."""
+    _check(_lib.kvc_prefill_acumul(cache.handle, layer, _ptr(q_full), _ptr(k), _ptr(v),
+                                   _stream(stream)), "kvc_prefill_acumul")
+
+
 def kvc_append(cache: Cache, layer: int, k_new, v_new, stream=None):
     _check(_lib.kvc_append(cache.handle, layer, _ptr(k_new), _ptr(v_new), _stream(stream)),
            "kvc_append")
@@ -298,6 +306,6 @@ __all__ = ["KvcDims", "KvcError", "Cache", "make_dims", "dims_from_spec", "kvc_p
            "kvc_append",
            "kvc_append_layers", "kvc_decode_attn", "kvc_decode_step", "kvc_free",
            "kvc_layer_info_get", "kvc_export_layer", "kvc_scores_layer", "kvc_cache_reset",
-           "kvc_plan_budgets_weighted", "kvc_score_variance",
+           "kvc_plan_budgets_weighted", "kvc_score_variance", "kvc_prefill_acumul",
            "kvc_launch_count", "kvc_check_device", "kvc_select_noalloc", "LIB_PATH",
            "exported_symbols"]

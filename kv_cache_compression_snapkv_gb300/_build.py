@@ -21,7 +21,8 @@ LIB = os.path.join(PKG, "libkvc.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["api.cu", "score.cu", "score_tc.cu", "topk.cu", "quant.cu", "decode.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "score.cu", "score_tc.cu", "acumul_tc.cu", "topk.cu", "quant.cu", "decode.cu",
+           "noalloc.cu"]
 
 
 def nvcc() -> str:

@@ -1,0 +1,422 @@
+// acumul_tc.cu -- full-prompt cumulated attention (MiniKV's A_cumul) on the
+// 5th-generation tensor cores, one persistent launch per layer.
+//
+// MiniKV: Pushing the Limits of LLM Inference via 2-Bit Layer-Discriminative KV
+// Cache, §4.3 "selective flash-attention" and Figure 9; Algorithm 1 (prefill: the
+// heavy hitters are chosen from A_cumul). Every prompt query attends causally to
+// the prompt keys; the keys are visited in blocks of 128 from the first on, each
+// visit raises every row's running maximum to the block's, and the tile
+// P = exp(S - running maximum) is added column by column into A_cumul. Rows are
+// never normalised. The g query heads sharing a kv head add into one score per
+// kv head; only the columns [0, n - alpha) are kept (the observation window
+// stays whole), so key blocks past them are not visited.
+//
+// Work: an item is (unit = (sequence, kv head), row block) with a row block of
+// P = 128 / g consecutive prompt positions for each of the g query heads (128
+// rows, head-major). Items are dealt to the CTAs longest first in snake order.
+// Per item the query tile stays in shared memory while its key tiles 0..T-1
+// stream through a ring of stages; for every key tile the MMA thread issues
+//   D1[row][key] = Q . K^T   (the running row maxima), and
+//   D2[key][row] = K . Q^T   (the column sums, one key per thread),
+// each 128 x 128 in tensor memory, double-buffered over tiles (512 columns).
+// Eight epilogue warps take each tile in two column halves: the row maxima of
+// D1 are merged in shared memory into the running maxima, then each thread sums
+// exp2(D2 * log2(e)/sqrt(d) - m_row) over its half of the rows for its key; the
+// halves meet in shared memory and one atomic add per key lands the item's
+// contribution in the score row (zeroed before the launch).
+//
+// Roles: warp 0 TMA producer, warp 1 tensor-memory owner and MMA issuer, warps
+// 2..9 epilogue. Every wait is bounded; a wait that gives up sets a bit of the
+// error word and the CTA winds down without further waits.
+#include <algorithm>
+#include <cudaTypedefs.h>
+
+#include "kvc_internal.cuh"
+#include "tc_common.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int kAcEpiWarps = 8;
+constexpr int kAcThreads = 64 + 32 * kAcEpiWarps;   // producer, MMA, epilogue warps
+constexpr int kAcTmemCols = 512;
+constexpr int kAcSmemLimit = 232448;                // opt-in shared memory per CTA
+
+enum : unsigned { kErrAcProducer = 128u, kErrAcMma = 256u, kErrAcEpilogue = 512u };
+
+template <int D>
+struct AcCfg {
+  static constexpr int KB = D / 64;                 // 64-element K blocks
+  static constexpr int TBYTES = 128 * D * 2;        // one 128-row bf16 tile
+  static constexpr int QBUF = 2;
+  static constexpr int FIT = (kAcSmemLimit - QBUF * TBYTES - 8192) / TBYTES;
+  static constexpr int STAGES = FIT > 6 ? 6 : FIT;
+  static constexpr int oQ = 0;
+  static constexpr int oK = QBUF * TBYTES;
+  static constexpr int oBar = oK + STAGES * TBYTES;
+  // full[S], empty[S], qfull[QBUF], qempty[QBUF], tfull[2], tempty[2], drain
+  static constexpr int NBAR = 2 * STAGES + 2 * QBUF + 2 * 2 + 1;
+  static constexpr int oTmem = oBar + NBAR * 8;
+  static constexpr int oMax = (oTmem + 16 + 15) / 16 * 16;   // [2 halves][128] row maxima
+  static constexpr int oNegM = oMax + 2 * 128 * 4;           // [2 tiles][128] -m per row
+  static constexpr int oPart = oNegM + 2 * 128 * 4;          // [2 tiles][128] half sums
+  static constexpr int total = oPart + 2 * 128 * 4 + 1024;   // + alignment slack
+  static_assert(STAGES >= 2, "at least two key stages");
+  static_assert(total <= kAcSmemLimit, "fits the shared memory of one CTA");
+  static_assert(TBYTES % 1024 == 0, "1024-byte aligned tiles");
+};
+
+struct AcArgs {
+  int n;           // prompt length
+  int ns;          // scored keys (n - alpha)
+  int g;           // query heads per kv head
+  int P;           // positions per row block (128 / g)
+  int Hq, Hk;
+  int units;       // batch * Hk
+  int rblocks;     // row blocks per unit
+  long long items; // units * rblocks
+  float sl2;       // log2(e) / sqrt(d)
+  float* scores;   // [unit][ns], zero before the launch
+  unsigned* err;
+};
+
+// The j-th item of CTA c (of G): items are dealt in snake order, c, 2G-1-c,
+// 2G+c, 4G-1-c, ...; the sequence is increasing, so the first index past the end
+// ends the CTA's list.
+__device__ __forceinline__ long long item_at(int c, int j, int G) {
+  const long long base = (long long)(j >> 1) * 2 * G;
+  return base + ((j & 1) ? (2 * G - 1 - c) : c);
+}
+
+struct Item {
+  int unit, p0, T;
+};
+// Item i: longest first (the last row blocks), units interleaved. T = key tiles
+// visited: through the row block's last position, at most through the last
+// scored key.
+__device__ __forceinline__ Item item_of(long long i, const AcArgs& a) {
+  Item it;
+  it.unit = (int)(i % a.units);
+  const int rb = a.rblocks - 1 - (int)(i / a.units);
+  it.p0 = rb * a.P;
+  const int last = min(it.p0 + a.P, a.n) - 1;
+  it.T = min(last, a.ns - 1) / 128 + 1;
+  return it;
+}
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAcThreads, 1)
+acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                 const AcArgs a) {
+  using C = AcCfg<D>;
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
+                                            ~uintptr_t(1023));
+  uint8_t* sQ = dsm + C::oQ;
+  uint8_t* sK = dsm + C::oK;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + C::oBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* qfull = bars + 2 * C::STAGES;
+  uint64_t* qempty = qfull + C::QBUF;
+  uint64_t* tfull = qempty + C::QBUF;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(dsm + C::oTmem);
+  float* smax = reinterpret_cast<float*>(dsm + C::oMax);
+  float* snegm = reinterpret_cast<float*>(dsm + C::oNegM);
+  float* spart = reinterpret_cast<float*>(dsm + C::oPart);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) { tc::mbar_init(&full[s], 1); tc::mbar_init(&empty[s], 1); }
+    for (int q = 0; q < C::QBUF; ++q) { tc::mbar_init(&qfull[q], 1); tc::mbar_init(&qempty[q], 1); }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&tfull[b], 1);
+      tc::mbar_init(&tempty[b], kAcEpiWarps);
+    }
+    tc::mbar_init(drain, 1);
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&tmK);
+    tc::tma_prefetch_desc(&tmQ);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_holder, kAcTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tmem_holder;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      int k = 0, nq = 0;
+      for (int j = 0; ok; ++j) {
+        const long long i = item_at(cta, j, G);
+        if (i >= a.items) break;
+        const Item it = item_of(i, a);
+        const int qb = nq % C::QBUF;
+        if (nq >= C::QBUF)
+          ok = tc::mbar_wait(&qempty[qb], (uint32_t)((nq / C::QBUF - 1) & 1), a.err,
+                             kErrAcProducer);
+        if (!ok) break;
+        // the row block: P positions of each of the g query heads, head-major
+        tc::mbar_expect_tx(&qfull[qb], (uint32_t)C::TBYTES);
+        uint8_t* q = sQ + qb * C::TBYTES;
+        const int b = it.unit / a.Hk, hk = it.unit % a.Hk;
+        for (int hh = 0; hh < a.g; ++hh) {
+          const int row = ((b * a.Hq + hk * a.g + hh) * a.n) + it.p0;
+          for (int kb = 0; kb < C::KB; ++kb)
+            tc::tma_load_2d(q + kb * 128 * 128 + hh * a.P * 128, &tmQ, kb * 64, row, &qfull[qb]);
+        }
+        ++nq;
+        for (int t = 0; t < it.T && ok; ++t, ++k) {
+          const int s = k % C::STAGES, round = k / C::STAGES;
+          if (round > 0)
+            ok = tc::mbar_wait(&empty[s], (uint32_t)((round - 1) & 1), a.err, kErrAcProducer);
+          if (!ok) break;
+          tc::mbar_expect_tx(&full[s], (uint32_t)C::TBYTES);
+          uint8_t* dst = sK + s * C::TBYTES;
+          for (int kb = 0; kb < C::KB; ++kb)
+            tc::tma_load_2d(dst + kb * 128 * 128, &tmK, kb * 64, it.unit * a.n + t * 128,
+                            &full[s]);
+        }
+      }
+      // every copy issued here has landed before the CTA can leave
+      for (int kk = max(0, k - C::STAGES); kk < k; ++kk)
+        tc::mbar_wait(&full[kk % C::STAGES], (uint32_t)((kk / C::STAGES) & 1), a.err,
+                      kErrAcProducer);
+      for (int q = max(0, nq - C::QBUF); q < nq; ++q)
+        tc::mbar_wait(&qfull[q % C::QBUF], (uint32_t)((q / C::QBUF) & 1), a.err, kErrAcProducer);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 128);
+      int k = 0, nq = 0;
+      for (int j = 0; ok; ++j) {
+        const long long i = item_at(cta, j, G);
+        if (i >= a.items) break;
+        const Item it = item_of(i, a);
+        const int qb = nq % C::QBUF;
+        ok = tc::mbar_wait(&qfull[qb], (uint32_t)((nq / C::QBUF) & 1), a.err, kErrAcMma);
+        if (!ok) break;
+        ++nq;
+        for (int t = 0; t < it.T && ok; ++t, ++k) {
+          const int s = k % C::STAGES;
+          ok = tc::mbar_wait(&full[s], (uint32_t)((k / C::STAGES) & 1), a.err, kErrAcMma);
+          if (!ok) break;
+          const int bb = k & 1, rb = k >> 1;
+          if (rb > 0) ok = tc::mbar_wait(&tempty[bb], (uint32_t)((rb - 1) & 1), a.err, kErrAcMma);
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint32_t sQa = tc::saddr(sQ + qb * C::TBYTES);
+          const uint32_t sKa = tc::saddr(sK + s * C::TBYTES);
+          const uint32_t d1 = tbase + (uint32_t)(bb * 256), d2 = d1 + 128u;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int kb = kk / 4, kin = (kk % 4) * 32;
+            const uint64_t qd = tc::sw128_desc(sQa + kb * 128 * 128 + kin);
+            const uint64_t kd = tc::sw128_desc(sKa + kb * 128 * 128 + kin);
+            tc::mma_bf16(d1, qd, kd, idesc, kk > 0 ? 1u : 0u);   // [row][key]
+            tc::mma_bf16(d2, kd, qd, idesc, kk > 0 ? 1u : 0u);   // [key][row]
+          }
+          tc::mma_commit(&empty[s]);
+          tc::mma_commit(&tfull[bb]);
+          if (t + 1 == it.T) tc::mma_commit(&qempty[qb]);
+        }
+      }
+      // every MMA issued here has completed before tensor memory is released
+      tc::mma_commit(drain);
+      tc::mbar_wait(drain, 0u, a.err, kErrAcMma);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;                 // tensor-memory lane quarter
+    const int half = (warp - 2) >> 2;             // column half of each tile
+    const int r = quarter * 32 + lane;            // row of D1 / key of D2 this thread reads
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const int ET = 32 * kAcEpiWarps;
+    int k = 0;
+    for (int j = 0;; ++j) {
+      const long long i = item_at(cta, j, G);
+      if (i >= a.items) break;
+      const Item it = item_of(i, a);
+      const int pos_r = it.p0 + r % a.P;          // prompt position of row r
+      const bool row_ok = pos_r < a.n;
+      float m = -INFINITY;                        // running maximum of row r (log2 units)
+      for (int t = 0; t < it.T; ++t, ++k) {
+        const int bb = k & 1;
+        if (ok) ok = tc::mbar_wait(&tfull[bb], (uint32_t)((k >> 1) & 1), a.err, kErrAcEpilogue);
+        ok = __all_sync(0xffffffffu, ok);
+        tc::fence_after_sync();
+        const int key0 = t * 128;
+        // does some row miss some key of this tile (causal diagonal, or rows past n)?
+        const bool masked = key0 + 127 > it.p0 || it.p0 + a.P > a.n;
+        // --- row maxima: row r, columns [64 half, 64 half + 64) of D1
+        const uint32_t c1 = tbase + lane_addr + (uint32_t)(bb * 256 + half * 64);
+        float pm = -INFINITY;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(c1 + (uint32_t)c0, v);
+          if (masked) {
+            const int lim = row_ok ? pos_r - (key0 + half * 64 + c0) : -1;   // last visible column
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) v[jj] = jj <= lim ? v[jj] : -INFINITY;
+          }
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) pm = fmaxf(pm, v[jj]);
+        }
+        smax[half * 128 + r] = pm;
+        named_bar(1, ET);
+        const float mt = fmaxf(smax[r], smax[128 + r]);
+        if (mt != -INFINITY) m = fmaxf(m, mt * a.sl2);
+        if (half == 0) snegm[bb * 128 + r] = -m;
+        named_bar(1, ET);
+        // --- column sums: key r, rows [64 half, 64 half + 64) of D2
+        const uint32_t c2 = tbase + lane_addr + (uint32_t)(bb * 256 + 128 + half * 64);
+        const float* nm = snegm + bb * 128 + half * 64;
+        const int key = key0 + r;
+        float acc = 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(c2 + (uint32_t)c0, v);
+          if (!masked) {
+            const float4* nm4 = reinterpret_cast<const float4*>(nm + c0);
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 4) {
+              const float4 b4 = nm4[jj / 4];
+              v[jj] = fmaf(v[jj], a.sl2, b4.x);
+              v[jj + 1] = fmaf(v[jj + 1], a.sl2, b4.y);
+              v[jj + 2] = fmaf(v[jj + 2], a.sl2, b4.z);
+              v[jj + 3] = fmaf(v[jj + 3], a.sl2, b4.w);
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const int row = half * 64 + c0 + jj;
+              const int pos = it.p0 + row % a.P;
+              v[jj] = (pos < a.n && key <= pos) ? fmaf(v[jj], a.sl2, nm[c0 + jj]) : -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(v[jj]) : "f"(v[jj]));
+#pragma unroll
+          for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+            for (int jj = 0; jj < w; ++jj) v[jj] += v[jj + w];
+          acc += v[0];
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&tempty[bb]);
+        // the halves meet in shared memory; one atomic add per key
+        float* part = spart + bb * 128;
+        if (half == 1) part[r] = acc;
+        named_bar(1, ET);
+        if (half == 0 && ok && key < a.ns) atomicAdd(a.scores + (size_t)it.unit * a.ns + key,
+                                                    acc + part[r]);
+      }
+    }
+  }
+
+  // teardown: every MMA this CTA issued has completed once the epilogue consumed
+  // its last tile; on an error path the MMA thread drained before this point
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tbase, kAcTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 ac_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 map over [rows][d]: boxes of 64 elements x box_rows rows, 128-byte swizzle.
+cudaError_t ac_make_map(CUtensorMap* m, const void* base, long long rows, int d, int box_rows) {
+  auto fn = ac_encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t run_acumul(const kvc_dims& d, const __nv_bfloat16* q_full, const __nv_bfloat16* k,
+                       float* scores, unsigned* err, cudaStream_t stream) {
+  using C = AcCfg<D>;
+  const int g = d.n_q_heads / d.n_kv_heads;
+  AcArgs a{};
+  a.n = d.prompt_len;
+  a.ns = d.prompt_len - d.obs_window;
+  a.g = g;
+  a.P = 128 / g;
+  a.Hq = d.n_q_heads;
+  a.Hk = d.n_kv_heads;
+  a.units = d.batch * d.n_kv_heads;
+  a.rblocks = (a.n + a.P - 1) / a.P;
+  a.items = (long long)a.units * a.rblocks;
+  a.sl2 = 1.4426950408889634f / sqrtf((float)D);
+  a.scores = scores;
+  a.err = err;
+  cudaError_t e = cudaMemsetAsync(scores, 0, (size_t)a.units * a.ns * 4, stream);
+  if (e != cudaSuccess) return e;
+  CUtensorMap mk, mq;
+  if ((e = ac_make_map(&mk, k, (long long)a.units * a.n, D, 128)) != cudaSuccess) return e;
+  if ((e = ac_make_map(&mq, q_full, (long long)d.batch * a.Hq * a.n, D, a.P)) != cudaSuccess)
+    return e;
+  e = ensure_smem(reinterpret_cast<const void*>(acumul_tc_kernel<D>), C::total);
+  if (e != cudaSuccess) return e;
+  int dev = 0, n_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const int grid = (int)std::min<long long>(n_sm, a.items);
+  acumul_tc_kernel<D><<<grid, kAcThreads, C::total, stream>>>(mk, mq, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_acumul(const kvc_dims& d, const __nv_bfloat16* q_full, const __nv_bfloat16* k,
+                          float* scores, unsigned* err, cudaStream_t stream) {
+  const int g = d.n_q_heads / d.n_kv_heads;
+  if (g < 1 || g > 16 || 128 % g != 0) return cudaErrorInvalidValue;
+  if (d.prompt_len - d.obs_window < 1) return cudaErrorInvalidValue;
+  if (d.head_dim == 128) return run_acumul<128>(d, q_full, k, scores, err, stream);
+  if (d.head_dim == 64) return run_acumul<64>(d, q_full, k, scores, err, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvc

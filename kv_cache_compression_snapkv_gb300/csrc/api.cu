@@ -394,6 +394,35 @@ kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets, in
   return finish_prefill(c, layer, n_kept, kept, k, v, s);
 }
 
+kvc_status kvc_prefill_acumul(kvc_cache* c, int32_t layer, const void* q_full, const void* k,
+                              const void* v, void* stream) {
+  if (!c || !k || !v) return KVC_E_ARG;
+  if (layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
+  LayerState& ls = c->L[layer];
+  if (ls.prefilled) return KVC_E_STATE;
+  const int ns = c->dims.prompt_len - c->dims.obs_window;
+  const int n_kept = ls.budget < ns ? ls.budget : ns;
+  if (!window_fits(c->dims, n_kept)) return KVC_E_SHAPE;
+  const int g = c->dims.n_q_heads / c->dims.n_kv_heads;
+  if (g > 16 || 128 % g != 0) return KVC_E_SHAPE;
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n_kept >= ns) {                 // the budget keeps every token
+    ls.scored = 0;
+    return finish_prefill(c, layer, n_kept, nullptr, k, v, s);
+  }
+  if (!q_full) return KVC_E_ARG;
+  int32_t* kp = ls.kept_ptr;
+  cudaError_t e = kvc::launch_acumul(c->dims, static_cast<const __nv_bfloat16*>(q_full),
+                                     static_cast<const __nv_bfloat16*>(k), c->scores, c->err, s);
+  if (e == cudaSuccess) e = kvc::launch_pool_topk(c, layer, kp, n_kept, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  ls.scored = 1;
+  c->last_scored_layer = layer;
+  return finish_prefill(c, layer, n_kept, kp, k, v, s);
+}
+
 kvc_status kvc_prefill_sinks(kvc_cache* c, int32_t layer, int32_t n_sinks, const void* k,
                              const void* v, void* stream) {
   if (!c || !k || !v || n_sinks < 0) return KVC_E_ARG;

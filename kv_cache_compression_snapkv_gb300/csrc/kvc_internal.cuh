@@ -259,6 +259,11 @@ cudaError_t launch_score_tc(const kvc_dims& d, const __nv_bfloat16* q_obs,
 cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
                               const __nv_bfloat16* k, float2* stats, unsigned* gsync,
                               float* scores, cudaStream_t stream);
+// Full-prompt cumulated attention (un-normalised column sums, key blocks of 128 with
+// running row maxima) of every unit into scores [unit][n - alpha]; q_full is
+// [B][Hq][n][d]. Zeroes the scores first (stream-ordered); err may be NULL.
+cudaError_t launch_acumul(const kvc_dims& d, const __nv_bfloat16* q_full, const __nv_bfloat16* k,
+                          float* scores, unsigned* err, cudaStream_t stream);
 // Population variance of each of `units` rows of m scores (fp32 out, one per row).
 cudaError_t launch_score_variance(const float* scores, int units, int m, float* var,
                                   cudaStream_t stream);

@@ -82,3 +82,28 @@ def acumul_select(q_group: np.ndarray, k: np.ndarray, budget: int, obs_window: i
     s = acumul_scores(q_group, k, key_block)[:n - obs_window]
     p = max_pool(s, pool_kernel)
     return select_topk(p, budget), s, p
+
+
+def acumul_columns(q_group: np.ndarray, k: np.ndarray, cols, key_block: int = KEY_BLOCK):
+    """A_cumul at the given columns only, each straight from its definition:
+    A[j] = sum over rows i >= j of exp(S_ij - m_i), m_i the maximum of row i's
+    logits over keys <= i in the key blocks up to and including j's. Cheap for
+    columns near either end of a long prompt (few rows, or keys of few blocks)."""
+    q_group = np.asarray(q_group, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    g, n, d = q_group.shape
+    scale = 1.0 / math.sqrt(d)
+    out = []
+    for j in cols:
+        j = int(j)
+        end = min((j // key_block + 1) * key_block, n)   # keys of blocks 0..t(j)
+        total = 0.0
+        for h in range(g):
+            rows = q_group[h, j:]                          # rows i >= j
+            s = (rows @ k[:end].T) * scale                 # [i - j][key]
+            i = np.arange(j, n)
+            s = np.where(np.arange(end)[None, :] <= i[:, None], s, -np.inf)
+            m = s.max(axis=1)
+            total += float(np.exp(s[:, j] - m).sum())
+        out.append(total)
+    return np.array(out)

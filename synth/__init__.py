@@ -179,6 +179,23 @@ def layer_inputs(spec: Spec, layer: int, device="cpu", with_q: bool = True) -> d
     return out
 
 
+def prompt_queries(spec: Spec, layer: int, device="cpu") -> torch.Tensor:
+    """Queries of every prompt position, [B][Hq][n][d] bf16: the first n - obs_window
+    drawn like the observation queries (seed stream +700), the last obs_window the
+    layer's q_obs itself."""
+    B, Hq, d, n, a = spec.batch, spec.n_q_heads, spec.head_dim, spec.prompt_len, spec.obs_window
+    g = _gen(_layer_seed(spec, layer) + 700, device)
+    z = torch.randn(B, Hq, n - a, d, generator=g, device=device, dtype=torch.float32)
+    if spec.dist != "toy":
+        _, u = _head_params(spec, layer, device)
+        z += 2.0 * u.repeat_interleave(spec.gqa, dim=0)[None, :, None, :]
+    head = z.to(torch.bfloat16)
+    if a == 0:
+        return head
+    tail = layer_inputs(spec, layer, device=device)["q_obs"]
+    return torch.cat([head, tail], dim=2).contiguous()
+
+
 def decode_inputs(spec: Spec, layer: int, step: int, device="cpu") -> dict:
     """One decode step of one layer: q [B][Hq][d], k_new, v_new [B][Hkv][d] (bf16)."""
     B, Hq, Hk, d = spec.batch, spec.n_q_heads, spec.n_kv_heads, spec.head_dim

@@ -97,7 +97,8 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
 
     selection: "score" (GPU scores and selects; the oracle does the same),
                "oracle" (the GPU is given the oracle's kept positions) or
-               ("sinks", s) (both keep s attention sinks + the most recent tokens).
+               ("sinks", s) (both keep s attention sinks + the most recent tokens) or
+               "acumul" (both score by the full-prompt cumulated attention).
     budgets: per-layer budgets to use instead of the spec's schedule.
     """
     K = kvc()
@@ -123,8 +124,9 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
             sel = sinks_window_select(n - a, bud, sinks)
             oc.prefill(k_np, v_np, a, kept=[[sel] * Hk for _ in range(B)])
         else:
+            qf = synth.prompt_queries(spec, layer, device="cpu") if selection == "acumul" else None
             oc.prefill(k_np, v_np, a, budget=bud if scoring else None, q_obs=q_np,
-                       pool_kernel=spec.pool_kernel)
+                       pool_kernel=spec.pool_kernel, q_full=None if qf is None else np64(qf))
         kd, vd = x["k"].to(dev), x["v"].to(dev)
         qd = x["q_obs"].to(dev) if "q_obs" in x else None
         if sinks is not None:
@@ -149,7 +151,12 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
             K.kvc_prefill_selected(cache, layer, kept, nk, kd, vd)
             ok_heads = [(b, h) for b in range(B) for h in range(Hk)]
         else:
-            cache = K.kvc_prefill_compress(dims, budgets, layer, qd, kd, vd, cache=cache)
+            if selection == "acumul":
+                if cache is None:
+                    cache = K.kvc_cache_create(dims, budgets)
+                K.kvc_prefill_acumul(cache, layer, qf.to(dev), kd, vd)
+            else:
+                cache = K.kvc_prefill_compress(dims, budgets, layer, qd, kd, vd, cache=cache)
             sc = torch.empty(B, Hk, n - a, device=dev)
             pl = torch.empty(B, Hk, n - a, device=dev)
             K.kvc_scores_layer(cache, sc, pl)

@@ -133,3 +133,15 @@ def test_cache_prefill_with_full_prompt_queries():
         want, _, _ = acumul_select(q[0, 2 * h:2 * h + 2], k[0, h], 64, alpha)
         np.testing.assert_array_equal(oc.heads[0][h].kept, want)
         assert oc.n_packed() == 64 and len(oc.heads[0][h].win_k) == alpha
+
+
+@pytest.mark.parametrize("n,g,block", [(300, 2, 128), (513, 1, 128), (257, 4, 64), (40, 3, 7)])
+def test_sampled_columns_match_the_full_computation(n, g, block):
+    """The per-column evaluator (used at full sizes) against the blocked sweep."""
+    rng = np.random.default_rng(n + g)
+    q = rng.standard_normal((g, n, 32)) * 1.5
+    k = rng.standard_normal((n, 32))
+    from oracle import acumul_columns
+    cols = sorted(set([0, 1, block - 1, block, n // 2, n - 2, n - 1]) & set(range(n)))
+    np.testing.assert_allclose(acumul_columns(q, k, cols, block),
+                               acumul_scores(q, k, block)[cols], rtol=1e-12)
