@@ -18,16 +18,21 @@
 // stream through a ring of stages; for every key tile the MMA thread issues
 //   D1[row][key] = Q . K^T   (the running row maxima), and
 //   D2[key][row] = K . Q^T   (the column sums, one key per thread),
-// each 128 x 128 in tensor memory, double-buffered over tiles (512 columns).
-// Eight epilogue warps take each tile in two column halves: the row maxima of
-// D1 are merged in shared memory into the running maxima, then each thread sums
-// exp2(D2 * log2(e)/sqrt(d) - m_row) over its half of the rows for its key; the
-// halves meet in shared memory and one atomic add per key lands the item's
-// contribution in the score row (zeroed before the launch).
+// each 128 x 128 in tensor memory. A CTA runs two items at once, one per
+// epilogue group of eight warps: even items of its list go to group 0, odd ones
+// to group 1, and the producer and MMA thread interleave the two items' tiles
+// (group 0, group 1, group 0, ...; one group alone once the other has run out),
+// so that one group's epilogue overlaps the other's MMAs. Group x owns tensor
+// memory columns [256 x, 256 x + 256) and query buffer x. A group takes each tile
+// in two column halves: the row maxima of D1 are merged in shared memory into the
+// running maxima, then each thread sums exp2(D2 * log2(e)/sqrt(d) - m_row) over
+// its half of the rows for its key; the halves meet in shared memory and one
+// atomic add per key lands the item's contribution in the score row (zeroed
+// before the launch).
 //
 // Roles: warp 0 TMA producer, warp 1 tensor-memory owner and MMA issuer, warps
-// 2..9 epilogue. Every wait is bounded; a wait that gives up sets a bit of the
-// error word and the CTA winds down without further waits.
+// 2..17 epilogue (two groups). Every wait is bounded; a wait that gives up sets a
+// bit of the error word and the CTA winds down without further waits.
 #include <algorithm>
 #include <cudaTypedefs.h>
 
@@ -37,8 +42,8 @@
 namespace kvc {
 namespace {
 
-constexpr int kAcEpiWarps = 8;
-constexpr int kAcThreads = 64 + 32 * kAcEpiWarps;   // producer, MMA, epilogue warps
+constexpr int kAcGroupWarps = 8;                    // epilogue warps per group
+constexpr int kAcThreads = 64 + 2 * 32 * kAcGroupWarps;   // producer, MMA, two groups
 constexpr int kAcTmemCols = 512;
 constexpr int kAcSmemLimit = 232448;                // opt-in shared memory per CTA
 
@@ -48,7 +53,7 @@ template <int D>
 struct AcCfg {
   static constexpr int KB = D / 64;                 // 64-element K blocks
   static constexpr int TBYTES = 128 * D * 2;        // one 128-row bf16 tile
-  static constexpr int QBUF = 2;
+  static constexpr int QBUF = 2;                    // one query buffer per group
   static constexpr int FIT = (kAcSmemLimit - QBUF * TBYTES - 8192) / TBYTES;
   static constexpr int STAGES = FIT > 6 ? 6 : FIT;
   static constexpr int oQ = 0;
@@ -57,9 +62,10 @@ struct AcCfg {
   // full[S], empty[S], qfull[QBUF], qempty[QBUF], tfull[2], tempty[2], drain
   static constexpr int NBAR = 2 * STAGES + 2 * QBUF + 2 * 2 + 1;
   static constexpr int oTmem = oBar + NBAR * 8;
-  static constexpr int oMax = (oTmem + 16 + 15) / 16 * 16;   // [2 halves][128] row maxima
-  static constexpr int oNegM = oMax + 2 * 128 * 4;           // [2 tiles][128] -m per row
-  static constexpr int oPart = oNegM + 2 * 128 * 4;          // [2 tiles][128] half sums
+  // per group: [2 halves][128] row maxima, [128] -m per row, [128] half sums
+  static constexpr int oMax = (oTmem + 16 + 15) / 16 * 16;
+  static constexpr int oNegM = oMax + 2 * 2 * 128 * 4;
+  static constexpr int oPart = oNegM + 2 * 128 * 4;
   static constexpr int total = oPart + 2 * 128 * 4 + 1024;   // + alignment slack
   static_assert(STAGES >= 2, "at least two key stages");
   static_assert(total <= kAcSmemLimit, "fits the shared memory of one CTA");
@@ -104,6 +110,23 @@ __device__ __forceinline__ Item item_of(long long i, const AcArgs& a) {
   return it;
 }
 
+// The interleaved tile order of the producer and the MMA thread: group x works
+// through items x, x + 2, x + 4, ... of the CTA's list; turns alternate between
+// the groups while both have tiles left.
+struct Cursor {
+  Item it;
+  int t;       // next tile of the current item
+  int jn;      // next list position of this group
+  bool live;
+};
+__device__ __forceinline__ void cursor_next_item(Cursor& c, int cta, int G, const AcArgs& a) {
+  const long long i = item_at(cta, c.jn, G);
+  c.live = i < a.items;
+  if (c.live) c.it = item_of(i, a);
+  c.t = 0;
+  c.jn += 2;
+}
+
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
@@ -138,7 +161,7 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     for (int q = 0; q < C::QBUF; ++q) { tc::mbar_init(&qfull[q], 1); tc::mbar_init(&qempty[q], 1); }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&tfull[b], 1);
-      tc::mbar_init(&tempty[b], kAcEpiWarps);
+      tc::mbar_init(&tempty[b], kAcGroupWarps);
     }
     tc::mbar_init(drain, 1);
     tc::fence_mbar_init();
@@ -158,81 +181,90 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   if (warp == 0) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
-      int k = 0, nq = 0;
-      for (int j = 0; ok; ++j) {
-        const long long i = item_at(cta, j, G);
-        if (i >= a.items) break;
-        const Item it = item_of(i, a);
-        const int qb = nq % C::QBUF;
-        if (nq >= C::QBUF)
-          ok = tc::mbar_wait(&qempty[qb], (uint32_t)((nq / C::QBUF - 1) & 1), a.err,
-                             kErrAcProducer);
-        if (!ok) break;
-        // the row block: P positions of each of the g query heads, head-major
-        tc::mbar_expect_tx(&qfull[qb], (uint32_t)C::TBYTES);
-        uint8_t* q = sQ + qb * C::TBYTES;
-        const int b = it.unit / a.Hk, hk = it.unit % a.Hk;
-        for (int hh = 0; hh < a.g; ++hh) {
-          const int row = ((b * a.Hq + hk * a.g + hh) * a.n) + it.p0;
-          for (int kb = 0; kb < C::KB; ++kb)
-            tc::tma_load_2d(q + kb * 128 * 128 + hh * a.P * 128, &tmQ, kb * 64, row, &qfull[qb]);
-        }
-        ++nq;
-        for (int t = 0; t < it.T && ok; ++t, ++k) {
-          const int s = k % C::STAGES, round = k / C::STAGES;
-          if (round > 0)
-            ok = tc::mbar_wait(&empty[s], (uint32_t)((round - 1) & 1), a.err, kErrAcProducer);
+      int k = 0, nq[2] = {0, 0}, turn = 0;
+      Cursor cur[2];
+      for (int x = 0; x < 2; ++x) { cur[x].jn = x; cursor_next_item(cur[x], cta, G, a); }
+      while (ok && (cur[0].live || cur[1].live)) {
+        const int x = cur[turn].live ? turn : turn ^ 1;
+        Cursor& c = cur[x];
+        if (c.t == 0) {
+          // the row block: P positions of each of the g query heads, head-major
+          if (nq[x] > 0)
+            ok = tc::mbar_wait(&qempty[x], (uint32_t)((nq[x] - 1) & 1), a.err, kErrAcProducer);
           if (!ok) break;
-          tc::mbar_expect_tx(&full[s], (uint32_t)C::TBYTES);
-          uint8_t* dst = sK + s * C::TBYTES;
-          for (int kb = 0; kb < C::KB; ++kb)
-            tc::tma_load_2d(dst + kb * 128 * 128, &tmK, kb * 64, it.unit * a.n + t * 128,
-                            &full[s]);
+          tc::mbar_expect_tx(&qfull[x], (uint32_t)C::TBYTES);
+          uint8_t* q = sQ + x * C::TBYTES;
+          const int b = c.it.unit / a.Hk, hk = c.it.unit % a.Hk;
+          for (int hh = 0; hh < a.g; ++hh) {
+            const int row = ((b * a.Hq + hk * a.g + hh) * a.n) + c.it.p0;
+            for (int kb = 0; kb < C::KB; ++kb)
+              tc::tma_load_2d(q + kb * 128 * 128 + hh * a.P * 128, &tmQ, kb * 64, row,
+                              &qfull[x]);
+          }
+          ++nq[x];
         }
+        const int s = k % C::STAGES, round = k / C::STAGES;
+        if (round > 0)
+          ok = tc::mbar_wait(&empty[s], (uint32_t)((round - 1) & 1), a.err, kErrAcProducer);
+        if (!ok) break;
+        tc::mbar_expect_tx(&full[s], (uint32_t)C::TBYTES);
+        uint8_t* dst = sK + s * C::TBYTES;
+        for (int kb = 0; kb < C::KB; ++kb)
+          tc::tma_load_2d(dst + kb * 128 * 128, &tmK, kb * 64, c.it.unit * a.n + c.t * 128,
+                          &full[s]);
+        ++k;
+        if (++c.t == c.it.T) cursor_next_item(c, cta, G, a);
+        turn = x ^ 1;
       }
       // every copy issued here has landed before the CTA can leave
       for (int kk = max(0, k - C::STAGES); kk < k; ++kk)
         tc::mbar_wait(&full[kk % C::STAGES], (uint32_t)((kk / C::STAGES) & 1), a.err,
                       kErrAcProducer);
-      for (int q = max(0, nq - C::QBUF); q < nq; ++q)
-        tc::mbar_wait(&qfull[q % C::QBUF], (uint32_t)((q / C::QBUF) & 1), a.err, kErrAcProducer);
+      for (int x = 0; x < 2; ++x)
+        if (nq[x] > 0)
+          tc::mbar_wait(&qfull[x], (uint32_t)((nq[x] - 1) & 1), a.err, kErrAcProducer);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 128);
-      int k = 0, nq = 0;
-      for (int j = 0; ok; ++j) {
-        const long long i = item_at(cta, j, G);
-        if (i >= a.items) break;
-        const Item it = item_of(i, a);
-        const int qb = nq % C::QBUF;
-        ok = tc::mbar_wait(&qfull[qb], (uint32_t)((nq / C::QBUF) & 1), a.err, kErrAcMma);
-        if (!ok) break;
-        ++nq;
-        for (int t = 0; t < it.T && ok; ++t, ++k) {
-          const int s = k % C::STAGES;
-          ok = tc::mbar_wait(&full[s], (uint32_t)((k / C::STAGES) & 1), a.err, kErrAcMma);
+      int k = 0, nq[2] = {0, 0}, kx[2] = {0, 0}, turn = 0;
+      Cursor cur[2];
+      for (int x = 0; x < 2; ++x) { cur[x].jn = x; cursor_next_item(cur[x], cta, G, a); }
+      while (ok && (cur[0].live || cur[1].live)) {
+        const int x = cur[turn].live ? turn : turn ^ 1;
+        Cursor& c = cur[x];
+        if (c.t == 0) {
+          ok = tc::mbar_wait(&qfull[x], (uint32_t)(nq[x] & 1), a.err, kErrAcMma);
           if (!ok) break;
-          const int bb = k & 1, rb = k >> 1;
-          if (rb > 0) ok = tc::mbar_wait(&tempty[bb], (uint32_t)((rb - 1) & 1), a.err, kErrAcMma);
-          if (!ok) break;
-          tc::fence_after_sync();
-          const uint32_t sQa = tc::saddr(sQ + qb * C::TBYTES);
-          const uint32_t sKa = tc::saddr(sK + s * C::TBYTES);
-          const uint32_t d1 = tbase + (uint32_t)(bb * 256), d2 = d1 + 128u;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int kb = kk / 4, kin = (kk % 4) * 32;
-            const uint64_t qd = tc::sw128_desc(sQa + kb * 128 * 128 + kin);
-            const uint64_t kd = tc::sw128_desc(sKa + kb * 128 * 128 + kin);
-            tc::mma_bf16(d1, qd, kd, idesc, kk > 0 ? 1u : 0u);   // [row][key]
-            tc::mma_bf16(d2, kd, qd, idesc, kk > 0 ? 1u : 0u);   // [key][row]
-          }
-          tc::mma_commit(&empty[s]);
-          tc::mma_commit(&tfull[bb]);
-          if (t + 1 == it.T) tc::mma_commit(&qempty[qb]);
+          ++nq[x];
         }
+        const int s = k % C::STAGES;
+        ok = tc::mbar_wait(&full[s], (uint32_t)((k / C::STAGES) & 1), a.err, kErrAcMma);
+        if (!ok) break;
+        if (kx[x] > 0) ok = tc::mbar_wait(&tempty[x], (uint32_t)((kx[x] - 1) & 1), a.err, kErrAcMma);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t sQa = tc::saddr(sQ + x * C::TBYTES);
+        const uint32_t sKa = tc::saddr(sK + s * C::TBYTES);
+        const uint32_t d1 = tbase + (uint32_t)(x * 256), d2 = d1 + 128u;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int kb = kk / 4, kin = (kk % 4) * 32;
+          const uint64_t qd = tc::sw128_desc(sQa + kb * 128 * 128 + kin);
+          const uint64_t kd = tc::sw128_desc(sKa + kb * 128 * 128 + kin);
+          tc::mma_bf16(d1, qd, kd, idesc, kk > 0 ? 1u : 0u);   // [row][key]
+          tc::mma_bf16(d2, kd, qd, idesc, kk > 0 ? 1u : 0u);   // [key][row]
+        }
+        tc::mma_commit(&empty[s]);
+        tc::mma_commit(&tfull[x]);
+        ++k;
+        ++kx[x];
+        if (++c.t == c.it.T) {
+          tc::mma_commit(&qempty[x]);
+          cursor_next_item(c, cta, G, a);
+        }
+        turn = x ^ 1;
       }
       // every MMA issued here has completed before tensor memory is released
       tc::mma_commit(drain);
@@ -240,13 +272,17 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------- epilogue
+    const int x = (warp - 2) / kAcGroupWarps;    // group
     const int quarter = warp & 3;                 // tensor-memory lane quarter
-    const int half = (warp - 2) >> 2;             // column half of each tile
+    const int half = ((warp - 2) % kAcGroupWarps) >> 2;   // column half of each tile
     const int r = quarter * 32 + lane;            // row of D1 / key of D2 this thread reads
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const int ET = 32 * kAcEpiWarps;
-    int k = 0;
-    for (int j = 0;; ++j) {
+    const int ET = 32 * kAcGroupWarps;
+    float* gmax = smax + x * 256;
+    float* gnegm = snegm + x * 128;
+    float* gpart = spart + x * 128;
+    int k = 0;                                    // tiles of this group so far
+    for (int j = x;; j += 2) {
       const long long i = item_at(cta, j, G);
       if (i >= a.items) break;
       const Item it = item_of(i, a);
@@ -254,15 +290,14 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       const bool row_ok = pos_r < a.n;
       float m = -INFINITY;                        // running maximum of row r (log2 units)
       for (int t = 0; t < it.T; ++t, ++k) {
-        const int bb = k & 1;
-        if (ok) ok = tc::mbar_wait(&tfull[bb], (uint32_t)((k >> 1) & 1), a.err, kErrAcEpilogue);
+        if (ok) ok = tc::mbar_wait(&tfull[x], (uint32_t)(k & 1), a.err, kErrAcEpilogue);
         ok = __all_sync(0xffffffffu, ok);
         tc::fence_after_sync();
         const int key0 = t * 128;
         // does some row miss some key of this tile (causal diagonal, or rows past n)?
         const bool masked = key0 + 127 > it.p0 || it.p0 + a.P > a.n;
         // --- row maxima: row r, columns [64 half, 64 half + 64) of D1
-        const uint32_t c1 = tbase + lane_addr + (uint32_t)(bb * 256 + half * 64);
+        const uint32_t c1 = tbase + lane_addr + (uint32_t)(x * 256 + half * 64);
         float pm = -INFINITY;
 #pragma unroll 1
         for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -276,15 +311,15 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) pm = fmaxf(pm, v[jj]);
         }
-        smax[half * 128 + r] = pm;
-        named_bar(1, ET);
-        const float mt = fmaxf(smax[r], smax[128 + r]);
+        gmax[half * 128 + r] = pm;
+        named_bar(1 + x, ET);
+        const float mt = fmaxf(gmax[r], gmax[128 + r]);
         if (mt != -INFINITY) m = fmaxf(m, mt * a.sl2);
-        if (half == 0) snegm[bb * 128 + r] = -m;
-        named_bar(1, ET);
+        if (half == 0) gnegm[r] = -m;
+        named_bar(1 + x, ET);
         // --- column sums: key r, rows [64 half, 64 half + 64) of D2
-        const uint32_t c2 = tbase + lane_addr + (uint32_t)(bb * 256 + 128 + half * 64);
-        const float* nm = snegm + bb * 128 + half * 64;
+        const uint32_t c2 = tbase + lane_addr + (uint32_t)(x * 256 + 128 + half * 64);
+        const float* nm = gnegm + half * 64;
         const int key = key0 + r;
         float acc = 0.f;
 #pragma unroll 1
@@ -320,13 +355,12 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         }
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&tempty[bb]);
+        if (lane == 0) tc::mbar_arrive(&tempty[x]);
         // the halves meet in shared memory; one atomic add per key
-        float* part = spart + bb * 128;
-        if (half == 1) part[r] = acc;
-        named_bar(1, ET);
+        if (half == 1) gpart[r] = acc;
+        named_bar(1 + x, ET);
         if (half == 0 && ok && key < a.ns) atomicAdd(a.scores + (size_t)it.unit * a.ns + key,
-                                                    acc + part[r]);
+                                                    acc + gpart[r]);
       }
     }
   }
