@@ -127,6 +127,12 @@ __device__ __forceinline__ void cursor_next_item(Cursor& c, int cta, int G, cons
   c.jn += 2;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
@@ -181,16 +187,18 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   if (warp == 0) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
-      int k = 0, nq[2] = {0, 0}, turn = 0;
-      Cursor cur[2];
-      for (int x = 0; x < 2; ++x) { cur[x].jn = x; cursor_next_item(cur[x], cta, G, a); }
-      while (ok && (cur[0].live || cur[1].live)) {
-        const int x = cur[turn].live ? turn : turn ^ 1;
-        Cursor& c = cur[x];
+      int k = 0, nq0 = 0, nq1 = 0, turn = 0;
+      Cursor c0, c1;                // kept in registers: selected by value, written back
+      c0.jn = 0; cursor_next_item(c0, cta, G, a);
+      c1.jn = 1; cursor_next_item(c1, cta, G, a);
+      while (ok && (c0.live || c1.live)) {
+        const int x = (turn ? c1.live : c0.live) ? turn : turn ^ 1;
+        Cursor c = x ? c1 : c0;
+        const int nqx = x ? nq1 : nq0;
         if (c.t == 0) {
           // the row block: P positions of each of the g query heads, head-major
-          if (nq[x] > 0)
-            ok = tc::mbar_wait(&qempty[x], (uint32_t)((nq[x] - 1) & 1), a.err, kErrAcProducer);
+          if (nqx > 0)
+            ok = tc::mbar_wait(&qempty[x], (uint32_t)((nqx - 1) & 1), a.err, kErrAcProducer);
           if (!ok) break;
           tc::mbar_expect_tx(&qfull[x], (uint32_t)C::TBYTES);
           uint8_t* q = sQ + x * C::TBYTES;
@@ -201,7 +209,7 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
               tc::tma_load_2d(q + kb * 128 * 128 + hh * a.P * 128, &tmQ, kb * 64, row,
                               &qfull[x]);
           }
-          ++nq[x];
+          if (x) ++nq1; else ++nq0;
         }
         const int s = k % C::STAGES, round = k / C::STAGES;
         if (round > 0)
@@ -214,35 +222,37 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
                           &full[s]);
         ++k;
         if (++c.t == c.it.T) cursor_next_item(c, cta, G, a);
+        if (x) c1 = c; else c0 = c;
         turn = x ^ 1;
       }
       // every copy issued here has landed before the CTA can leave
       for (int kk = max(0, k - C::STAGES); kk < k; ++kk)
         tc::mbar_wait(&full[kk % C::STAGES], (uint32_t)((kk / C::STAGES) & 1), a.err,
                       kErrAcProducer);
-      for (int x = 0; x < 2; ++x)
-        if (nq[x] > 0)
-          tc::mbar_wait(&qfull[x], (uint32_t)((nq[x] - 1) & 1), a.err, kErrAcProducer);
+      if (nq0 > 0) tc::mbar_wait(&qfull[0], (uint32_t)((nq0 - 1) & 1), a.err, kErrAcProducer);
+      if (nq1 > 0) tc::mbar_wait(&qfull[1], (uint32_t)((nq1 - 1) & 1), a.err, kErrAcProducer);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 128);
-      int k = 0, nq[2] = {0, 0}, kx[2] = {0, 0}, turn = 0;
-      Cursor cur[2];
-      for (int x = 0; x < 2; ++x) { cur[x].jn = x; cursor_next_item(cur[x], cta, G, a); }
-      while (ok && (cur[0].live || cur[1].live)) {
-        const int x = cur[turn].live ? turn : turn ^ 1;
-        Cursor& c = cur[x];
+      int k = 0, nq0 = 0, nq1 = 0, kx0 = 0, kx1 = 0, turn = 0;
+      Cursor c0, c1;                // kept in registers: selected by value, written back
+      c0.jn = 0; cursor_next_item(c0, cta, G, a);
+      c1.jn = 1; cursor_next_item(c1, cta, G, a);
+      while (ok && (c0.live || c1.live)) {
+        const int x = (turn ? c1.live : c0.live) ? turn : turn ^ 1;
+        Cursor c = x ? c1 : c0;
+        const int kxx = x ? kx1 : kx0;
         if (c.t == 0) {
-          ok = tc::mbar_wait(&qfull[x], (uint32_t)(nq[x] & 1), a.err, kErrAcMma);
+          ok = tc::mbar_wait(&qfull[x], (uint32_t)((x ? nq1 : nq0) & 1), a.err, kErrAcMma);
           if (!ok) break;
-          ++nq[x];
+          if (x) ++nq1; else ++nq0;
         }
         const int s = k % C::STAGES;
         ok = tc::mbar_wait(&full[s], (uint32_t)((k / C::STAGES) & 1), a.err, kErrAcMma);
         if (!ok) break;
-        if (kx[x] > 0) ok = tc::mbar_wait(&tempty[x], (uint32_t)((kx[x] - 1) & 1), a.err, kErrAcMma);
+        if (kxx > 0) ok = tc::mbar_wait(&tempty[x], (uint32_t)((kxx - 1) & 1), a.err, kErrAcMma);
         if (!ok) break;
         tc::fence_after_sync();
         const uint32_t sQa = tc::saddr(sQ + x * C::TBYTES);
@@ -259,11 +269,12 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         tc::mma_commit(&empty[s]);
         tc::mma_commit(&tfull[x]);
         ++k;
-        ++kx[x];
+        if (x) ++kx1; else ++kx0;
         if (++c.t == c.it.T) {
           tc::mma_commit(&qempty[x]);
           cursor_next_item(c, cta, G, a);
         }
+        if (x) c1 = c; else c0 = c;
         turn = x ^ 1;
       }
       // every MMA issued here has completed before tensor memory is released
@@ -308,8 +319,13 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) v[jj] = jj <= lim ? v[jj] : -INFINITY;
           }
+          float ma = v[0], mb = v[16];
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) pm = fmaxf(pm, v[jj]);
+          for (int jj = 1; jj < 15; jj += 2) {
+            ma = max3(ma, v[jj], v[jj + 1]);
+            mb = max3(mb, v[jj + 16], v[jj + 17]);
+          }
+          pm = max3(pm, max3(ma, v[15], v[31]), mb);
         }
         gmax[half * 128 + r] = pm;
         named_bar(1 + x, ET);
@@ -327,14 +343,17 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
           float v[32];
           tc::tmem_ld32(c2 + (uint32_t)c0, v);
           if (!masked) {
+            // paired fp32 arithmetic: two logits per instruction
             const float4* nm4 = reinterpret_cast<const float4*>(nm + c0);
+            const float2 s2 = make_float2(a.sl2, a.sl2);
 #pragma unroll
             for (int jj = 0; jj < 32; jj += 4) {
               const float4 b4 = nm4[jj / 4];
-              v[jj] = fmaf(v[jj], a.sl2, b4.x);
-              v[jj + 1] = fmaf(v[jj + 1], a.sl2, b4.y);
-              v[jj + 2] = fmaf(v[jj + 2], a.sl2, b4.z);
-              v[jj + 3] = fmaf(v[jj + 3], a.sl2, b4.w);
+              const float2 lo = __ffma2_rn(make_float2(v[jj], v[jj + 1]), s2,
+                                           make_float2(b4.x, b4.y));
+              const float2 hi = __ffma2_rn(make_float2(v[jj + 2], v[jj + 3]), s2,
+                                           make_float2(b4.z, b4.w));
+              v[jj] = lo.x; v[jj + 1] = lo.y; v[jj + 2] = hi.x; v[jj + 3] = hi.y;
             }
           } else {
 #pragma unroll
@@ -347,11 +366,16 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj)
             asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(v[jj]) : "f"(v[jj]));
+          float2 sum[8];
 #pragma unroll
-          for (int w = 16; w > 0; w >>= 1)
+          for (int q = 0; q < 8; ++q)
+            sum[q] = __fadd2_rn(make_float2(v[2 * q], v[2 * q + 1]),
+                                make_float2(v[2 * q + 16], v[2 * q + 17]));
 #pragma unroll
-            for (int jj = 0; jj < w; ++jj) v[jj] += v[jj + w];
-          acc += v[0];
+          for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+            for (int q = 0; q < w; ++q) sum[q] = __fadd2_rn(sum[q], sum[q + w]);
+          acc += sum[0].x + sum[0].y;
         }
         tc::fence_before_sync();
         __syncwarp();
