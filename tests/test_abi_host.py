@@ -122,3 +122,13 @@ def test_weighted_planner_rejects(kvc):
         with pytest.raises(kvc.KvcError) as e:
             kvc.kvc_plan_budgets_weighted(dims, avg, w)
         assert e.value.status == 1
+
+
+def test_new_entry_points_reject_null_handles(kvc):
+    lib = ctypes.CDLL(LIB)
+    for name, args in (("kvc_prefill_acumul", (None, 0, None, None, None, None)),
+                       ("kvc_score_variance", (None, None, None)),
+                       ("kvc_plan_budgets_weighted", (None, 64, None, None))):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        assert f(*args) in (1, 2), name       # KVC_E_ARG (or KVC_E_SHAPE for null dims)
