@@ -290,9 +290,15 @@ def run_gpu(args):
     block_bytes = 8 * D * (spec.bits + 1)
 
     dec_bytes = []   # algorithmic bytes of each decode-attention launch
+    HOLD_CYCLES = 60_000_000 * max(1, S // 256)   # ~30 ms at 2 GHz per 256 decode steps
 
     def one_step(record_bytes=False):
         K.kvc_cache_reset(cache)
+        # hold the device (outside every timed interval) while the host enqueues the
+        # step: a decode call costs the host about as long as a flush + decode costs
+        # the device, and a late enqueue would leave the device idle inside a timed
+        # launch interval
+        torch.cuda._sleep(HOLD_CYCLES)
         c0.record(stream)
         for l in range(L):
             x = prompt[l]
