@@ -369,6 +369,31 @@ def run_gpu(args):
                 sms.append(cs0.elapsed_time(cs1))
         sink_ms = statistics.mean(sms) / L
 
+    # the variance score of the last scored layer (the statistic behind Var-prop /
+    # Var-inv budgets): one launch reading the layer's scores twice
+    variance = None
+    if any(b_ < spec.prompt_len - spec.obs_window for b_ in budgets):
+        K.kvc_cache_reset(cache)
+        for l in range(L):
+            x = prompt[l]
+            K.kvc_prefill_compress(dims, budgets, l, x.get("q_obs"), x["k"], x["v"],
+                                   cache=cache)
+        var = torch.empty(B, Hk, device=dev)
+        v0, v1 = ev(), ev()
+        for _ in range(3):
+            K.kvc_score_variance(cache, var)
+        v0.record(stream)
+        for _ in range(20):
+            K.kvc_score_variance(cache, var)
+        v1.record(stream)
+        torch.cuda.synchronize()
+        v_us = v0.elapsed_time(v1) * 1e3 / 20
+        v_bytes = B * Hk * (spec.prompt_len - spec.obs_window) * 4 * 2
+        variance = {"us_per_launch": v_us, "bytes": v_bytes,
+                    "gbs": v_bytes / (v_us * 1e-6) / 1e9,
+                    "note": "per-(sequence, kv head) variance of the last scored layer's "
+                            "scores (two passes over them; they sit in L2)"}
+
     # selection by the full-prompt cumulated attention (every prompt query, un-normalised
     # column sums): the first two layers compressed with it, outside the timed steps
     acumul = None
@@ -491,6 +516,7 @@ def run_gpu(args):
         "compress_ms_per_layer": comp_ms / L,
         "decode_16bit": None if exact16 is None else dict(
             exact16, frac=exact16["gbs"] / hbm),
+        "score_variance": variance,
         "compress_acumul": None if acumul is None else dict(
             acumul, frac=acumul["tflops"] / tc),
         "compress_sinks": None if sink_ms is None else {
