@@ -39,22 +39,39 @@ __device__ double block_sum(double v, double* red) {
 // MiniKV §4.2 "Layer-Specific Selectivity" (the variance policy) and Figure 7:
 // the variance score of cumulated attention. One CTA per (sequence, kv head):
 // population variance of its m selection scores, two passes (mean, then squared
-// deviations) accumulated in fp64.
+// deviations). Each thread keeps a compensated fp32 sum (Kahan) of its strided
+// elements; the block adds the 256 partial sums in fp64 in a fixed order. (fp64
+// arithmetic per element would run at the part's small fp64 rate.)
 constexpr int kVarThreads = 256;
+
+struct Kahan {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float y = x - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+  }
+  __device__ __forceinline__ double value() const { return (double)s - (double)c; }
+};
+
 __global__ void __launch_bounds__(kVarThreads) score_variance_kernel(
     const float* __restrict__ scores, int m, float* __restrict__ var) {
   __shared__ double red[kVarThreads / 32];
   const float* row = scores + (size_t)blockIdx.x * m;
-  double acc = 0.0;
-  for (int i = threadIdx.x; i < m; i += kVarThreads) acc += (double)row[i];
-  const double mean = block_sum(acc, red) / m;
-  double acc2 = 0.0;
+  Kahan acc;
+  for (int i = threadIdx.x; i < m; i += kVarThreads) acc.add(row[i]);
+  const double mean = block_sum(acc.value(), red) / m;
+  const float mean_f = (float)mean;
+  Kahan acc2;
   for (int i = threadIdx.x; i < m; i += kVarThreads) {
-    const double dv = (double)row[i] - mean;
-    acc2 += dv * dv;
+    const float dv = row[i] - mean_f;
+    acc2.add(dv * dv);
   }
-  const double v = block_sum(acc2, red) / m;
-  if (threadIdx.x == 0) var[blockIdx.x] = (float)v;
+  // sum (x - mean_f)^2 = n var + n (mean - mean_f)^2: remove the second term
+  const double dm = mean - (double)mean_f;
+  const double v = block_sum(acc2.value(), red) / m - dm * dm;
+  if (threadIdx.x == 0) var[blockIdx.x] = (float)(v > 0.0 ? v : 0.0);
 }
 
 }  // namespace
