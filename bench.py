@@ -36,7 +36,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--workload", type=int, default=5,
+                    help="the headline workload (default 5: long context, 2-bit)")
+    ap.add_argument("--legs", default="3,4",
+                    help="comma-separated workloads measured after the headline one "
+                         "(decode GB/s and compression ms/layer each); empty for none")
     ap.add_argument("--decode-steps", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None,
                     help="use only the first N layers (small cases for profiler captures)")
@@ -313,13 +317,7 @@ def run_gpu(args):
             K.kvc_decode_step(cache, 0, L, qs[t], kns[t], vns[t], out)
             e2.record(stream)
             if record_bytes:
-                tot = 0
-                for l in range(L):
-                    info = K.kvc_layer_info_get(cache, l)
-                    tot += B * Hk * (info["packed_tokens"] // 32 * block_bytes
-                                     + info["window_tokens"] * D * 4)
-                tot += L * B * Hq * D * (2 + 4) + L * B * Hk * D * 2 * 2
-                dec_bytes.append(tot)
+                dec_bytes.append(decode_bytes(K, cache, spec))
 
     def collect():
         torch.cuda.synchronize()
@@ -473,16 +471,7 @@ def run_gpu(args):
     dec_gbs = mean_bytes / (att_ms / 1e3) / 1e9
     # compression: algorithmic bytes and flops per layer
     ns = spec.prompt_len - spec.obs_window
-    comp_bytes = comp_flops = 0
-    for l in range(L):
-        kept = min(budgets[l], ns)
-        scored = kept < ns
-        comp_bytes += (B * Hk * spec.prompt_len * D * 2 * (1 if scored else 2)
-                       + (B * Hk * kept * D * 2 * 2 if scored else 0)
-                       + B * Hk * (kept // 32) * block_bytes
-                       + (B * Hq * spec.obs_window * D * 2 if scored else 0))
-        comp_flops += 2 * B * Hq * spec.obs_window * spec.prompt_len * D if scored else 0
-    t_roof = max(comp_bytes / (hbm * 1e9), comp_flops / (tc * 1e12))
+    comp_bytes, comp_flops, t_roof = compress_roofline(spec, budgets, hbm, tc)
     comp_frac = t_roof / (comp_ms / 1e3)
     # sink + recent selection: kept rows read, packed groups and window rows written
     sink_bytes = 0
@@ -541,11 +530,112 @@ def run_gpu(args):
         line["cpu_baseline"] = {"value": B / per_token, "unit": UNIT, "cores": cpu_cores(),
                                 "kind": "oracle", "sample": text,
                                 "compress_ms_per_layer": c * 1e3}
+    cache.close()
+    legs = [int(w) for w in args.legs.split(",") if w.strip()] if args.legs else []
+    legs = [w for w in legs if w != args.workload]
+    if legs and world == 1 and not args.layers:
+        del prompt, qs, kns, vns, cache
+        torch.cuda.empty_cache()
+        line["legs"] = {str(w): run_leg(K, w, hbm, tc, dev, flush) for w in legs}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    cache.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+def decode_bytes(K, cache, spec):
+    """Algorithmic bytes one decode launch over all layers reads and writes in the
+    cache's current state (packed groups, window tokens incl. the new one, q, o,
+    the new key/value)."""
+    B, Hk, Hq, D, L = spec.batch, spec.n_kv_heads, spec.n_q_heads, spec.head_dim, spec.n_layers
+    tot = 0
+    for l in range(L):
+        info = K.kvc_layer_info_get(cache, l)
+        blk = 8 * D * (info["bits"] + 1) if info["bits"] != 16 else 0
+        tot += B * Hk * (info["packed_tokens"] // 32 * blk + info["window_tokens"] * D * 4)
+    return tot + L * B * Hq * D * (2 + 4) + L * B * Hk * D * 2 * 2
+
+
+def compress_roofline(spec, budgets, hbm, tc):
+    """Algorithmic bytes and flops of compressing every layer, and the roofline time."""
+    B, Hk, Hq, D, L = spec.batch, spec.n_kv_heads, spec.n_q_heads, spec.head_dim, spec.n_layers
+    block_bytes = 8 * D * (spec.bits + 1)
+    ns = spec.prompt_len - spec.obs_window
+    comp_bytes = comp_flops = 0
+    for l in range(L):
+        kept = min(budgets[l], ns)
+        scored = kept < ns
+        comp_bytes += (B * Hk * spec.prompt_len * D * 2 * (1 if scored else 2)
+                       + (B * Hk * kept * D * 2 * 2 if scored else 0)
+                       + B * Hk * (kept // 32) * block_bytes
+                       + (B * Hq * spec.obs_window * D * 2 if scored else 0))
+        comp_flops += 2 * B * Hq * spec.obs_window * spec.prompt_len * D if scored else 0
+    t_roof = max(comp_bytes / (hbm * 1e9), comp_flops / (tc * 1e12))
+    return comp_bytes, comp_flops, t_roof
+
+
+def run_leg(K, wid, hbm, tc, dev, flush):
+    """One more workload, measured like the headline one: compression of every layer
+    (CUDA events around each layer's call; the layer's inputs are generated just
+    before, outside the timed interval, so that the largest workload need not hold
+    its whole prompt), then every decode step (one launch over all layers, L2
+    flushed before each, CUDA events around the launch)."""
+    import torch
+    import synth
+    spec = synth.workload(wid)
+    S = spec.steps
+    L, B, Hq, D = spec.n_layers, spec.batch, spec.n_q_heads, spec.head_dim
+    dims = K.dims_from_spec(spec, max_new_tokens=S)
+    budgets = K.kvc_plan_budgets(dims, spec.schedule, spec.avg_budget, spec.pyramid_depth)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    cache = K.kvc_cache_create(dims, budgets)
+    comp = []
+    for rep_i in range(2):      # the first pass warms up
+        K.kvc_cache_reset(cache)
+        tot = 0.0
+        for l in range(L):
+            x = synth.layer_inputs(spec, l, device=dev)
+            torch.cuda.synchronize()
+            a, b = ev(), ev()
+            a.record(stream)
+            K.kvc_prefill_compress(dims, budgets, l, x.get("q_obs"), x["k"], x["v"], cache=cache)
+            b.record(stream)
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+            del x
+        comp.append(tot)
+    comp_ms = comp[-1]
+    out = torch.empty(L, B, Hq, D, device=dev)
+    att, nbytes = [], []
+    for t in range(S):
+        dx = synth.decode_inputs_layers(spec, t, range(L), device=dev)
+        nbytes.append(decode_bytes(K, cache, spec))
+        flush.max()
+        a, b = ev(), ev()
+        a.record(stream)
+        K.kvc_decode_step(cache, 0, L, dx["q"], dx["k_new"], dx["v_new"], out)
+        b.record(stream)
+        torch.cuda.synchronize()
+        att.append(a.elapsed_time(b))
+        del dx
+    K.kvc_check_device(cache)
+    cache.close()
+    warm = 3 if S > 6 else 0    # the first launches pay one-time set-up
+    att_ms = statistics.mean(att[warm:])
+    mean_bytes = statistics.mean(nbytes[warm:])
+    gbs = mean_bytes / (att_ms / 1e3) / 1e9
+    cb, cf, t_roof = compress_roofline(spec, budgets, hbm, tc)
+    return {"workload": workload_desc(spec, S),
+            "decode_tokens_per_s": B * S / (sum(att) / 1e3),
+            "decode_attn_us_per_launch": att_ms * 1e3,
+            "bytes_per_launch": mean_bytes, "cache_gbs": gbs, "cache_frac_of_hbm": gbs / hbm,
+            "compress_ms_per_layer": comp_ms / L,
+            "compress_roofline": {"bytes": cb, "flops": cf, "t_roof_ms": t_roof * 1e3,
+                                  "frac": t_roof / (comp_ms / 1e3)},
+            "note": "decode: one launch per token over all layers (append + split-K attention), "
+                    "L2 flushed before each; compression: each layer's call timed alone, its "
+                    "inputs generated outside the timed interval"}
 
 
 def e2e_measure(K, spec, dims, budgets, cache, prompt, qs, kns, vns, S, dev, steps=2):

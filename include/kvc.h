@@ -36,6 +36,13 @@
  *   - Arguments are validated on the host before anything is enqueued; a
  *     failing call returns a status and enqueues nothing (or, for a launch
  *     failure, KVC_E_CUDA). Calls never abort, exit or trap.
+ *   - Every device-side wait is bounded. A wait that gives up sets the cache's
+ *     error word and its kernel winds down (its output is then undefined).
+ *     Where the device has native atomics on host memory (e.g. a Grace-hosted
+ *     GPU) the word lives in mapped pinned host memory, and the next call on the
+ *     cache made after the word was set returns KVC_E_TIMEOUT, enqueues nothing
+ *     and clears it; elsewhere kvc_check_device reports it. After KVC_E_TIMEOUT
+ *     the cache's contents are undefined: kvc_cache_reset and prefill again.
  *   - Tensors are dense, row-major, bf16 unless stated; outputs are fp32.
  */
 #ifndef KVC_H_
@@ -229,6 +236,25 @@ kvc_status kvc_cache_create(const kvc_dims* dims, const int32_t* budgets,
                             kvc_cache** cache);
 
 /* ---------------------------------------------------------------------------
+ * kvc_cache_create_layers -- create an empty cache whose layers differ in
+ *   precision: MiniKV Figure 1's layer-discriminative cache (16-bit top layers,
+ *   2-bit lower layers; §4.1's 16-bit buffer holds the exact tokens).
+ *   layer_bits: host array of n_layers entries, each 2, 4 or 16. A 2/4-bit layer
+ *   is stored as kvc_cache_create stores it at that precision, with a window of
+ *   dims->window_len slots. A 16-bit layer keeps every token exact: when
+ *   dims->bits is 2 or 4 its bf16 ring is sized to hold its kept, observation
+ *   and max_new_tokens appended tokens (rounded up to 32); when dims->bits is 16
+ *   the ring has dims->window_len slots, which must hold them. dims->bits must
+ *   still be 2, 4 or 16. Every other call works on such a cache unchanged, and
+ *   one decode launch attends over all its layers, whatever their precision.
+ *   Errors: KVC_E_ARG (null pointer, an entry not 2/4/16), KVC_E_SHAPE (a
+ *   16-bit ring longer than 65,536 slots, or an initial window that does not
+ *   fit), KVC_E_OOM.
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_cache_create_layers(const kvc_dims* dims, const int32_t* budgets,
+                                   const int32_t* layer_bits, kvc_cache** cache);
+
+/* ---------------------------------------------------------------------------
  * kvc_append -- append one token per (sequence, kv head) to one layer.
  *   MiniKV Algorithm 1 (decoding: concatenate into the 16-bit buffer; quantize
  *   when it fills). k_new, v_new: device bf16 [batch][n_kv_heads][head_dim].
@@ -252,9 +278,12 @@ kvc_status kvc_append_layers(kvc_cache* cache, int32_t layer_begin, int32_t laye
  *   blog "Measured on a real model" (exact window, rounded rest).
  *   q:   device bf16 [layer_count][batch][n_q_heads][head_dim].
  *   out: device fp32 [layer_count][batch][n_q_heads][head_dim] (written).
- *   Query head j reads kv head j / g. The token axis of each (sequence, kv
- *   head) is split over warps of one CTA and merged with a log-sum-exp combine
- *   inside the same launch.
+ *   Query head j reads kv head j / g. q and out must be 16-byte aligned. The token
+ *   axis of every (layer, sequence, kv head) of the call is cut into chunks (16
+ *   window tokens, or the packed groups of the same bytes), and the chunks of
+ *   all of them are shared out evenly over every warp of the grid; a unit
+ *   spread over several warps is merged with a log-sum-exp combine, in a fixed
+ *   order, by the warp that finishes it last (same launch).
  *   Errors: KVC_E_STATE (a layer not prefilled), KVC_E_ARG, KVC_E_CUDA.
  * ------------------------------------------------------------------------- */
 kvc_status kvc_decode_attn(kvc_cache* cache, int32_t layer_begin, int32_t layer_count,
@@ -276,6 +305,14 @@ kvc_status kvc_decode_step(kvc_cache* cache, int32_t layer_begin, int32_t layer_
  * The error word is cleared. */
 kvc_status kvc_check_device(kvc_cache* cache, void* stream);
 
+/* kvc_set_wait_limit -- bound every staging wait of this cache's decode launches
+ * to `polls` polls of its mbarrier (0: each wait gives up at once); a negative
+ * value restores the default bound (2^20 polls). A testing aid: it lets a test
+ * drive the timeout path (the kernel winds down, lets its copies land, hands its
+ * partial units over so the arrival counters return to zero, and the error is
+ * reported) without faulting anything. Errors: KVC_E_ARG. */
+kvc_status kvc_set_wait_limit(kvc_cache* cache, int64_t polls);
+
 /* kvc_free -- release the cache and all device storage it owns. The caller
  * must ensure no enqueued work still uses it (synchronize the stream first).
  * NULL is accepted. */
@@ -293,6 +330,8 @@ typedef struct kvc_layer_info {
   int32_t window_tokens;  /* tokens in the bf16 window                           */
   int32_t appended;       /* tokens appended since prefill                       */
   int64_t packed_bytes;   /* device bytes of this layer's packed store           */
+  int32_t bits;           /* storage precision of the layer: 2, 4 or 16          */
+  int32_t window_capacity;/* slots of the layer's bf16 ring                      */
 } kvc_layer_info;
 
 kvc_status kvc_layer_info_get(const kvc_cache* cache, int32_t layer, kvc_layer_info* out);
@@ -361,12 +400,26 @@ kvc_status kvc_scores_layer(kvc_cache* cache, float* scores, float* pooled, void
  *   kept:  device int32 [B][H][min(budget, n - alpha)] (written, ascending);
  *   scores: optional device fp32 [B][H][n - alpha] (written when not NULL).
  *   Only the fields n_layers..pool_kernel of dims are read.
+ *   The static arrays are committed on a device by the first call made on it
+ *   (the runtime loads their module lazily): make that call before an arena
+ *   reserves the rest of the device's memory.
+ *   A bounded wait inside the scoring launch that gives up sets the entry
+ *   point's own error word; the top-k launch then writes every kept index as
+ *   -1 (never a stale selection), and kvc_select_noalloc_check reports it.
  *   Errors: KVC_E_ARG, KVC_E_SHAPE, KVC_E_CAPACITY (the sizes need more than
- *   the static scratch, or B*H > 8192; nothing is enqueued), KVC_E_CUDA.
+ *   the static scratch, or B*H > 8192; nothing is enqueued), KVC_E_OOM (the
+ *   static arrays could not be committed on this device), KVC_E_CUDA.
  * ------------------------------------------------------------------------- */
 #define KVC_NOALLOC_SCRATCH_BYTES (32u << 20)
 kvc_status kvc_select_noalloc(const kvc_dims* dims, int32_t budget, const void* q_obs,
                               const void* k, int32_t* kept, float* scores, void* stream);
+
+/* kvc_select_noalloc_check -- synchronize `stream` and report whether a bounded
+ * wait of a kvc_select_noalloc call on the current device gave up since the
+ * last check (KVC_E_TIMEOUT; those calls wrote -1 kept indices), then clear the
+ * word. KVC_OK when none did or no call was made on this device. Allocates
+ * nothing. Errors: KVC_E_CUDA. */
+kvc_status kvc_select_noalloc_check(void* stream);
 
 /* kvc_cache_reset -- forget every layer's contents (host-side state only; the
  * device storage is kept) so the cache can take the next prompt with the same

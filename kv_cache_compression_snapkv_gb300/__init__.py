@@ -46,7 +46,8 @@ class KvcLayerInfo(ctypes.Structure):
     _fields_ = [("prefilled", ctypes.c_int32), ("budget", ctypes.c_int32),
                 ("n_kept", ctypes.c_int32), ("packed_tokens", ctypes.c_int32),
                 ("capacity_tokens", ctypes.c_int32), ("window_tokens", ctypes.c_int32),
-                ("appended", ctypes.c_int32), ("packed_bytes", ctypes.c_int64)]
+                ("appended", ctypes.c_int32), ("packed_bytes", ctypes.c_int64),
+                ("bits", ctypes.c_int32), ("window_capacity", ctypes.c_int32)]
 
 
 class KvcExport(ctypes.Structure):
@@ -67,6 +68,7 @@ _SIGS = {
     "kvc_prefill_sinks": [_P, _I, _I, _P, _P, _P],
     "kvc_prefill_acumul": [_P, _I, _P, _P, _P, _P],
     "kvc_cache_create": [ctypes.POINTER(KvcDims), _P, ctypes.POINTER(ctypes.c_void_p)],
+    "kvc_cache_create_layers": [ctypes.POINTER(KvcDims), _P, _P, ctypes.POINTER(ctypes.c_void_p)],
     "kvc_append": [_P, _I, _P, _P, _P],
     "kvc_append_layers": [_P, _I, _I, _P, _P, _P],
     "kvc_decode_attn": [_P, _I, _I, _P, _P, _P],
@@ -78,7 +80,9 @@ _SIGS = {
     "kvc_score_variance": [_P, _P, _P],
     "kvc_cache_reset": [_P],
     "kvc_select_noalloc": [ctypes.POINTER(KvcDims), _I, _P, _P, _P, _P, _P],
+    "kvc_select_noalloc_check": [_P],
     "kvc_check_device": [_P, _P],
+    "kvc_set_wait_limit": [_P, ctypes.c_int64],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -176,6 +180,18 @@ def kvc_cache_create(dims: KvcDims, budgets: Sequence[int]) -> Cache:
     h = ctypes.c_void_p()
     _check(_lib.kvc_cache_create(ctypes.byref(dims), _budget_array(budgets), ctypes.byref(h)),
            "kvc_cache_create")
+    return Cache(h.value, dims, budgets)
+
+
+def kvc_cache_create_layers(dims: KvcDims, budgets: Sequence[int],
+                            layer_bits: Sequence[int]) -> Cache:
+    """A cache whose layers have their own precision (2, 4 or 16 bits each)."""
+    if len(layer_bits) != dims.n_layers:
+        raise ValueError("need one precision per layer")
+    h = ctypes.c_void_p()
+    _check(_lib.kvc_cache_create_layers(ctypes.byref(dims), _budget_array(budgets),
+                                        _budget_array(list(layer_bits)), ctypes.byref(h)),
+           "kvc_cache_create_layers")
     return Cache(h.value, dims, budgets)
 
 
@@ -287,9 +303,20 @@ def kvc_select_noalloc(dims: KvcDims, budget: int, q_obs, k, kept, scores=None, 
                                    _ptr(scores), _stream(stream)), "kvc_select_noalloc")
 
 
+def kvc_select_noalloc_check(stream=None):
+    """Synchronize and raise KvcError(KVC_E_TIMEOUT) if a bounded wait of a
+    kvc_select_noalloc call on this device gave up since the last check."""
+    _check(_lib.kvc_select_noalloc_check(_stream(stream)), "kvc_select_noalloc_check")
+
+
 def kvc_check_device(cache: Cache, stream=None):
     """Synchronize and raise KvcError(KVC_E_TIMEOUT) if a bounded device wait gave up."""
     _check(_lib.kvc_check_device(cache.handle, _stream(stream)), "kvc_check_device")
+
+
+def kvc_set_wait_limit(cache: Cache, polls: int):
+    """Bound the cache's decode staging waits to `polls` polls (negative: default)."""
+    _check(_lib.kvc_set_wait_limit(cache.handle, polls), "kvc_set_wait_limit")
 
 
 def kvc_launch_count() -> int:
@@ -302,10 +329,11 @@ def exported_symbols() -> list:
 
 
 __all__ = ["KvcDims", "KvcError", "Cache", "make_dims", "dims_from_spec", "kvc_plan_budgets",
-           "kvc_cache_create", "kvc_prefill_compress", "kvc_prefill_selected", "kvc_prefill_sinks",
+           "kvc_cache_create", "kvc_cache_create_layers", "kvc_prefill_compress", "kvc_prefill_selected", "kvc_prefill_sinks",
            "kvc_append",
            "kvc_append_layers", "kvc_decode_attn", "kvc_decode_step", "kvc_free",
            "kvc_layer_info_get", "kvc_export_layer", "kvc_scores_layer", "kvc_cache_reset",
            "kvc_plan_budgets_weighted", "kvc_score_variance", "kvc_prefill_acumul",
-           "kvc_launch_count", "kvc_check_device", "kvc_select_noalloc", "LIB_PATH",
+           "kvc_launch_count", "kvc_check_device", "kvc_select_noalloc",
+           "kvc_select_noalloc_check", "kvc_set_wait_limit", "LIB_PATH",
            "exported_symbols"]

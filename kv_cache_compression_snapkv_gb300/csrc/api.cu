@@ -87,6 +87,46 @@ void release_all(kvc_cache* c) {
     else cudaFree(p);
   }
   c->allocations.clear();
+  if (c->err_pinned) cudaFreeHost(c->err_pinned);
+  c->err_pinned = nullptr;
+  c->err_host = nullptr;
+}
+
+// The cache's error word: in mapped pinned host memory when the device has native
+// atomics on host memory (the kernels' atomicOr then lands where the host reads it
+// without synchronising), else in device memory.
+bool make_error_word(kvc_cache* c) {
+  int native = 0, can_map = 0;
+  if (cudaDeviceGetAttribute(&native, cudaDevAttrHostNativeAtomicSupported, c->device) ==
+          cudaSuccess &&
+      cudaDeviceGetAttribute(&can_map, cudaDevAttrCanMapHostMemory, c->device) == cudaSuccess &&
+      native && can_map) {
+    void* h = nullptr;
+    void* d = nullptr;
+    if (cudaHostAlloc(&h, 16, cudaHostAllocMapped | cudaHostAllocPortable) == cudaSuccess) {
+      if (cudaHostGetDevicePointer(&d, h, 0) == cudaSuccess) {
+        std::memset(h, 0, 16);
+        c->err_pinned = h;
+        c->err_host = static_cast<volatile unsigned*>(h);
+        c->err = static_cast<unsigned*>(d);
+        return true;
+      }
+      cudaFreeHost(h);
+    }
+    cudaGetLastError();
+  }
+  c->err = static_cast<unsigned*>(dev_alloc(c, 16));
+  return c->err != nullptr && cudaMemset(c->err, 0, 16) == cudaSuccess;
+}
+
+// A bounded device wait of earlier work on the cache gave up (seen without a
+// synchronisation where the error word is host-visible): report it once.
+kvc_status pending_error(kvc_cache* c) {
+  if (c->err_host && *c->err_host != 0u) {
+    *c->err_host = 0u;
+    return KVC_E_TIMEOUT;
+  }
+  return KVC_OK;
 }
 
 int kept_cap(const kvc_dims& d, int budget) {
@@ -94,15 +134,26 @@ int kept_cap(const kvc_dims& d, int budget) {
   return budget < ns ? budget : ns;
 }
 
-// The initial window of a layer keeping n_kept tokens fits the ring: the tokens past
-// the last whole group plus the observation tokens (2/4-bit), or, with 16-bit
-// storage (no packed store, no flush), every kept, observation and appended token.
-bool window_fits(const kvc_dims& d, int n_kept) {
-  if (d.bits == 16) return n_kept + d.obs_window + d.max_new_tokens <= d.window_len;
-  return n_kept % KVC_GROUP + d.obs_window < d.window_len;
+// The initial window of a layer keeping n_kept tokens fits its ring of R slots: the
+// tokens past the last whole group plus the observation tokens (2/4-bit), or, with
+// 16-bit storage (no packed store, no flush), every kept, observation and appended
+// token.
+bool window_fits(const kvc_dims& d, int bits, int R, int n_kept) {
+  if (bits == 16) return n_kept + d.obs_window + d.max_new_tokens <= R;
+  return n_kept % KVC_GROUP + d.obs_window < R;
 }
 
-kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out) {
+// Ring length of a layer stored at `bits`: the cache's window_len, except a 16-bit
+// layer of a cache whose default precision is 2 or 4 bits, whose ring is sized to
+// hold every token it will store.
+int ring_len(const kvc_dims& d, int bits, int n_kept) {
+  if (bits != 16 || d.bits == 16) return d.window_len;
+  const int need = n_kept + d.obs_window + d.max_new_tokens;
+  return std::max(KVC_GROUP, (need + KVC_GROUP - 1) / KVC_GROUP * KVC_GROUP);
+}
+
+kvc_status create(const kvc_dims* dims, const int32_t* budgets, const int32_t* layer_bits,
+                  kvc_cache** out) {
   kvc_status st = check_dims(dims);
   if (st != KVC_OK) return st;
   if (!budgets || !out) return KVC_E_ARG;
@@ -113,8 +164,11 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
   bool scoring = false;
   for (int l = 0; l < d.n_layers; ++l) {
     if (budgets[l] < 0) return KVC_E_ARG;
+    const int bits = layer_bits ? layer_bits[l] : d.bits;
+    if (bits != 2 && bits != 4 && bits != 16) return KVC_E_ARG;
     const int nk = kept_cap(d, budgets[l]);
-    if (!window_fits(d, nk)) return KVC_E_SHAPE;
+    const int R = ring_len(d, bits, nk);
+    if (R > 65536 || !window_fits(d, bits, R, nk)) return KVC_E_SHAPE;
     if (nk < ns) scoring = true;
   }
   if (scoring && (d.obs_window < 1 || g * d.obs_window > 256)) return KVC_E_SHAPE;
@@ -123,27 +177,38 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
   if (!c) return KVC_E_OOM;
   c->dims = d;
   c->g = g;
-  c->block_bytes = kvc::block_bytes(d.head_dim, d.bits == 16 ? 2 : d.bits);   // 16-bit: unused
-  if (cudaGetDevice(&c->device) != cudaSuccess) { delete c; return KVC_E_CUDA; }
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return KVC_E_CUDA;
+  }
   c->L.resize(d.n_layers);
-  size_t packed = 0;
+  size_t packed = 0, win = 0;
   for (int l = 0; l < d.n_layers; ++l) {
     LayerState& ls = c->L[l];
+    ls.bits = layer_bits ? layer_bits[l] : d.bits;
     ls.budget = kept_cap(d, budgets[l]);
-    ls.cap_groups = d.bits == 16 ? 0 :   // 16-bit storage: everything stays in the window
+    ls.R = ring_len(d, ls.bits, ls.budget);
+    ls.block_bytes = ls.bits == 16 ? 0 : kvc::block_bytes(d.head_dim, ls.bits);
+    ls.cap_groups = ls.bits == 16 ? 0 :   // 16-bit storage: everything stays in the window
                     ls.budget / KVC_GROUP +
                     (KVC_GROUP - 1 + d.obs_window + d.max_new_tokens + KVC_GROUP - 1) / KVC_GROUP + 1;
     ls.packed_off = packed;
-    packed += (size_t)units * ls.cap_groups * c->block_bytes;
+    packed += (size_t)units * ls.cap_groups * ls.block_bytes;
+    ls.win_off = win;
+    win += (size_t)units * ls.R * d.head_dim;
   }
   c->packed_bytes = packed;
-  c->win_elems = (size_t)d.n_layers * units * d.window_len * d.head_dim;
+  c->win_elems = win;
 
   c->packed = static_cast<uint8_t*>(dev_alloc(c, packed));
   c->win_k = static_cast<__nv_bfloat16*>(dev_alloc(c, c->win_elems * 2));
   c->win_v = static_cast<__nv_bfloat16*>(dev_alloc(c, c->win_elems * 2));
-  c->err = static_cast<unsigned*>(dev_alloc(c, 16));
-  bool ok = c->packed && c->win_k && c->win_v && c->err;
+  const bool err_ok = make_error_word(c);
+  c->dec_ws_floats = kvc::decode_workspace_floats(c->n_sm, g, d.head_dim);
+  c->dec_ws = static_cast<float*>(dev_alloc(c, c->dec_ws_floats * 4));
+  c->dec_cnt = static_cast<unsigned*>(dev_alloc(c, (size_t)d.n_layers * units * 4));
+  bool ok = c->packed && c->win_k && c->win_v && err_ok && c->dec_ws && c->dec_cnt;
   if (ok && scoring) {
     const int M = g * d.obs_window;
     c->stats_elems = (size_t)units * kvc::score_stat_chunks(d.prompt_len) * M;
@@ -172,7 +237,7 @@ kvc_status create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** out)
     // the window is zero-initialised: masked slots must hold finite values
     ok = cudaMemset(c->win_k, 0, c->win_elems * 2) == cudaSuccess &&
          cudaMemset(c->win_v, 0, c->win_elems * 2) == cudaSuccess &&
-         cudaMemset(c->err, 0, 16) == cudaSuccess &&
+         cudaMemset(c->dec_cnt, 0, (size_t)d.n_layers * units * 4) == cudaSuccess &&
          cudaDeviceSynchronize() == cudaSuccess;
   }
   if (!ok) {
@@ -194,7 +259,7 @@ kvc_status finish_prefill(kvc_cache* c, int layer, int n_kept, const int32_t* ke
   cudaError_t e = kvc::launch_gather_quant(c, layer, kept, n_kept, K, V, stream, sinks, kept_out);
   if (e != cudaSuccess) return from_cuda(e);
   LayerState& ls = c->L[layer];
-  const bool exact = c->dims.bits == 16;
+  const bool exact = ls.bits == 16;
   ls.n_kept = n_kept;
   ls.n_groups = exact ? 0 : n_kept / KVC_GROUP;
   ls.win_start = 0;
@@ -354,7 +419,14 @@ kvc_status kvc_plan_budgets_weighted(const kvc_dims* dims, int32_t avg_budget,
 kvc_status kvc_cache_create(const kvc_dims* dims, const int32_t* budgets, kvc_cache** cache) {
   if (!cache) return KVC_E_ARG;
   *cache = nullptr;
-  return create(dims, budgets, cache);
+  return create(dims, budgets, nullptr, cache);
+}
+
+kvc_status kvc_cache_create_layers(const kvc_dims* dims, const int32_t* budgets,
+                                   const int32_t* layer_bits, kvc_cache** cache) {
+  if (!cache || !layer_bits) return KVC_E_ARG;
+  *cache = nullptr;
+  return create(dims, budgets, layer_bits, cache);
 }
 
 kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets, int32_t layer,
@@ -362,7 +434,7 @@ kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets, in
                                 kvc_cache** cache, void* stream) {
   if (!cache || !dims) return KVC_E_ARG;
   if (*cache == nullptr) {
-    kvc_status st = create(dims, budgets, cache);
+    kvc_status st = create(dims, budgets, nullptr, cache);
     if (st != KVC_OK) return st;
   } else if (!same_dims((*cache)->dims, *dims)) {
     return KVC_E_SHAPE;
@@ -370,6 +442,7 @@ kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets, in
   kvc_cache* c = *cache;
   if (layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
   if (!k || !v) return KVC_E_ARG;
+  if (kvc_status pe = pending_error(c)) return pe;
   LayerState& ls = c->L[layer];
   if (ls.prefilled) return KVC_E_STATE;
   DeviceGuard dg(c->device);
@@ -397,12 +470,13 @@ kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets, in
 kvc_status kvc_prefill_acumul(kvc_cache* c, int32_t layer, const void* q_full, const void* k,
                               const void* v, void* stream) {
   if (!c || !k || !v) return KVC_E_ARG;
+  if (kvc_status pe = pending_error(c)) return pe;
   if (layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
   LayerState& ls = c->L[layer];
   if (ls.prefilled) return KVC_E_STATE;
   const int ns = c->dims.prompt_len - c->dims.obs_window;
   const int n_kept = ls.budget < ns ? ls.budget : ns;
-  if (!window_fits(c->dims, n_kept)) return KVC_E_SHAPE;
+  if (!window_fits(c->dims, ls.bits, ls.R, n_kept)) return KVC_E_SHAPE;
   const int g = c->dims.n_q_heads / c->dims.n_kv_heads;
   if (g > 16 || 128 % g != 0) return KVC_E_SHAPE;
   DeviceGuard dg(c->device);
@@ -426,12 +500,13 @@ kvc_status kvc_prefill_acumul(kvc_cache* c, int32_t layer, const void* q_full, c
 kvc_status kvc_prefill_sinks(kvc_cache* c, int32_t layer, int32_t n_sinks, const void* k,
                              const void* v, void* stream) {
   if (!c || !k || !v || n_sinks < 0) return KVC_E_ARG;
+  if (kvc_status pe = pending_error(c)) return pe;
   if (layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
   LayerState& ls = c->L[layer];
   if (ls.prefilled) return KVC_E_STATE;
   const int ns = c->dims.prompt_len - c->dims.obs_window;
   const int n_kept = ls.budget < ns ? ls.budget : ns;
-  if (!window_fits(c->dims, n_kept)) return KVC_E_SHAPE;
+  if (!window_fits(c->dims, ls.bits, ls.R, n_kept)) return KVC_E_SHAPE;
   DeviceGuard dg(c->device);
   if (!dg.ok) return KVC_E_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -452,13 +527,14 @@ kvc_status kvc_prefill_sinks(kvc_cache* c, int32_t layer, int32_t n_sinks, const
 kvc_status kvc_prefill_selected(kvc_cache* c, int32_t layer, const int32_t* kept, int32_t n_kept,
                                 const void* k, const void* v, void* stream) {
   if (!c || !k || !v || (!kept && n_kept > 0)) return KVC_E_ARG;
+  if (kvc_status pe = pending_error(c)) return pe;
   if (layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
   LayerState& ls = c->L[layer];
   if (ls.prefilled) return KVC_E_STATE;
   const int ns = c->dims.prompt_len - c->dims.obs_window;
   if (n_kept < 0 || n_kept > ns) return KVC_E_ARG;
   if (n_kept > ls.budget) return KVC_E_CAPACITY;
-  if (!window_fits(c->dims, n_kept)) return KVC_E_SHAPE;
+  if (!window_fits(c->dims, ls.bits, ls.R, n_kept)) return KVC_E_SHAPE;
   DeviceGuard dg(c->device);
   if (!dg.ok) return KVC_E_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -481,6 +557,7 @@ kvc_status kvc_prefill_selected(kvc_cache* c, int32_t layer, const int32_t* kept
 kvc_status kvc_append_layers(kvc_cache* c, int32_t layer_begin, int32_t layer_count,
                              const void* k_new, const void* v_new, void* stream) {
   if (!c || !k_new || !v_new) return KVC_E_ARG;
+  if (kvc_status pe = pending_error(c)) return pe;
   if (layer_count < 1 || layer_begin < 0 || layer_begin + layer_count > c->dims.n_layers)
     return KVC_E_ARG;
   for (int l = layer_begin; l < layer_begin + layer_count; ++l) {
@@ -489,10 +566,11 @@ kvc_status kvc_append_layers(kvc_cache* c, int32_t layer_begin, int32_t layer_co
   }
   DeviceGuard dg(c->device);
   if (!dg.ok) return KVC_E_CUDA;
-  const int R = c->dims.window_len;
   std::vector<int> flush(layer_count);
-  for (int i = 0; i < layer_count; ++i)   // 16-bit storage never flushes
-    flush[i] = c->dims.bits != 16 && c->L[layer_begin + i].win_len + 1 == R;
+  for (int i = 0; i < layer_count; ++i) {   // 16-bit storage never flushes
+    const LayerState& ls = c->L[layer_begin + i];
+    flush[i] = ls.bits != 16 && ls.win_len + 1 == ls.R;
+  }
   cudaError_t e = kvc::launch_append(c, layer_begin, layer_count,
                                      static_cast<const __nv_bfloat16*>(k_new),
                                      static_cast<const __nv_bfloat16*>(v_new), flush.data(),
@@ -504,7 +582,7 @@ kvc_status kvc_append_layers(kvc_cache* c, int32_t layer_begin, int32_t layer_co
     ls.appended += 1;
     if (flush[i]) {
       ls.n_groups += 1;
-      ls.win_start = (ls.win_start + KVC_GROUP) % R;
+      ls.win_start = (ls.win_start + KVC_GROUP) % ls.R;
       ls.win_len -= KVC_GROUP;
     }
   }
@@ -519,6 +597,9 @@ kvc_status kvc_append(kvc_cache* c, int32_t layer, const void* k_new, const void
 kvc_status kvc_decode_attn(kvc_cache* c, int32_t layer_begin, int32_t layer_count, const void* q,
                            float* out, void* stream) {
   if (!c || !q || !out) return KVC_E_ARG;
+  if (kvc_status pe = pending_error(c)) return pe;
+  // q is staged by bulk copies and out written in 16-byte vectors
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(out) % 16) return KVC_E_ARG;
   if (layer_count < 1 || layer_begin < 0 || layer_begin + layer_count > c->dims.n_layers)
     return KVC_E_ARG;
   for (int l = layer_begin; l < layer_begin + layer_count; ++l)
@@ -533,6 +614,9 @@ kvc_status kvc_decode_attn(kvc_cache* c, int32_t layer_begin, int32_t layer_coun
 kvc_status kvc_decode_step(kvc_cache* c, int32_t layer_begin, int32_t layer_count, const void* q,
                            const void* k_new, const void* v_new, float* out, void* stream) {
   if (!c || !q || !out || !k_new || !v_new) return KVC_E_ARG;
+  if (kvc_status pe = pending_error(c)) return pe;
+  // q is staged by bulk copies and out written in 16-byte vectors
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(out) % 16) return KVC_E_ARG;
   if (layer_count < 1 || layer_begin < 0 || layer_begin + layer_count > c->dims.n_layers)
     return KVC_E_ARG;
   for (int l = layer_begin; l < layer_begin + layer_count; ++l) {
@@ -541,10 +625,11 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t layer_begin, int32_t layer_coun
   }
   DeviceGuard dg(c->device);
   if (!dg.ok) return KVC_E_CUDA;
-  const int R = c->dims.window_len;
   std::vector<int> flush(layer_count);
-  for (int i = 0; i < layer_count; ++i)   // 16-bit storage never flushes
-    flush[i] = c->dims.bits != 16 && c->L[layer_begin + i].win_len + 1 == R;
+  for (int i = 0; i < layer_count; ++i) {   // 16-bit storage never flushes
+    const LayerState& ls = c->L[layer_begin + i];
+    flush[i] = ls.bits != 16 && ls.win_len + 1 == ls.R;
+  }
   // one launch: append (+ flush of the oldest group) and attention for every layer
   cudaError_t e = kvc::launch_decode_step(c, layer_begin, layer_count,
                                           static_cast<const __nv_bfloat16*>(q),
@@ -558,7 +643,7 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t layer_begin, int32_t layer_coun
     ls.appended += 1;
     if (flush[i]) {
       ls.n_groups += 1;
-      ls.win_start = (ls.win_start + KVC_GROUP) % R;
+      ls.win_start = (ls.win_start + KVC_GROUP) % ls.R;
       ls.win_len -= KVC_GROUP;
     }
   }
@@ -572,11 +657,23 @@ kvc_status kvc_check_device(kvc_cache* c, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned word = 0;
   if (cudaStreamSynchronize(s) != cudaSuccess) return KVC_E_CUDA;
+  if (c->err_host) {
+    word = *c->err_host;
+    *c->err_host = 0u;
+    return word == 0 ? KVC_OK : KVC_E_TIMEOUT;
+  }
   if (cudaMemcpy(&word, c->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
     return KVC_E_CUDA;
   if (word == 0) return KVC_OK;
   if (cudaMemset(c->err, 0, sizeof(word)) != cudaSuccess) return KVC_E_CUDA;
   return KVC_E_TIMEOUT;
+}
+
+kvc_status kvc_set_wait_limit(kvc_cache* c, int64_t polls) {
+  if (!c) return KVC_E_ARG;
+  c->wait_limit_set = polls >= 0;
+  c->wait_limit = polls >= 0 ? (unsigned)std::min<int64_t>(polls, 0xffffffffLL) : 0u;
+  return KVC_OK;
 }
 
 kvc_status kvc_free(kvc_cache* c) {
@@ -597,7 +694,9 @@ kvc_status kvc_layer_info_get(const kvc_cache* c, int32_t layer, kvc_layer_info*
   out->capacity_tokens = ls.cap_groups * KVC_GROUP;
   out->window_tokens = ls.win_len;
   out->appended = ls.appended;
-  out->packed_bytes = (int64_t)c->dims.batch * c->dims.n_kv_heads * ls.cap_groups * c->block_bytes;
+  out->packed_bytes = (int64_t)c->dims.batch * c->dims.n_kv_heads * ls.cap_groups * ls.block_bytes;
+  out->bits = ls.bits;
+  out->window_capacity = ls.R;
   return KVC_OK;
 }
 

@@ -8,29 +8,30 @@
 // A_unquant . R_V. Blog "KV Cache Compression: Eviction and Quantization",
 // "Measured on a real model": exact recent window, rounded rest, one softmax.
 //
-// Work decomposition (one persistent launch for a range of layers):
-//   unit = (layer, sequence b, kv head h); its work is cut into chunks of 16
-//   window slots or 1 packed group block. There is one CTA per SM; CTA i takes
-//   the units i, 2P-1-i, 2P+i, ... (P CTAs, snake order over units that come
-//   largest first) and lays their chunks end to end. When the CTA's units all fit
-//   in the query ring, warp w takes the w-th of NW contiguous runs of that list
-//   (a unit is split over as few warps as the balance allows, so few partial
-//   states are merged); otherwise warp w takes chunks w, w + NW, w + 2 NW, ...,
-//   which keeps the warps within a few units of each other (a unit's queries are
-//   issued only when the unit QR places before it has been merged). Each warp
-//   double-buffers its chunks in
-//   shared memory with bulk asynchronous copies (cp.async.bulk on per-slot
-//   mbarriers, bounded waits): the copy of its next-but-one chunk is issued as
-//   soon as a slot is read. A warp keeps an online softmax for the g query heads
-//   of its current unit and deposits it (m, l, o) in shared memory when it leaves
-//   the unit; the last warp to deposit merges the deposits with a log-sum-exp
-//   combine and writes the fp32 output. No state crosses CTAs and nothing waits
-//   on another CTA.
+// Work decomposition (one launch for a range of layers): a unit = (layer,
+//   sequence b, kv head h); its work is cut into chunks of 16 window slots or
+//   GPC packed group blocks (GPC = groups that fill one window chunk's bytes: 2 at
+//   2 bits, 1 at 4 bits). The chunks of every unit of the launch are laid end to
+//   end (layer by layer, unit by unit) and the list is cut into equal contiguous
+//   ranges, one per warp of the grid (one CTA per SM): a split-K over the whole
+//   launch, so a large unit is spread over many warps of many SMs and small units
+//   share a warp, and every warp gets the same number of chunks. Each warp
+//   double-buffers its chunks in shared memory with bulk asynchronous copies
+//   (cp.async.bulk on per-slot mbarriers, bounded waits); the copy of a unit's
+//   first chunk also brings the unit's g queries. A warp keeps an online softmax
+//   of the g query heads over the part of a unit it holds. A unit held whole by
+//   one warp is normalised and written by it; otherwise each holder writes its
+//   partial state (m, l, o) to a workspace in global memory and takes a ticket
+//   from the unit's arrival counter, and the holder that arrives last merges
+//   the partial states with a log-sum-exp combine in a fixed order (the result
+//   does not depend on arrival order), writes the fp32 output and resets the
+//   counter. Nothing waits on another warp or CTA.
 //   The new token of a fused step is stored into the ring by the warp whose
 //   window chunk holds its slot (which also patches its staged copy). A step in
 //   which some layer's window reaches R runs the append kernel first (it stores
 //   the new tokens and quantizes the oldest group of each full window) and then
-//   this kernel over the updated cache.
+//   this kernel over the updated cache. Layers of one launch may differ in
+//   precision (2 or 4 bits, or 16: window only) and in ring length.
 //
 // Arithmetic. Per 32-token group block the key logits are
 //     q . k_t = sum_c (q_c S_c) code_tc + sum_c q_c Z_c
@@ -56,44 +57,9 @@
 namespace kvc {
 namespace {
 
-constexpr int kGroupsPerWarp = kDecGroupsPerChunk;
 constexpr int kSlotsPerWarp = kDecSlotsPerChunk;
 static_assert(kSlotsPerWarp == 16, "window warps take 16 slots");
 constexpr unsigned kWaitLimit = 1u << 20;   // bounded mbarrier polls (far above any copy)
-static_assert(kGroupsPerWarp <= 8, "the key zero-point product covers at most 8 groups");
-
-struct DecLayer {
-  int n_groups;     // packed groups read from the store (a group flushed here excluded)
-  int win_start;    // ring start slot after this launch's append
-  int win_len;      // window tokens after this launch's append
-  int n_ctas;       // CTAs per unit
-  int cta_begin;    // first CTA of the layer in the grid
-  int cap_groups;
-  int new_slot;     // ring slot of the token appended in this launch, or -1
-  int flush_start;  // ring slot of the oldest token when this launch flushes a group, or -1
-  int wchunks;      // window chunks (16 slots) per unit; packed chunks (1 group) follow
-  int pchunks;      // packed chunks per unit
-  long long packed_off;
-};
-
-struct DecParams {
-  DecLayer L[KVC_MAX_LAUNCH_LAYERS];
-  const __nv_bfloat16* k_new;   // [n_layers][units][D] (fused append only)
-  const __nv_bfloat16* v_new;
-  unsigned* err;                // device error word (bit 0: a staging wait gave up)
-  int n_layers;                 // layers in this launch
-  int layer_begin;              // absolute index of L[0]
-  int units;                    // batch * n_kv_heads
-  int R;                        // window ring length
-  float sl2;                    // log2(e) / sqrt(head_dim)
-};
-
-template <int D, int BITS>
-constexpr int warp_buf_bytes() {
-  return kGroupsPerWarp * block_bytes(D, BITS) > kSlotsPerWarp * D * 4
-             ? kGroupsPerWarp * block_bytes(D, BITS)
-             : kSlotsPerWarp * D * 4;
-}
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
@@ -319,7 +285,7 @@ __device__ __forceinline__ void softmax_update(WarpState<D, GQ>& st,
 }
 
 // ------------------------------------------------------------ packed groups
-// `base` points at n_grp (<= kGroupsPerWarp) consecutive group blocks in shared
+// `base` points at n_grp (<= 8) consecutive group blocks in shared
 // memory. Per group: key logits (rows = tokens), one online-softmax update, the
 // value products (rows = channels). The group loop stays rolled so that the hot
 // code fits the instruction cache.
@@ -555,65 +521,74 @@ __device__ void window_warp(WarpState<D, GQ>& st, const __nv_bfloat16* qs, const
   }
 }
 
-// ----------------------------------------------------------- merge helpers
-// ----------------------------------------------------------- persistent layout
-// One CTA per SM. A CTA takes whole units (snake order over the launch's units,
-// which come largest first: layer 0 of a pyramid schedule holds the most groups)
-// and lays their chunks end to end; warp w takes chunks w, w + NW, w + 2 NW, ...
-// of that list, each staged by a bulk copy into one of its two ring slots (the
-// next one is in flight while the current one is computed). A warp deposits its
-// softmax state when it leaves a unit; the last warp to deposit merges the unit's
-// deposits in shared memory and writes the output. No state crosses CTAs.
-template <int D, int BITS, int GQ>
+// ------------------------------------------------------------ launch layout
+struct DecLayer {
+  long long chunk_begin;  // first chunk of the layer in the launch's chunk list
+  long long packed_off;   // byte offset of the layer inside the packed store
+  long long win_off;      // element offset of the layer's window rings
+  int n_groups;           // packed groups read (a group flushed in this step included)
+  int win_start;          // ring start slot after this launch's append
+  int win_len;            // window tokens after this launch's append
+  int cap_groups;
+  int new_slot;           // ring slot of the token appended in this launch, or -1
+  int wchunks;            // window chunks (16 slots) per unit; packed chunks follow
+  int pchunks;            // packed chunks per unit
+  int gpc;                // packed groups per chunk
+  int R;                  // ring length
+  int bits;               // 2, 4 or 16 (16: no packed chunks)
+};
+
+struct DecParams {
+  DecLayer L[KVC_MAX_LAUNCH_LAYERS];
+  const __nv_bfloat16* k_new;   // [n_layers][units][D] (fused append only)
+  const __nv_bfloat16* v_new;
+  unsigned* err;                // device error word (bit 0: a staging wait gave up)
+  float* ws;                    // partial states, two per CTA: [2 * grid][dep_floats]
+  unsigned* cnt;                // arrival tickets per (layer, unit) of the cache; zero between launches
+  long long total;              // chunks in the launch
+  int n_vwarps;                 // warps of the grid
+  int n_layers;                 // layers in this launch
+  int layer_begin;              // absolute index of L[0]
+  int units;                    // batch * n_kv_heads
+  unsigned wait_limit;          // polls of one staging wait before it gives up
+  float sl2;                    // log2(e) / sqrt(head_dim)
+};
+
+// One partial state in the workspace: o[GQ][D] (unnormalised; both column parts
+// and the value zero-point sums folded in), then m[GQ] (log2 units) and l[GQ],
+// padded to a whole number of 16-byte vectors so that every o starts aligned.
+__host__ __device__ constexpr int dep_floats(int D, int GQ) { return GQ * D + (2 * GQ + 3) / 4 * 4; }
+
+// BMASK: bit 0 = the launch has 2-bit layers, bit 1 = 4-bit layers (the packed
+// code of each present precision is instantiated; 16-bit layers need neither).
+template <int D, int GQ, int BMASK>
 struct DecCfg {
-  static constexpr int SLOT = warp_buf_bytes<D, BITS>();   // one chunk
-  static constexpr int DEPW = GQ * (D + 2);                // floats of one deposit: m, l, o
-  static constexpr int QB = GQ * D * 2;                    // bytes of one unit's queries
-  static constexpr int kQRing = 4;                         // query ring entries (<= 8)
-  // Two deposit buffers (by unit parity): a warp leaving unit k waits, before it
-  // deposits, for the merge of unit k - 2 (it may already compute unit k + 1).
-  static constexpr int NDEP = 2;
-  static constexpr int bytes(int nw) {
-    return nw * 2 * SLOT + NDEP * nw * DEPW * 4 + 16 + kQRing * QB + (2 * nw + kQRing) * 8 + 64;
-  }
-  static constexpr int pick(int nw) { return (nw <= 4 || bytes(nw) <= 224 * 1024) ? nw : pick(nw - 1); }
-  static constexpr int NW = pick(GQ > 4 ? 8 : 12);           // warps per CTA
-  static constexpr int kThreadsC = NW * 32;
-  // byte offsets inside dynamic shared memory
-  static constexpr int oRing = 0;
-  static constexpr int oDep = oRing + NW * 2 * SLOT;
-  static constexpr int oQ = (oDep + NDEP * NW * DEPW * 4 + 15) / 16 * 16;
-  static constexpr int oBars = oQ + kQRing * QB;
-  static constexpr int oCtl = oBars + (2 * NW + kQRing) * 8;
-  static constexpr int total = oCtl + 64;
-  static_assert(SLOT % 16 == 0 && DEPW % 1 == 0 && QB % 16 == 0, "alignment");
-  static_assert(oQ % 16 == 0 && oBars % 8 == 0, "alignment");
+  static constexpr int WB = kSlotsPerWarp * D * 4;   // one window chunk (keys + values)
+  static constexpr int PB2 = (BMASK & 1) ? dec_groups_per_chunk(D, 2) * block_bytes(D, 2) : 0;
+  static constexpr int PB4 = (BMASK & 2) ? dec_groups_per_chunk(D, 4) * block_bytes(D, 4) : 0;
+  static constexpr int SLOT = WB > PB2 ? (WB > PB4 ? WB : PB4) : (PB2 > PB4 ? PB2 : PB4);
+  static constexpr int QB = GQ * D * 2;              // one unit's queries (bf16)
+  static constexpr int DEPW = dep_floats(D, GQ);     // floats of one partial state
+  static constexpr int per_warp = 2 * SLOT + 2 * QB + 2 * DEPW * 4 + 2 * 8 + 4;
+  // warps per CTA: as many as shared memory holds, at most 12 (8 with eight query
+  // heads, whose state needs more registers per thread)
+  static constexpr int pick(int nw) { return nw * per_warp <= 227 * 1024 ? nw : pick(nw - 1); }
+  static constexpr int NW = pick(GQ > 4 ? 8 : 12);
+  static constexpr int kThreads = NW * 32;
+  static constexpr int oRing = 0;                    // [NW][2][SLOT]
+  static constexpr int oDep = oRing + NW * 2 * SLOT; // [NW][2][DEPW] fp32 partial states
+  static constexpr int oQ = oDep + NW * 2 * DEPW * 4;// [NW][2][GQ][D] bf16
+  static constexpr int oBars = oQ + NW * 2 * QB;     // [NW][2] mbarriers
+  static constexpr int oCnt = oBars + NW * 2 * 8;    // [NW] arrival tickets
+  static constexpr int total = oCnt + NW * 4;
+  static_assert(SLOT % 16 == 0 && QB % 16 == 0 && oDep % 16 == 0 && oBars % 8 == 0, "alignment");
+  static_assert(NW >= 4, "at least four warps per CTA");
 };
 
-// Control words of a CTA (shared memory): per unit parity, the number of deposits,
-// the mask of depositing warps and the number of merges done.
-struct DecCtl {
-  unsigned count[2];
-  unsigned mask[2];
-  unsigned gen[2];
-  int qunit[8];      // unit whose queries the ring entry was last issued for
-};
-static_assert(sizeof(DecCtl) <= 64, "control words fit their shared-memory region");
-
-// Unit k of CTA i (snake order): k even -> k*P + i, k odd -> (k+1)*P - 1 - i.
-__device__ __forceinline__ int snake_unit(int k, int i, int P) {
-  return (k & 1) ? (k + 1) * P - 1 - i : k * P + i;
-}
-
-// Write the warp's per-head state (both column parts and the value zero-point sums
-// folded in) as one deposit: m[GQ], l[GQ], o[GQ][D].
 template <int D, int GQ>
-__device__ void warp_deposit(WarpState<D, GQ>& st, float* dep, float sl2) {
+__device__ void write_partial(WarpState<D, GQ>& st, float* dep, float sl2) {
   constexpr int NH = n_tiles<GQ>();
   const int lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
-  float* dm = dep;
-  float* dl = dep + GQ;
-  float* dout = dep + 2 * GQ;
 #pragma unroll
   for (int u = 0; u < NH; ++u) {
     const int h = 4 * u + tid;
@@ -622,285 +597,365 @@ __device__ void warp_deposit(WarpState<D, GQ>& st, float* dep, float sl2) {
     l += __shfl_xor_sync(0xffffffffu, l, 8);
     l += __shfl_xor_sync(0xffffffffu, l, 16);
     if (h < GQ) {
+      float* o = dep + h * D;
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
-        dout[h * D + 16 * mt + gid] = st.o[u][mt][0] + st.o[u][mt][1];
-        dout[h * D + 16 * mt + gid + 8] = st.o[u][mt][2] + st.o[u][mt][3];
+        o[16 * mt + gid] = st.o[u][mt][0] + st.o[u][mt][1];
+        o[16 * mt + gid + 8] = st.o[u][mt][2] + st.o[u][mt][3];
       }
       if (gid == 0) {
-        dm[h] = st.m[u] == -INFINITY ? -INFINITY : st.m[u] * sl2;
-        dl[h] = l;
+        dep[GQ * D + h] = st.m[u] == -INFINITY ? -INFINITY : st.m[u] * sl2;
+        dep[GQ * D + GQ + h] = l;
       }
     }
   }
 }
 
-// One warp merges the deposits of the warps in `mask` (log-sum-exp combine) and
-// writes o[GQ][D] (fp32). The weight of each (warp, head) replaces its m slot.
-template <int D, int GQ, int NW>
-__device__ void merge_deposits(float* dep, unsigned mask, float* __restrict__ o) {
-  constexpr int DEPW = GQ * (D + 2);
-  constexpr int NWH = (NW * GQ + 31) / 32;
-  const int lane = threadIdx.x & 31;
-  float f[NWH];
+// The warp's state normalised (o / l per head) into out[GQ][D].
+template <int D, int GQ>
+__device__ void write_final(WarpState<D, GQ>& st, float* __restrict__ out) {
+  constexpr int NH = n_tiles<GQ>();
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
 #pragma unroll
-  for (int i = 0; i < NWH; ++i) {
-    const int idx = lane + 32 * i, w = idx / GQ, h = idx % GQ;
-    f[i] = 0.f;
-    if (idx < NW * GQ && (mask >> w & 1u) && dep[w * DEPW + GQ + h] > 0.f) {
-      float M = -INFINITY;
-      for (int v = 0; v < NW; ++v)
-        if (mask >> v & 1u) M = fmaxf(M, dep[v * DEPW + h]);
-      f[i] = exp2f(dep[w * DEPW + h] - M);
+  for (int u = 0; u < NH; ++u) {
+    const int h = 4 * u + tid;
+    float l = st.l[u];
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    if (h < GQ) {
+      float* o = out + h * D;
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        o[16 * mt + gid] = (st.o[u][mt][0] + st.o[u][mt][1]) * inv;
+        o[16 * mt + gid + 8] = (st.o[u][mt][2] + st.o[u][mt][3]) * inv;
+      }
     }
-  }
-  __syncwarp();
-#pragma unroll
-  for (int i = 0; i < NWH; ++i) {
-    const int idx = lane + 32 * i, w = idx / GQ, h = idx % GQ;
-    if (idx < NW * GQ) dep[w * DEPW + h] = f[i];   // unused warps get weight 0
-  }
-  __syncwarp();
-  // lane h < GQ sums head h's weighted l over the deposits; the sums are shuffled out
-  float Lh_lane = 0.f;
-  if (lane < GQ)
-    for (int w = 0; w < NW; ++w)
-      if (mask >> w & 1u) Lh_lane += dep[w * DEPW + lane] * dep[w * DEPW + GQ + lane];
-  float L[GQ];
-#pragma unroll
-  for (int h = 0; h < GQ; ++h) L[h] = __shfl_sync(0xffffffffu, Lh_lane, h);
-  // each lane owns E outputs; the deposits are walked in the outer loop so the E
-  // accumulations are independent (their shared-memory loads overlap)
-  constexpr int E = GQ * D / 32;
-  float acc[E];
-#pragma unroll
-  for (int i = 0; i < E; ++i) acc[i] = 0.f;
-  for (int w = 0; w < NW; ++w) {
-    if (!(mask >> w & 1u)) continue;
-    const float* dw = dep + w * DEPW;
-#pragma unroll
-    for (int i = 0; i < E; ++i) {
-      const int e = lane + 32 * i;
-      acc[i] += dw[e / D] * dw[2 * GQ + e];
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < E; ++i) {
-    const int e = lane + 32 * i, h = e / D;
-    float Lh = 0.f;
-#pragma unroll
-    for (int hh = 0; hh < GQ; ++hh) Lh = hh == h ? L[hh] : Lh;
-    o[e] = Lh > 0.f ? acc[i] / Lh : 0.f;
   }
 }
 
-template <int D, int BITS, int GQ>
-__global__ void __launch_bounds__(DecCfg<D, BITS, GQ>::kThreadsC, 1)
+template <bool GLOBAL>
+__device__ __forceinline__ float ld_dep(const float* p) {
+  if constexpr (GLOBAL) return __ldcg(p);
+  else return *p;
+}
+template <bool GLOBAL>
+__device__ __forceinline__ float4 ld_dep4(const float4* p) {
+  if constexpr (GLOBAL) return __ldcg(p);
+  else return *p;
+}
+
+// Log-sum-exp combine of the partial states dep_of(0 .. nc-1), in that order (the
+// result does not depend on which holder arrived last). GLOBAL: the partials were
+// written by other SMs and are read through L2; else they are in this CTA's
+// shared memory. NORMALISE: out[GQ][D] = o / l; else out is written as one
+// partial state (o, m, l) of the whole set. The maxima and weights are taken with
+// the lanes spread over the contributors; the outputs then loop over the
+// contributors with loads that do not depend on each other.
+template <int D, int GQ, bool GLOBAL, bool NORMALISE, typename DepOf>
+__device__ void merge_partials(int nc, DepOf dep_of, float* __restrict__ out) {
+  constexpr int N4 = GQ * D / 4;            // float4 outputs
+  constexpr int E4 = (N4 + 31) / 32;        // per lane
+  const int lane = threadIdx.x & 31;
+  float M[GQ];
+#pragma unroll
+  for (int h = 0; h < GQ; ++h) M[h] = -INFINITY;
+  for (int w0 = 0; w0 < nc; w0 += 32) {
+    if (w0 + lane < nc) {
+      const float* d = dep_of(w0 + lane) + GQ * D;
+#pragma unroll
+      for (int h = 0; h < GQ; ++h)
+        if (ld_dep<GLOBAL>(d + GQ + h) > 0.f) M[h] = fmaxf(M[h], ld_dep<GLOBAL>(d + h));
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < GQ; ++h)
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], o));
+  float4 acc[E4];
+  float L[GQ];
+#pragma unroll
+  for (int i = 0; i < E4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int h = 0; h < GQ; ++h) L[h] = 0.f;
+  // lane element i covers outputs 4 (lane + 32 i) .. + 3 (one head)
+  for (int w0 = 0; w0 < nc; w0 += 32) {
+    float f[GQ];
+    if (w0 + lane < nc) {
+      const float* d = dep_of(w0 + lane) + GQ * D;
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) {
+        const float l = ld_dep<GLOBAL>(d + GQ + h);
+        f[h] = l > 0.f ? exp2f(ld_dep<GLOBAL>(d + h) - M[h]) : 0.f;
+        L[h] += f[h] * l;
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) f[h] = 0.f;
+    }
+    const int cnt = min(32, nc - w0);
+#pragma unroll 4
+    for (int k = 0; k < cnt; ++k) {
+      const float4* o4 = reinterpret_cast<const float4*>(dep_of(w0 + k));
+      float fk[GQ];
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) fk[h] = __shfl_sync(0xffffffffu, f[h], k);
+#pragma unroll
+      for (int i = 0; i < E4; ++i) {
+        const int idx = lane + 32 * i;
+        if (idx < N4) {
+          const float4 v = ld_dep4<GLOBAL>(o4 + idx);
+          const float fh = fk[(4 * idx) / D];
+          acc[i].x += fh * v.x; acc[i].y += fh * v.y; acc[i].z += fh * v.z; acc[i].w += fh * v.w;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < GQ; ++h)
+#pragma unroll
+    for (int o = 16; o; o >>= 1) L[h] += __shfl_xor_sync(0xffffffffu, L[h], o);
+  float4* out4 = reinterpret_cast<float4*>(out);
+#pragma unroll
+  for (int i = 0; i < E4; ++i) {
+    const int idx = lane + 32 * i;
+    if (idx < N4) {
+      float inv = 1.f;
+      if constexpr (NORMALISE) {
+        const int h = (4 * idx) / D;
+        inv = L[h] > 0.f ? 1.f / L[h] : 0.f;
+      }
+      out4[idx] = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
+    }
+  }
+  if constexpr (!NORMALISE) {
+    if (lane < GQ) {
+      float m = -INFINITY, l = 0.f;
+#pragma unroll
+      for (int h = 0; h < GQ; ++h)
+        if (h == lane) { m = M[h]; l = L[h]; }
+      out[GQ * D + lane] = m;
+      out[GQ * D + GQ + lane] = l;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" :: "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+               :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// An even split of [0, T) into N contiguous ranges: range i is [first(i), first(i+1)),
+// and owner(c) is the range holding c.
+struct Split {
+  long long T, N, base;
+  __device__ long long first(long long i) const { return base + i * T / N; }
+  __device__ long long owner(long long c) const { return ((c - base + 1) * N - 1) / T; }
+};
+
+template <int D, int GQ, int BMASK>
+__global__ void __launch_bounds__(DecCfg<D, GQ, BMASK>::kThreads, 1)
 decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __restrict__ win_k,
               __nv_bfloat16* __restrict__ win_v, const __nv_bfloat16* __restrict__ q,
               float* __restrict__ out) {
-  using C = DecCfg<D, BITS, GQ>;
-  constexpr int NW = C::NW, BB = block_bytes(D, BITS), QR = C::kQRing;
+  using C = DecCfg<D, GQ, BMASK>;
+  constexpr int NW = C::NW;
   extern __shared__ __align__(128) uint8_t dsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint64_t* cbar = reinterpret_cast<uint64_t*>(dsm + C::oBars);   // [NW][2] chunk slots
-  uint64_t* qbar = cbar + 2 * NW;                                 // [QR] query ring
-  DecCtl& ctl = *reinterpret_cast<DecCtl*>(dsm + C::oCtl);
-  // layer table read in place from the launch parameters, each read warp-uniform (a
-  // per-thread copy into shared memory made the constant cache serialise)
-  const DecLayer* lay = P.L;
-  __nv_bfloat16* qring = reinterpret_cast<__nv_bfloat16*>(dsm + C::oQ);
-  const int P_ = gridDim.x, cta = blockIdx.x;
-  const int total_units = P.n_layers * P.units;
-
-  // the CTA's units: k = 0, 1, ... while snake_unit(k) < total_units
-  auto unit_of = [&](int k) { return snake_unit(k, cta, P_); };
-  auto chunks_of = [&](int g) { const DecLayer& L = lay[g / P.units]; return L.wchunks + L.pchunks; };
-  auto q_copy = [&](int k) {   // queries of the CTA's unit k into ring entry k % QR
-    const int g = unit_of(k);
-    if (g >= total_units) return;
-    uint64_t* b = &qbar[k % QR];
-    *reinterpret_cast<volatile int*>(&ctl.qunit[k % QR]) = k;
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
-                 :: "r"(smem_u32(b)), "r"((uint32_t)C::QB) : "memory");
-    bulk_g2s(qring + (k % QR) * GQ * D, q + (size_t)g * GQ * D, (uint32_t)C::QB, b);
-  };
-  // barriers and control words, then the first units' queries
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 2 * NW + QR; ++i)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" :: "r"(smem_u32(&cbar[i])) : "memory");
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dsm + C::oBars) + warp * 2;
+  uint8_t* ring = dsm + C::oRing + (size_t)warp * 2 * C::SLOT;
+  float* sdep = reinterpret_cast<float*>(dsm + C::oDep);           // [NW][2][DEPW]
+  unsigned* scnt = reinterpret_cast<unsigned*>(dsm + C::oCnt);     // [NW]
+  __nv_bfloat16* qbuf = reinterpret_cast<__nv_bfloat16*>(dsm + C::oQ) + (size_t)warp * 2 * GQ * D;
+  if (lane == 0) {
+    mbar_init(&bar[0]);
+    mbar_init(&bar[1]);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    for (int p = 0; p < 2; ++p) { ctl.count[p] = 0u; ctl.mask[p] = 0u; ctl.gen[p] = 0u; }
-    for (int e = 0; e < 8; ++e) ctl.qunit[e] = -1;
+    scnt[warp] = 0u;
   }
+  __syncthreads();
   pdl_wait();      // the previous kernels' writes (queries, cache) are visible
   pdl_release();
-  if (threadIdx.x == 0)
-    for (int k = 0; k < QR; ++k) q_copy(k);
-  __syncthreads();
+  // the launch's chunk list, cut into one contiguous range per CTA, each cut into one
+  // contiguous range per warp
+  const Split cs{P.total, (long long)gridDim.x, 0};
+  const long long C0 = cs.first(blockIdx.x), C1 = cs.first(blockIdx.x + 1);
+  const int nvw = (int)(C1 - C0 < NW ? C1 - C0 : NW);   // warps with chunks (>= 1: grid <= total)
+  if (warp >= nvw) return;
+  const Split ws{C1 - C0, (long long)nvw, C0};
+  const long long c0 = ws.first(warp), c1 = ws.first(warp + 1);
+  const int n = (int)(c1 - c0);   // >= 1
 
-  // this warp's chunk stream: positions w, w + NW, ... of the CTA's chunk list
-  struct Cursor { int k, base, g, n; };   // unit k of the CTA, first list position, unit, chunks
-  auto advance = [&](Cursor& c, int pos) {   // move c to the unit holding list position pos
-    while (c.g < total_units && pos >= c.base + c.n) {
-      c.base += c.n;
-      ++c.k;
-      c.g = unit_of(c.k);
-      c.n = c.g < total_units ? chunks_of(c.g) : 0;
-    }
-    return c.g < total_units;
+  // chunk cursor: layer, unit, chunk index j inside the unit, chunks per unit
+  struct Cur { int li, unit, j, cpu; };
+  auto cpu_of = [&](int li) { return P.L[li].wchunks + P.L[li].pchunks; };
+  auto locate = [&](long long c) {
+    Cur r;
+    r.li = 0;
+    while (r.li + 1 < P.n_layers && c >= P.L[r.li + 1].chunk_begin) ++r.li;
+    r.cpu = cpu_of(r.li);
+    const long long loc = c - P.L[r.li].chunk_begin;
+    r.unit = (int)(loc / r.cpu);
+    r.j = (int)(loc - (long long)r.unit * r.cpu);
+    return r;
   };
-  auto issue = [&](int slot, const Cursor& c, int pos) {   // lane 0: stage chunk pos - base of unit c.g
-    const DecLayer& L = lay[c.g / P.units];
-    const int unit = c.g % P.units, j = pos - c.base;
-    uint64_t* b = &cbar[warp * 2 + slot];
-    uint8_t* dst = dsm + C::oRing + (warp * 2 + slot) * C::SLOT;
-    if (j < L.wchunks) {
-      const size_t wunit = (size_t)(P.layer_begin + c.g / P.units) * P.units + unit;
-      const int slot0 = (L.win_start + j * kSlotsPerWarp) % P.R;
+  auto step = [&](Cur& r) {
+    if (++r.j < r.cpu) return;
+    r.j = 0;
+    if (++r.unit < P.units) return;
+    r.unit = 0;
+    do { ++r.li; } while (r.li < P.n_layers && cpu_of(r.li) == 0);
+    r.cpu = r.li < P.n_layers ? cpu_of(r.li) : 1;
+  };
+  // lane 0: stage chunk i (cursor r) into slot i & 1, with the unit's queries into
+  // qbuf[qpar] when the chunk starts one of the warp's unit segments
+  auto issue = [&](int i, const Cur& r, int qpar, bool with_q) {
+    const DecLayer& L = P.L[r.li];
+    uint64_t* b = &bar[i & 1];
+    uint8_t* dst = ring + (i & 1) * C::SLOT;
+    const uint32_t qb = with_q ? (uint32_t)C::QB : 0u;
+    if (r.j < L.wchunks) {
+      const size_t rb = (size_t)L.win_off + (size_t)r.unit * L.R * D;
+      const int slot0 = (L.win_start + r.j * kSlotsPerWarp) % L.R;
       const uint32_t wb = (uint32_t)(kSlotsPerWarp * D * 2);
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
-                   :: "r"(smem_u32(b)), "r"(2 * wb) : "memory");
-      bulk_g2s(dst, win_k + (wunit * P.R + slot0) * D, wb, b);
-      bulk_g2s(dst + wb, win_v + wunit * P.R * D + (size_t)(slot0 >> 1) * D * 2, wb, b);
+      mbar_expect(b, 2 * wb + qb);
+      bulk_g2s(dst, win_k + rb + (size_t)slot0 * D, wb, b);
+      bulk_g2s(dst + wb, win_v + rb + (size_t)(slot0 >> 1) * D * 2, wb, b);
     } else {
-      const int g0 = (j - L.wchunks) * kGroupsPerWarp;
-      const int ng = min(kGroupsPerWarp, L.n_groups - g0);
-      const uint8_t* src = packed + L.packed_off + ((size_t)unit * L.cap_groups + g0) * BB;
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
-                   :: "r"(smem_u32(b)), "r"((uint32_t)(ng * BB)) : "memory");
-      bulk_g2s(dst, src, (uint32_t)(ng * BB), b);
+      const int bb = block_bytes(D, L.bits);
+      const int g0 = (r.j - L.wchunks) * L.gpc;
+      const int ng = min(L.gpc, L.n_groups - g0);
+      const uint8_t* src = packed + L.packed_off + ((size_t)r.unit * L.cap_groups + g0) * bb;
+      mbar_expect(b, (uint32_t)(ng * bb) + qb);
+      bulk_g2s(dst, src, (uint32_t)(ng * bb), b);
+    }
+    if (with_q)
+      bulk_g2s(qbuf + qpar * GQ * D, q + ((size_t)r.li * P.units + r.unit) * GQ * D, qb, b);
+  };
+
+  Cur cur = locate(c0), pre = cur;
+  int pre_seg = 0;   // segment ordinal of the prefetch cursor's chunk
+  auto produce = [&](int i) {   // all lanes: advance the prefetch cursor to chunk i; lane 0 issues
+    if (i > 0) {
+      step(pre);
+      if (pre.j == 0) ++pre_seg;
+    }
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      issue(i, pre, pre_seg & 1, i == 0 || pre.j == 0);
     }
   };
-
-  // chunk list positions of this warp: a contiguous run when the CTA's units all
-  // fit in the query ring, else every NW-th position (-1: none left)
-  int n_units = 0, total = 0;
-  for (int k = 0; unit_of(k) < total_units; ++k) { ++n_units; total += chunks_of(unit_of(k)); }
-  const bool blocked = n_units <= QR;
-  const int per = (total + NW - 1) / NW;
-  const int w0 = min(total, warp * per), w1 = min(total, w0 + per);
-  auto position = [&](int n) -> int {
-    if (blocked) return w0 + n < w1 ? w0 + n : -1;
-    return warp + n * NW;   // past the list: advance() fails
-  };
-
-  Cursor cur{0, 0, unit_of(0), 0};
-  cur.n = cur.g < total_units ? chunks_of(cur.g) : 0;
-  Cursor pre = cur;   // cursor of the prefetch stream (runs two chunks ahead)
-  // prime the two slots
-  for (int s = 0; s < 2; ++s) {
-    const int pos = position(s);
-    if (pos >= 0 && advance(pre, pos) && lane == 0) issue(s, pre, pos);
-  }
+  produce(0);
+  if (n > 1) produce(1);
 
   WarpState<D, GQ> st;
   QRegs<D, GQ> qr;
-  int k_cur = -1, base_cur = 0;   // the warp's current unit and its first list position
-  bool ok = true;
-  const int units_per_layer = P.units;
-
-  auto deposit = [&](int k, int base) {   // hand over unit k's state; the last depositor merges
-    const int par = k % C::NDEP;
-    const int g = unit_of(k);
-    // depositors: the warps whose positions meet the unit's [base, base + chunks)
-    const unsigned expect = blocked ? (unsigned)((base + chunks_of(g) - 1) / per - base / per + 1)
-                                    : (unsigned)min(NW, chunks_of(g));
-    // the deposit buffer of unit k is free once unit k - NDEP is merged
-    if (lane == 0) {
-      bool ready = false;
-      for (unsigned it = 0; it < kWaitLimit && !ready; ++it)
-        ready = *reinterpret_cast<volatile unsigned*>(&ctl.gen[par]) == (unsigned)(k / C::NDEP);
-      if (!ready) { atomicOr(P.err, 2u); ok = false; }
+  int seg = -1;
+  int fail = -1;   // chunk whose staging wait gave up
+  // A segment = the chunks of one unit this warp holds. At its end the unit is
+  // written whole; or its partial state goes to this CTA's shared memory, where the
+  // last of the CTA's holders merges them; a unit that other CTAs also hold is
+  // handed on as the CTA's partial state in global memory, where the last CTA
+  // merges them. Tickets come from arrival counters (shared, then global); nothing
+  // waits.
+  auto finish = [&](const Cur& r, int seg_ord, bool failed) {
+    const DecLayer& L = P.L[r.li];
+    const long long ubeg = L.chunk_begin + (long long)r.unit * r.cpu, uend = ubeg + r.cpu;
+    const size_t ul = (size_t)r.li * P.units + r.unit;
+    float* o = out + ul * GQ * D;
+    if (ubeg >= c0 && uend <= c1) {
+      if (!failed) write_final<D, GQ>(st, o);
+      return;
     }
-    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
-    if (!ok) return;
-    float* dep = reinterpret_cast<float*>(dsm + C::oDep) + (par * NW) * C::DEPW;
-    warp_deposit<D, GQ>(st, dep + warp * C::DEPW, P.sl2);
-    __syncwarp();
-    unsigned last = 0;
-    if (lane == 0) {
+    const long long lbeg = max(ubeg, C0), lend = min(uend, C1);   // the CTA's part
+    const bool cta_whole = ubeg >= C0 && uend <= C1;
+    const int wa = (int)ws.owner(lbeg), wb = (int)ws.owner(lend - 1);
+    // this CTA's state of a unit that other CTAs also hold goes to global memory
+    const int cslot = lbeg == C0 ? 0 : 1;
+    float* gdep = P.ws + ((size_t)blockIdx.x * 2 + cslot) * C::DEPW;
+    if (wb > wa) {
+      // several holders in this CTA: partial state to shared memory, CTA ticket
+      float* mine = sdep + ((size_t)warp * 2 + (seg_ord == 0 ? 0 : 1)) * C::DEPW;
+      if (!failed) write_partial<D, GQ>(st, mine, P.sl2);
       __threadfence_block();
-      atomicOr(&ctl.mask[par], 1u << warp);
-      last = atomicAdd(&ctl.count[par], 1u) == expect - 1u;
+      __syncwarp();
+      unsigned last = 0;
+      if (lane == 0) last = atomicAdd(&scnt[wa], 1u) == (unsigned)(wb - wa);
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) return;
+      __threadfence_block();
+      const bool wa_late = ws.first(wa) < lbeg;   // its segment is its last one
+      auto sdep_of = [&](int k) -> const float* {
+        return sdep + ((size_t)(wa + k) * 2 + ((k == 0 && wa_late) ? 1 : 0)) * C::DEPW;
+      };
+      if (lane == 0) scnt[wa] = 0u;
+      if (cta_whole) {
+        if (!failed) merge_partials<D, GQ, false, true>(wb - wa + 1, sdep_of, o);
+        return;
+      }
+      if (!failed) merge_partials<D, GQ, false, false>(wb - wa + 1, sdep_of, gdep);
+    } else if (!failed) {
+      write_partial<D, GQ>(st, gdep, P.sl2);
     }
+    __threadfence();
+    __syncwarp();
+    const long long ca = cs.owner(ubeg), cb = cs.owner(uend - 1);
+    unsigned* cnt = P.cnt + (size_t)(P.layer_begin + r.li) * P.units + r.unit;
+    unsigned last = 0;
+    if (lane == 0) last = atomicAdd(cnt, 1u) == (unsigned)(cb - ca);
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
-    __threadfence_block();
-    const unsigned mask = *reinterpret_cast<volatile unsigned*>(&ctl.mask[par]);
-    const int li = g / units_per_layer, unit = g % units_per_layer;
-    merge_deposits<D, GQ, NW>(dep, mask, out + ((size_t)li * units_per_layer + unit) * GQ * D);
+    __threadfence();
+    const bool ca_late = cs.first(ca) < ubeg;   // the first CTA's segment is its last one
+    if (!failed)
+      merge_partials<D, GQ, true, true>((int)(cb - ca + 1), [&](int k) -> const float* {
+        return P.ws + ((size_t)(ca + k) * 2 + ((k == 0 && ca_late) ? 1 : 0)) * C::DEPW;
+      }, o);
     __syncwarp();
-    if (lane == 0) {
-      ctl.count[par] = 0u;
-      ctl.mask[par] = 0u;
-      // the query entry of unit k is free: fetch unit k + QR
-      q_copy(k + QR);
-      __threadfence_block();
-      atomicAdd(&ctl.gen[par], 1u);
-    }
+    if (lane == 0) *cnt = 0u;   // ready for the next launch
   };
 
-  for (int n = 0;; ++n) {
-    const int pos = position(n);
-    if (pos < 0 || !advance(cur, pos)) break;
-    const int slot = n & 1;
-    if (cur.k != k_cur) {
-      if (k_cur >= 0) deposit(k_cur, base_cur);
-      if (!ok) break;
-      k_cur = cur.k;
-      base_cur = cur.base;
+  for (int i = 0; i < n; ++i) {
+    if (i > 0) step(cur);
+    const bool seg_start = i == 0 || cur.j == 0;
+    if (seg_start) {
+      ++seg;
       state_init(st);
-      // this unit's queries: the ring entry must hold this unit's copy (issued once
-      // the unit QR places before it is merged, so the entry's mbarrier is at most
-      // one phase behind), then a bounded wait for that copy
-      bool done = false;
-      for (unsigned it = 0; it < kWaitLimit && !done; ++it)
-        done = *reinterpret_cast<volatile int*>(&ctl.qunit[k_cur % QR]) == k_cur;
-      const uint32_t qpar = (uint32_t)((k_cur / QR) & 1);
-      if (done) {
-        done = false;
-        for (unsigned it = 0; it < kWaitLimit && !done; ++it)
-          done = mbar_try_wait(&qbar[k_cur % QR], qpar);
-      }
-      if (!__all_sync(0xffffffffu, done)) { if (lane == 0) atomicOr(P.err, 1u); ok = false; break; }
-      load_qregs<D, GQ>(qr, qring + (k_cur % QR) * GQ * D);
     }
-    // wait for the chunk
+    // wait for the chunk (and, at a segment start, the unit's queries)
+    const uint32_t par = (uint32_t)((i >> 1) & 1);
     bool done = false;
-    uint64_t* b = &cbar[warp * 2 + slot];
-    const uint32_t par = (uint32_t)((n >> 1) & 1);
-    for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(b, par);
-    if (!done) {
+    for (unsigned it = 0; it < P.wait_limit && !done; ++it) done = mbar_try_wait(&bar[i & 1], par);
+    if (!__all_sync(0xffffffffu, done)) {
       if (lane == 0) atomicOr(P.err, 1u);
-      for (unsigned it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(b, par);
-      ok = false;
+      fail = i;
       break;
     }
-    __syncwarp();
-    const DecLayer& L = lay[cur.g / P.units];
-    const int unit = cur.g % P.units, j = pos - cur.base;
-    uint8_t* sbuf = dsm + C::oRing + (warp * 2 + slot) * C::SLOT;
-    const __nv_bfloat16* qs = qring + (k_cur % QR) * GQ * D;
-    if (j < L.wchunks) {
+    const DecLayer& L = P.L[cur.li];
+    const __nv_bfloat16* qs = qbuf + (seg & 1) * GQ * D;
+    if (seg_start) load_qregs<D, GQ>(qr, qs);
+    uint8_t* sbuf = ring + (i & 1) * C::SLOT;
+    if (cur.j < L.wchunks) {
       __nv_bfloat16* sk = reinterpret_cast<__nv_bfloat16*>(sbuf);
       uint32_t* sv = reinterpret_cast<uint32_t*>(sbuf + kSlotsPerWarp * D * 2);
-      const int pos0 = j * kSlotsPerWarp;
+      const int pos0 = cur.j * kSlotsPerWarp;
       const int n_valid = min(kSlotsPerWarp, L.win_len - pos0);
-      if (L.new_slot >= 0 && j == (L.win_len - 1) / kSlotsPerWarp) {
+      if (L.new_slot >= 0 && cur.j == (L.win_len - 1) / kSlotsPerWarp) {
         // the step's new token: store it into the ring (later steps read it) and
         // patch the staged copy (the bulk copy may predate the store)
-        const int li = cur.g / P.units;
-        const size_t wunit = (size_t)(P.layer_begin + li) * P.units + unit;
-        const __nv_bfloat16* kn = P.k_new + ((size_t)li * P.units + unit) * D;
-        const __nv_bfloat16* vn = P.v_new + ((size_t)li * P.units + unit) * D;
-        const int slot0 = (L.win_start + pos0) % P.R;
-        const int r = L.new_slot - slot0;
+        const size_t ul = (size_t)cur.li * P.units + cur.unit;
+        const size_t rb = (size_t)L.win_off + (size_t)cur.unit * L.R * D;
+        const __nv_bfloat16* kn = P.k_new + ul * D;
+        const __nv_bfloat16* vn = P.v_new + ul * D;
+        const int r = L.new_slot - (L.win_start + pos0) % L.R;
         __nv_bfloat16* svh = reinterpret_cast<__nv_bfloat16*>(sv);
         for (int c = lane; c < D; c += 32) {
           const __nv_bfloat16 kv = kn[c], vv = vn[c];
-          window_store(win_k + wunit * P.R * D, win_v + wunit * P.R * D, L.new_slot, c, D, kv, vv);
+          window_store(win_k + rb, win_v + rb, L.new_slot, c, D, kv, vv);
           sk[win_k_index(r, c, D)] = kv;
           svh[win_v_index(r, c, D)] = vv;
         }
@@ -908,60 +963,68 @@ decode_kernel(const DecParams P, uint8_t* __restrict__ packed, __nv_bfloat16* __
       }
       window_warp<D, GQ>(st, qs, sk, sv, n_valid, P.sl2);
     } else {
-      const int g0 = (j - L.wchunks) * kGroupsPerWarp;
-      packed_warp<D, BITS, GQ>(st, qr, sbuf, min(kGroupsPerWarp, L.n_groups - g0), P.sl2);
+      const int g0 = (cur.j - L.wchunks) * L.gpc;
+      const int ng = min(L.gpc, L.n_groups - g0);
+      if constexpr (BMASK == 1) {
+        packed_warp<D, 2, GQ>(st, qr, sbuf, ng, P.sl2);
+      } else if constexpr (BMASK == 2) {
+        packed_warp<D, 4, GQ>(st, qr, sbuf, ng, P.sl2);
+      } else {
+        if (L.bits == 2) packed_warp<D, 2, GQ>(st, qr, sbuf, ng, P.sl2);
+        else packed_warp<D, 4, GQ>(st, qr, sbuf, ng, P.sl2);
+      }
     }
-    __syncwarp();   // the slot is read: refill it with the chunk two steps ahead
-    const int npos = position(n + 2);
-    if (npos >= 0 && advance(pre, npos) && lane == 0) {
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      issue(slot, pre, npos);
-    }
+    __syncwarp();   // the slot is read: refill it with the chunk two ahead
+    if (i + 2 < n) produce(i + 2);
+    if (i == n - 1 || cur.j == cur.cpu - 1) finish(cur, seg, false);
   }
-  if (ok && k_cur >= 0) deposit(k_cur, base_cur);
+  if (fail >= 0) {
+    // let the copies in flight land (chunk fail and the one after it), then hand
+    // over the split units left open so every counter still returns to zero
+    for (int i = fail; i < n && i <= fail + 1; ++i) {
+      bool done = false;
+      for (unsigned it = 0; it < kWaitLimit && !done; ++it)
+        done = mbar_try_wait(&bar[i & 1], (uint32_t)((i >> 1) & 1));
+    }
+    __syncwarp();
+    finish(cur, seg, true);
+    const Cur last = locate(c1 - 1);
+    if (last.li != cur.li || last.unit != cur.unit) finish(last, seg + 1, true);
+  }
 }
 
-template <int D, int BITS, int GQ>
-cudaError_t launch_one(const DecParams& P, const kvc_cache* c, const __nv_bfloat16* q, float* out,
+template <int D, int GQ, int BMASK>
+cudaError_t launch_one(DecParams& P, const kvc_cache* c, const __nv_bfloat16* q, float* out,
                        cudaStream_t stream) {
-  using C = DecCfg<D, BITS, GQ>;
-  // kernel attributes and the SM count are looked up once per device
-  static int n_sm[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  using C = DecCfg<D, GQ, BMASK>;
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(decode_kernel<D, GQ, BMASK>), C::total);
   if (e != cudaSuccess) return e;
-  if (dev >= 64) return cudaErrorInvalidDevice;
-  if (!n_sm[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<D, BITS, GQ>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::total);
-    if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    n_sm[dev] = n;
-  }
-  const int total_units = P.n_layers * P.units;
-  const int grid = std::min(n_sm[dev], total_units);
+  // one CTA per SM, each holding at least one chunk per warp where the launch has
+  // that many (fewer, fuller CTAs merge less across SMs)
+  const long long T = P.total;
+  const int grid = (int)std::max<long long>(1, std::min<long long>(c->n_sm, T / C::NW));
+  P.n_vwarps = grid * C::NW;
+  if ((size_t)grid * 2 * C::DEPW > c->dec_ws_floats) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(C::kThreadsC);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::total;
   cfg.stream = stream;
   cudaLaunchAttribute at[1] = {pdl_attr()};
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<D, BITS, GQ>, P, c->packed, c->win_k, c->win_v,
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, GQ, BMASK>, P, c->packed, c->win_k, c->win_v,
                             q, out);
 }
 
-template <int D, int BITS>
-cudaError_t launch_g(const DecParams& P, const kvc_cache* c, const __nv_bfloat16* q, float* out,
+template <int D, int BMASK>
+cudaError_t launch_g(DecParams& P, const kvc_cache* c, const __nv_bfloat16* q, float* out,
                      cudaStream_t stream) {
   switch (c->g) {
-    case 1: return launch_one<D, BITS, 1>(P, c, q, out, stream);
-    case 2: return launch_one<D, BITS, 2>(P, c, q, out, stream);
-    case 4: return launch_one<D, BITS, 4>(P, c, q, out, stream);
-    case 8: return launch_one<D, BITS, 8>(P, c, q, out, stream);
+    case 1: return launch_one<D, 1, BMASK>(P, c, q, out, stream);
+    case 2: return launch_one<D, 2, BMASK>(P, c, q, out, stream);
+    case 4: return launch_one<D, 4, BMASK>(P, c, q, out, stream);
+    case 8: return launch_one<D, 8, BMASK>(P, c, q, out, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -976,7 +1039,7 @@ cudaError_t launch_common(const kvc_cache* c, int layer_begin, int layer_count,
                           cudaStream_t stream) {
   const kvc_dims& d = c->dims;
   const int units = d.batch * d.n_kv_heads;
-  const int D = d.head_dim, R = d.window_len;
+  const int D = d.head_dim;
   bool appending = k_new != nullptr;
   bool any_flush = false;
   if (appending)
@@ -992,20 +1055,28 @@ cudaError_t launch_common(const kvc_cache* c, int layer_begin, int layer_count,
     P.n_layers = cnt;
     P.layer_begin = layer_begin + base;
     P.units = units;
-    P.R = R;
     P.sl2 = 1.4426950408889634f / sqrtf((float)D);
     P.err = c->err;
+    P.ws = c->dec_ws;
+    P.cnt = c->dec_cnt;
+    P.wait_limit = c->wait_limit_set ? c->wait_limit : kWaitLimit;
     const bool fused = appending && !any_flush;
     P.k_new = fused ? k_new + (size_t)base * units * D : nullptr;
     P.v_new = fused ? v_new + (size_t)base * units * D : nullptr;
+    long long total = 0;
+    int bmask = 0;
+    const size_t gq = (size_t)c->g * D;
+    float* ob = out + (size_t)base * units * gq;
     for (int i = 0; i < cnt; ++i) {
       const LayerState& ls = c->L[layer_begin + base + i];
       DecLayer& L = P.L[i];
+      const int R = ls.R;
       L.cap_groups = ls.cap_groups;
       L.packed_off = (long long)ls.packed_off;
-      L.flush_start = -1;
-      L.n_ctas = 0;
-      L.cta_begin = 0;
+      L.win_off = (long long)ls.win_off;
+      L.R = R;
+      L.bits = ls.bits;
+      L.gpc = dec_groups_per_chunk(D, ls.bits == 16 ? 2 : ls.bits);
       if (appending) {
         const bool flush = flush_flags[base + i] != 0;
         L.new_slot = fused ? (ls.win_start + ls.win_len) % R : -1;
@@ -1019,19 +1090,26 @@ cudaError_t launch_common(const kvc_cache* c, int layer_begin, int layer_count,
         L.win_len = ls.win_len;
       }
       L.wchunks = (L.win_len + kSlotsPerWarp - 1) / kSlotsPerWarp;
-      L.pchunks = (L.n_groups + kGroupsPerWarp - 1) / kGroupsPerWarp;
+      L.pchunks = (L.n_groups + L.gpc - 1) / L.gpc;
+      L.chunk_begin = total;
+      total += (long long)units * (L.wchunks + L.pchunks);
+      if (L.pchunks > 0) bmask |= ls.bits == 2 ? 1 : (ls.bits == 4 ? 2 : 0);
+      if (L.wchunks + L.pchunks == 0) {   // nothing stored: the output is zero
+        cudaError_t e = cudaMemsetAsync(ob + (size_t)i * units * gq, 0, units * gq * 4, stream);
+        if (e != cudaSuccess) return e;
+      }
     }
-    const __nv_bfloat16* qb = q + (size_t)base * units * c->g * D;
-    float* ob = out + (size_t)base * units * c->g * D;
+    P.total = total;
+    if (total == 0) continue;
+    const __nv_bfloat16* qb = q + (size_t)base * units * gq;
+    if (bmask == 0) bmask = 1;   // window only: any instantiation serves
     cudaError_t e;
-    // 16-bit storage has no packed groups (everything is in the window): any packed
-    // instantiation serves it
-    const int bits = d.bits == 16 ? 2 : d.bits;
-    if (D == 128 && bits == 2) e = launch_g<128, 2>(P, c, qb, ob, stream);
-    else if (D == 128 && bits == 4) e = launch_g<128, 4>(P, c, qb, ob, stream);
-    else if (D == 64 && bits == 2) e = launch_g<64, 2>(P, c, qb, ob, stream);
-    else if (D == 64 && bits == 4) e = launch_g<64, 4>(P, c, qb, ob, stream);
-    else return cudaErrorInvalidValue;
+    if (D == 128 && bmask == 1) e = launch_g<128, 1>(P, c, qb, ob, stream);
+    else if (D == 128 && bmask == 2) e = launch_g<128, 2>(P, c, qb, ob, stream);
+    else if (D == 128) e = launch_g<128, 3>(P, c, qb, ob, stream);
+    else if (bmask == 1) e = launch_g<64, 1>(P, c, qb, ob, stream);
+    else if (bmask == 2) e = launch_g<64, 2>(P, c, qb, ob, stream);
+    else e = launch_g<64, 3>(P, c, qb, ob, stream);
     if (e != cudaSuccess) return e;
     count_launches(1);
     e = cudaGetLastError();
@@ -1052,6 +1130,10 @@ cudaError_t launch_decode_step(const kvc_cache* c, int layer_begin, int layer_co
                                const __nv_bfloat16* v_new, const int* flush_flags, float* out,
                                cudaStream_t stream) {
   return launch_common(c, layer_begin, layer_count, q, k_new, v_new, flush_flags, out, stream);
+}
+
+size_t decode_workspace_floats(int n_sm, int g, int D) {
+  return (size_t)2 * n_sm * 16 * dep_floats(D, g);
 }
 
 }  // namespace kvc

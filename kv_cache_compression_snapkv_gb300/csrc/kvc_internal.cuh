@@ -162,6 +162,9 @@ __host__ __device__ constexpr int off_vzero(int D, int bits) { return 2 * code_b
 // ------------------------------------------------------------------ cache state
 struct LayerState {
   int prefilled = 0;
+  int bits = 2;          // 2 or 4 (packed groups), or 16 (every token exact in the window)
+  int R = 0;             // window ring length (slots)
+  int block_bytes = 0;   // bytes of one packed group block (0 at 16 bits)
   int budget = 0;        // clipped budget (tokens per head)
   int n_kept = 0;        // selected prompt tokens per head
   int scored = 0;        // 1 if the selection is stored in kept_ptr (else identity)
@@ -172,6 +175,7 @@ struct LayerState {
   int win_len = 0;       // tokens in the window
   int appended = 0;
   size_t packed_off = 0; // byte offset of the layer inside the packed store
+  size_t win_off = 0;    // element offset of the layer's rings inside win_k / win_v
   size_t kept_off = 0;   // element offset of the layer inside kept[]
 };
 
@@ -180,8 +184,8 @@ struct LayerState {
 struct kvc_cache {
   kvc_dims dims{};
   int device = 0;
+  int n_sm = 0;                 // SMs of the device (decode grid)
   int g = 1;                    // GQA group
-  int block_bytes = 0;
   std::vector<kvc::LayerState> L;
   // storage
   uint8_t* packed = nullptr;  size_t packed_bytes = 0;
@@ -193,7 +197,16 @@ struct kvc_cache {
   unsigned* gsync = nullptr;  // scoring counters, 1 + B*H words (zero between launches)
   float* scores = nullptr;
   float* pooled = nullptr;    size_t score_elems = 0;
-  unsigned* err = nullptr;     // device error word (bounded waits that gave up)
+  float* dec_ws = nullptr;    size_t dec_ws_floats = 0;  // decode partial states
+  unsigned* dec_cnt = nullptr; // decode arrival tickets, n_layers * B*H words (zero between launches)
+  // error word set by bounded device waits that gave up: mapped pinned host memory
+  // where the device has native host atomics (err_host then reads it without a
+  // synchronisation, so the next call on the cache reports it), else device memory
+  unsigned* err = nullptr;
+  volatile unsigned* err_host = nullptr;
+  void* err_pinned = nullptr;
+  bool wait_limit_set = false; // polls per decode staging wait set by kvc_set_wait_limit
+  unsigned wait_limit = 0;
   int last_scored_layer = -1;
   std::vector<void*> allocations;
 };
@@ -255,10 +268,11 @@ cudaError_t launch_export(const kvc_cache* c, int layer, const kvc_export* dst,
 cudaError_t launch_score_tc(const kvc_dims& d, const __nv_bfloat16* q_obs,
                             const __nv_bfloat16* k, float2* stats, unsigned* gsync, float* scores,
                             unsigned* err, cudaStream_t stream);
-// Selection launches with explicit scratch (allocation-free entry point).
+// Selection launches with explicit scratch (allocation-free entry point); err is
+// the scoring launch's error word.
 cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
                               const __nv_bfloat16* k, float2* stats, unsigned* gsync,
-                              float* scores, cudaStream_t stream);
+                              float* scores, unsigned* err, cudaStream_t stream);
 // Full-prompt cumulated attention (un-normalised column sums, key blocks of 128 with
 // running row maxima) of every unit into scores [unit][n - alpha]; q_full is
 // [B][Hq][n][d]. Zeroes the scores first (stream-ordered); err may be NULL.
@@ -267,13 +281,22 @@ cudaError_t launch_acumul(const kvc_dims& d, const __nv_bfloat16* q_full, const 
 // Population variance of each of `units` rows of m scores (fp32 out, one per row).
 cudaError_t launch_score_variance(const float* scores, int units, int m, float* var,
                                   cudaStream_t stream);
+// abort_flag (may be NULL): when it is non-zero at launch time every kept index is
+// written as -1.
 cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float* pooled,
-                                  int32_t* kept_out, int k_sel, cudaStream_t stream);
+                                  int32_t* kept_out, int k_sel, const unsigned* abort_flag,
+                                  cudaStream_t stream);
 
 // Decode work decomposition: a unit's work is cut into chunks of 16 window slots
-// or 1 packed group (fine chunks keep the warps of a CTA evenly loaded).
-constexpr int kDecGroupsPerChunk = 1;
+// or of the packed groups that fill the same bytes (at least one).
 constexpr int kDecSlotsPerChunk = 16;
+__host__ __device__ constexpr int dec_groups_per_chunk(int D, int bits) {
+  return kDecSlotsPerChunk * D * 4 / block_bytes(D, bits) > 1
+             ? kDecSlotsPerChunk * D * 4 / block_bytes(D, bits) : 1;
+}
+// Floats of the decode workspace of a cache: two partial states per warp, at
+// most 16 warps per SM.
+size_t decode_workspace_floats(int n_sm, int g, int D);
 
 // Scoring: partial row statistics kept per (unit, row) for a prompt of n keys
 // (at most four epilogue groups in each CTA that owns one of the ceil(n/128) key

@@ -19,11 +19,18 @@
 //     sharing a context) race on it: serialize them.
 // A second static array, zero at load, holds the scoring launch's counters (one
 // per (sequence, kv head) plus one); each launch leaves them at zero again, and it
-// bounds B*H at kMaxUnits.
-// In host code the array's name is only a host-side stand-in, not a device
-// address, so its device address is looked up once per device
+// bounds B*H at kMaxUnits. A third static word is the scoring launch's error
+// word: a bounded wait that gives up sets it, the top-k launch then writes every
+// kept index as -1 (never a stale selection), and kvc_select_noalloc_check
+// reports and clears it.
+// In host code the arrays' names are only host-side stand-ins, not device
+// addresses, so their device addresses are looked up once per device
 // (cudaGetSymbolAddress, with that device current) on the first call made on
-// that device; make that first call before any stream capture.
+// that device; make that first call before any stream capture. The runtime
+// loads the module holding the arrays lazily, so that first lookup is also when
+// the device commits the 32 MiB: make the first call before an arena reserves
+// the rest of the device's memory (if it cannot be committed, the call returns
+// KVC_E_OOM).
 #include <mutex>
 
 #include "kvc_internal.cuh"
@@ -36,30 +43,37 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_select_scratch[kScratchBytes];
 constexpr int kMaxUnits = 8192;
 static __device__ unsigned g_select_sync[1 + kMaxUnits] = {0u};
+static __device__ unsigned g_select_err = 0u;
 
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 void* g_sync_addr[kMaxDevices] = {};
+void* g_err_addr[kMaxDevices] = {};
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-kvc_status scratch_for_current_device(void** out, unsigned** sync) {
+kvc_status scratch_for_current_device(void** out, unsigned** sync, unsigned** err) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_E_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
     void* q = nullptr;
-    if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || !p ||
-        cudaGetSymbolAddress(&q, g_select_sync) != cudaSuccess || !q) {
+    void* r = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_select_scratch);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&q, g_select_sync);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&r, g_select_err);
+    if (e != cudaSuccess || !p || !q || !r) {
       cudaGetLastError();
-      return KVC_E_CUDA;
+      return e == cudaErrorMemoryAllocation ? KVC_E_OOM : KVC_E_CUDA;
     }
     g_scratch_addr[dev] = p;
     g_sync_addr[dev] = q;
+    g_err_addr[dev] = r;
   }
   *out = g_scratch_addr[dev];
   *sync = static_cast<unsigned*>(g_sync_addr[dev]);
+  *err = static_cast<unsigned*>(g_err_addr[dev]);
   return KVC_OK;
 }
 
@@ -91,7 +105,8 @@ extern "C" kvc_status kvc_select_noalloc(const kvc_dims* dims, int32_t budget, c
 
   void* base = nullptr;
   unsigned* gsync = nullptr;
-  kvc_status st = scratch_for_current_device(&base, &gsync);
+  unsigned* err = nullptr;
+  kvc_status st = scratch_for_current_device(&base, &gsync, &err);
   if (st != KVC_OK) return st;
   unsigned char* p = static_cast<unsigned char*>(base);
   float2* stats = reinterpret_cast<float2*>(p);
@@ -102,8 +117,24 @@ extern "C" kvc_status kvc_select_noalloc(const kvc_dims* dims, int32_t budget, c
   const int k_sel = (size_t)budget < ns ? budget : (int)ns;
   cudaError_t e = kvc::launch_score_into(d, static_cast<const __nv_bfloat16*>(q_obs),
                                          static_cast<const __nv_bfloat16*>(k), stats, gsync, sc,
-                                         s);
-  if (e == cudaSuccess) e = kvc::launch_pool_topk_into(d, sc, pooled, kept, k_sel, s);
+                                         err, s);
+  if (e == cudaSuccess) e = kvc::launch_pool_topk_into(d, sc, pooled, kept, k_sel, err, s);
   if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? KVC_E_OOM : KVC_E_CUDA;
   return KVC_OK;
+}
+
+extern "C" kvc_status kvc_select_noalloc_check(void* stream) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_E_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_err_addr[dev]) return KVC_OK;   // no call on this device yet
+  }
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_E_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_select_err, sizeof(word)) != cudaSuccess) return KVC_E_CUDA;
+  if (word == 0) return KVC_OK;
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_select_err, &zero, sizeof(zero)) != cudaSuccess) return KVC_E_CUDA;
+  return KVC_E_TIMEOUT;
 }

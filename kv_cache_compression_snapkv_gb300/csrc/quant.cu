@@ -82,22 +82,25 @@ struct AppendParams {
   int flush_start[KVC_MAX_LAUNCH_LAYERS]; // -1: no flush; else ring slot of the oldest token
   int flush_group[KVC_MAX_LAUNCH_LAYERS]; // packed group index to write
   long long packed_off[KVC_MAX_LAUNCH_LAYERS];
+  long long win_off[KVC_MAX_LAUNCH_LAYERS];  // element offset of the layer's rings
   int cap_groups[KVC_MAX_LAUNCH_LAYERS];
+  int R[KVC_MAX_LAUNCH_LAYERS];           // ring length
+  int bits[KVC_MAX_LAUNCH_LAYERS];        // 2, 4 or 16 (16 never flushes)
 };
 
 // grid.x = layer_rel * units + unit
-template <int D, int BITS>
+template <int D>
 __global__ void __launch_bounds__(kThreads)
-append_kernel(AppendParams P, int layer_begin, int units, int R, const __nv_bfloat16* __restrict__ k_new,
+append_kernel(AppendParams P, int units, const __nv_bfloat16* __restrict__ k_new,
               const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ win_k,
-              __nv_bfloat16* __restrict__ win_v, uint8_t* __restrict__ packed, int block_bytes) {
+              __nv_bfloat16* __restrict__ win_v, uint8_t* __restrict__ packed) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   pdl_wait();      // the previous step's reads of the window are complete
   pdl_release();
   const int lrel = blockIdx.x / units, unit = blockIdx.x % units;
-  const size_t wunit = (size_t)(layer_begin + lrel) * units + unit;
-  __nv_bfloat16* wk = win_k + wunit * R * D;
-  __nv_bfloat16* wv = win_v + wunit * R * D;
+  const int R = P.R[lrel];
+  __nv_bfloat16* wk = win_k + P.win_off[lrel] + (size_t)unit * R * D;
+  __nv_bfloat16* wv = win_v + P.win_off[lrel] + (size_t)unit * R * D;
   const __nv_bfloat16* kn = k_new + ((size_t)lrel * units + unit) * D;
   const __nv_bfloat16* vn = v_new + ((size_t)lrel * units + unit) * D;
   const int slot = P.slot[lrel];
@@ -113,9 +116,11 @@ append_kernel(AppendParams P, int layer_begin, int units, int R, const __nv_bflo
     s.v[t][c] = window_load_v(wv, sl, c, D);
   }
   __syncthreads();
+  const int bits = P.bits[lrel];
   uint8_t* blk = packed + P.packed_off[lrel] +
-                 ((size_t)unit * P.cap_groups[lrel] + P.flush_group[lrel]) * block_bytes;
-  quantize_block<D, BITS, kThreads>(s, blk);
+                 ((size_t)unit * P.cap_groups[lrel] + P.flush_group[lrel]) * block_bytes(D, bits);
+  if (bits == 2) quantize_block<D, 2, kThreads>(s, blk);
+  else quantize_block<D, 4, kThreads>(s, blk);
 }
 
 // Export: grid.x = group j (or window when j == n_groups), grid.y = unit
@@ -204,13 +209,13 @@ cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* ke
                                 cudaStream_t stream, int sinks, int32_t* kept_out) {
   const kvc_dims& d = c->dims;
   const LayerState& ls = c->L[layer];
-  const bool exact = d.bits == 16;   // 16-bit storage: no packed groups, all in the window
+  const bool exact = ls.bits == 16;   // 16-bit storage: no packed groups, all in the window
   const int groups = exact ? 0 : n_kept / KVC_GROUP;
   const int win_rows = n_kept - groups * KVC_GROUP + d.obs_window;
   const int win_ctas = (win_rows + KVC_GROUP - 1) / KVC_GROUP;
   const int units = d.batch * d.n_kv_heads;
-  const size_t woff = (size_t)layer * units * d.window_len * d.head_dim;
-  KVC_DISPATCH_DB(d.head_dim, exact ? 2 : d.bits, {
+  const size_t woff = ls.win_off;
+  KVC_DISPATCH_DB(d.head_dim, exact ? 2 : ls.bits, {
     const size_t sm = group_smem<D>();
     cudaError_t e = set_smem(gather_quant_kernel<D, BITS>, sm);
     if (e != cudaSuccess) return e;
@@ -224,7 +229,7 @@ cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* ke
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gather_quant_kernel<D, BITS>, k, v, kept, n_kept, d.prompt_len,
                            d.obs_window, c->packed + ls.packed_off, ls.cap_groups,
-                           c->block_bytes, d.window_len, c->win_k + woff, c->win_v + woff,
+                           ls.block_bytes, ls.R, c->win_k + woff, c->win_v + woff,
                            sinks, kept_out, groups);
     if (e != cudaSuccess) return e;
   });
@@ -243,17 +248,20 @@ cudaError_t launch_append(const kvc_cache* c, int layer_begin, int layer_count,
     AppendParams P;
     for (int i = 0; i < cnt; ++i) {
       const LayerState& ls = c->L[layer_begin + base + i];
-      P.slot[i] = (ls.win_start + ls.win_len) % d.window_len;
+      P.slot[i] = (ls.win_start + ls.win_len) % ls.R;
       P.flush_start[i] = flush_flags[base + i] ? ls.win_start : -1;
       P.flush_group[i] = ls.n_groups;
       P.packed_off[i] = (long long)ls.packed_off;
+      P.win_off[i] = (long long)ls.win_off;
       P.cap_groups[i] = ls.cap_groups;
+      P.R[i] = ls.R;
+      P.bits[i] = ls.bits;
     }
     const __nv_bfloat16* kn = k_new + (size_t)base * units * d.head_dim;
     const __nv_bfloat16* vn = v_new + (size_t)base * units * d.head_dim;
-    KVC_DISPATCH_DB(d.head_dim, d.bits, {
+    KVC_DISPATCH_DB(d.head_dim, 2, {
       const size_t sm = group_smem<D>();
-      cudaError_t e = set_smem(append_kernel<D, BITS>, sm);
+      cudaError_t e = set_smem(append_kernel<D>, sm);
       if (e != cudaSuccess) return e;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(cnt * units);
@@ -263,9 +271,8 @@ cudaError_t launch_append(const kvc_cache* c, int layer_begin, int layer_count,
       cudaLaunchAttribute at[1] = {pdl_attr()};
       cfg.attrs = at;
       cfg.numAttrs = 1;
-      e = cudaLaunchKernelEx(&cfg, append_kernel<D, BITS>, P, layer_begin + base, units,
-                             d.window_len, kn, vn, c->win_k, c->win_v, c->packed,
-                             c->block_bytes);
+      e = cudaLaunchKernelEx(&cfg, append_kernel<D>, P, units, kn, vn, c->win_k, c->win_v,
+                             c->packed);
       if (e != cudaSuccess) return e;
     });
     count_launches(1);
@@ -280,11 +287,11 @@ cudaError_t launch_export(const kvc_cache* c, int layer, const kvc_export* dst,
   const kvc_dims& d = c->dims;
   const LayerState& ls = c->L[layer];
   const int units = d.batch * d.n_kv_heads;
-  const size_t woff = (size_t)layer * units * d.window_len * d.head_dim;
-  KVC_DISPATCH_DB(d.head_dim, d.bits == 16 ? 2 : d.bits, {   // 16-bit: window only
+  const size_t woff = ls.win_off;
+  KVC_DISPATCH_DB(d.head_dim, ls.bits == 16 ? 2 : ls.bits, {   // 16-bit: window only
     export_kernel<D, BITS><<<dim3(ls.n_groups + 1, units), kThreads, 0, stream>>>(
-        c->packed + ls.packed_off, ls.cap_groups, ls.n_groups, c->block_bytes, c->win_k + woff,
-        c->win_v + woff, d.window_len, ls.win_start, ls.win_len, *dst);
+        c->packed + ls.packed_off, ls.cap_groups, ls.n_groups, ls.block_bytes, c->win_k + woff,
+        c->win_v + woff, ls.R, ls.win_start, ls.win_len, *dst);
   });
   count_launches(1);
   cudaError_t e = cudaGetLastError();

@@ -13,12 +13,12 @@ cudaError_t launch_score(const kvc_cache* c, int layer, const __nv_bfloat16* q_o
   return launch_score_tc(c->dims, q_obs, k, c->stats, c->gsync, c->scores, c->err, stream);
 }
 
-// The same launch with the scratch buffers given explicitly (used by the
-// allocation-free selection entry point, which has no error word).
+// The same launch with the scratch buffers and the error word given explicitly
+// (used by the allocation-free selection entry point).
 cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
                               const __nv_bfloat16* k, float2* stats, unsigned* gsync,
-                              float* scores, cudaStream_t stream) {
-  return launch_score_tc(d, q_obs, k, stats, gsync, scores, nullptr, stream);
+                              float* scores, unsigned* err, cudaStream_t stream) {
+  return launch_score_tc(d, q_obs, k, stats, gsync, scores, err, stream);
 }
 
 namespace {

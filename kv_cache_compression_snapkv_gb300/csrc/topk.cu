@@ -61,11 +61,21 @@ __device__ __forceinline__ void block_scan2(TopkSmem& s, unsigned a, unsigned b,
   eb = pb + ib - b;
 }
 
+// When the scoring launch before this one gave up a wait (*abort_flag != 0; the
+// flag may be NULL), its scores are incomplete: every kept index is written as -1.
+__device__ __forceinline__ bool selection_aborted(const unsigned* abort_flag, int32_t* out,
+                                                  int k_sel, bool writer) {
+  if (!abort_flag || *reinterpret_cast<const volatile unsigned*>(abort_flag) == 0u) return false;
+  if (writer)
+    for (int i = threadIdx.x; i < k_sel; i += blockDim.x) out[i] = -1;
+  return true;
+}
+
 // SMEM: the pooled row lives in dynamic shared memory; else in `pooled` (global).
 template <bool SMEM>
 __global__ void __launch_bounds__(kTopkThreads)
 pool_topk_kernel(const float* __restrict__ scores, float* __restrict__ pooled, int ns, int w,
-                 int k_sel, int32_t* __restrict__ kept) {
+                 int k_sel, int32_t* __restrict__ kept, const unsigned* abort_flag) {
   __shared__ TopkSmem s;
   extern __shared__ __align__(16) float spool[];
   const int unit = blockIdx.x;
@@ -73,6 +83,7 @@ pool_topk_kernel(const float* __restrict__ scores, float* __restrict__ pooled, i
   float* pg = pooled + (size_t)unit * ns;
   float* pl = SMEM ? spool : pg;
   int32_t* out = kept + (size_t)unit * k_sel;
+  if (selection_aborted(abort_flag, out, k_sel < ns ? k_sel : ns, true)) return;
   const int r = (w - 1) / 2;
   if constexpr (SMEM) {
     // stage the scores (coalesced), pool from shared memory into registers, write back
@@ -449,11 +460,19 @@ __device__ void cluster_pool_select(ClusterSmem& s, float* dyn, const float* __r
 
 __global__ void __launch_bounds__(kCThreads)
 pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ pooled, int ns,
-                         int w, int k_sel, int32_t* __restrict__ kept) {
+                         int w, int k_sel, int32_t* __restrict__ kept,
+                         const unsigned* abort_flag) {
   __shared__ ClusterSmem s;
   extern __shared__ __align__(16) float dyn[];
   const int unit = blockIdx.x / kCluster;
   pdl_wait();      // the scores are complete
+  // every CTA of the cluster reads the same flag (written before this launch) and
+  // leaves before any cluster barrier
+  if (selection_aborted(abort_flag, kept + (size_t)unit * k_sel, k_sel < ns ? k_sel : ns,
+                        blockIdx.x % kCluster == 0)) {
+    pdl_release();
+    return;
+  }
   cluster_pool_select(s, dyn, scores + (size_t)unit * ns, pooled + (size_t)unit * ns,
                       kept + (size_t)unit * k_sel, ns, w, k_sel);
   // only now: dependents scheduled earlier would wait on these SMs beside the selection
@@ -462,7 +481,8 @@ pool_topk_cluster_kernel(const float* __restrict__ scores, float* __restrict__ p
 }
 
 cudaError_t launch_topk_cluster(const float* scores, float* pooled, int units, int ns, int w,
-                                int k_sel, int32_t* kept, cudaStream_t stream) {
+                                int k_sel, int32_t* kept, const unsigned* abort_flag,
+                                cudaStream_t stream) {
   const int seg = (ns + kCluster - 1) / kCluster;
   // a dependent launch (its set-up overlaps the scoring launch's end); the shared
   // memory is padded so that one CTA fits an SM: scheduled early, the CTAs would
@@ -484,25 +504,26 @@ cudaError_t launch_topk_cluster(const float* scores, float* pooled, int units, i
   attr[1] = pdl_attr();
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, pool_topk_cluster_kernel, scores, pooled, ns, w, k_sel, kept);
+  e = cudaLaunchKernelEx(&cfg, pool_topk_cluster_kernel, scores, pooled, ns, w, k_sel, kept,
+                         abort_flag);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const float* scores, float* pooled, int units, int ns, int w, int k_sel,
-                        int32_t* kept, cudaStream_t stream) {
+                        int32_t* kept, const unsigned* abort_flag, cudaStream_t stream) {
   if ((ns + kCluster - 1) / kCluster <= kMaxSeg && w <= 129)
-    return launch_topk_cluster(scores, pooled, units, ns, w, k_sel, kept, stream);
+    return launch_topk_cluster(scores, pooled, units, ns, w, k_sel, kept, abort_flag, stream);
   if (ns <= kSmemMax) {
     const size_t sm = (size_t)ns * sizeof(float);
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(pool_topk_kernel<true>), sm);
     if (e != cudaSuccess) return e;
     pool_topk_kernel<true><<<units, kTopkThreads, sm, stream>>>(scores, pooled, ns, w, k_sel,
-                                                                 kept);
+                                                                 kept, abort_flag);
   } else {
     pool_topk_kernel<false><<<units, kTopkThreads, 0, stream>>>(scores, pooled, ns, w, k_sel,
-                                                                 kept);
+                                                                 kept, abort_flag);
   }
   count_launches(1);
   return cudaGetLastError();
@@ -515,15 +536,17 @@ cudaError_t launch_pool_topk(const kvc_cache* c, int layer, int32_t* kept_out, i
   (void)layer;
   const kvc_dims& d = c->dims;
   return launch_topk(c->scores, c->pooled, d.batch * d.n_kv_heads, d.prompt_len - d.obs_window,
-                     d.pool_kernel, k_sel, kept_out, stream);
+                     d.pool_kernel, k_sel, kept_out, nullptr, stream);
 }
 
 // The same launch with the score and pooled buffers given explicitly (used by
-// the allocation-free selection entry point).
+// the allocation-free selection entry point, whose scoring error word is
+// abort_flag).
 cudaError_t launch_pool_topk_into(const kvc_dims& d, const float* scores, float* pooled,
-                                  int32_t* kept_out, int k_sel, cudaStream_t stream) {
+                                  int32_t* kept_out, int k_sel, const unsigned* abort_flag,
+                                  cudaStream_t stream) {
   return launch_topk(scores, pooled, d.batch * d.n_kv_heads, d.prompt_len - d.obs_window,
-                     d.pool_kernel, k_sel, kept_out, stream);
+                     d.pool_kernel, k_sel, kept_out, abort_flag, stream);
 }
 
 }  // namespace kvc

@@ -5,7 +5,13 @@ Acceptance rules (compressed-KV parity):
   * packed codes, fp16 scales and zero-points: bit-exact;
   * kept index sets: bit-exact, except an index in the symmetric difference is
     excused when its oracle pooled score is within 1e-5 relative of the oracle's
-    k-th largest pooled score (fp32 GPU scores vs fp64 oracle scores);
+    k-th largest pooled score (fp32 GPU scores vs fp64 oracle scores); a unit
+    with an excused difference is then stored by the oracle on the GPU's own
+    kept set, so that its codes, window and decode are still compared;
+  * selection scores: relative error <= 1e-4, each score against itself with a
+    floor of 1e-3 of the largest score of the unit's unplanted keys (planted
+    sinks and needles take most of a row's weight and would otherwise hide the
+    error on the ordinary keys being ranked);
   * bf16 window: bit-exact;
   * decode output (fp32): max over (sequence, query head, step) of
     ||o - o*||_inf / ||o*||_inf <= 2e-3.
@@ -39,6 +45,7 @@ class Report:
     decode_err: float = 0.0
     decode_checked: int = 0
     score_err: float = 0.0
+    rebuilt_units: int = 0
     notes: list = field(default_factory=list)
 
 
@@ -60,17 +67,35 @@ def check_kept(gpu_kept, ora_kept, ora_pooled, k, rep: Report):
     return False
 
 
-def check_scores(gpu_s, ora_s, rep: Report):
-    scale = np.abs(ora_s).max()
+def planted_positions(x: dict, b: int, h: int) -> list:
+    """Sink and needle positions of unit (b, h) of synth.layer_inputs' output."""
+    pos = list(x.get("sinks") or [])
+    if x.get("needles") is not None:
+        pos += [int(i) for i in x["needles"][b, h].tolist()]
+    return pos
+
+
+def check_scores(gpu_s, ora_s, rep: Report, planted=()):
+    ordinary = np.ones(len(ora_s), dtype=bool)
+    ordinary[[p for p in planted if p < len(ora_s)]] = False
+    scale = np.abs(ora_s[ordinary]).max() if ordinary.any() else np.abs(ora_s).max()
     err = np.abs(gpu_s - ora_s) / np.maximum(np.abs(ora_s), 1e-3 * scale)
     rep.score_err = max(rep.score_err, float(err.max()))
     assert err.max() <= SCORE_RTOL, f"score error {err.max():.3g}"
 
 
 def check_export(ex: dict, oc: OracleCache, heads, rep: Report):
-    """Bit-exact comparison of one layer's packed store and window."""
+    """Bit-exact comparison of one layer's packed store and window. A 16-bit layer
+    keeps every token in the GPU's window: the oracle's exact store (its packed
+    part, then its window) is compared with it."""
     for (b, h) in heads:
         st = oc.heads[b][h]
+        if oc.bits == 16:
+            assert ex["k_codes"].shape[2] == 0
+            np.testing.assert_array_equal(np64(ex["win_k"][b, h]), np.vstack([st.k_hat, st.win_k]))
+            np.testing.assert_array_equal(np64(ex["win_v"][b, h]), np.vstack([st.v_hat, st.win_v]))
+            rep.codes_compared += len(st.k_hat) + len(st.win_k)
+            continue
         T = st.n_packed
         assert ex["k_codes"].shape[2] == T, (ex["k_codes"].shape, T)
         np.testing.assert_array_equal(ex["k_codes"][b, h].cpu().numpy(), st.kcodes)
@@ -92,7 +117,7 @@ def decode_error(o_gpu, o_ora):
 
 
 def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=True,
-              dev="cuda", budgets=None):
+              dev="cuda", budgets=None, layer_bits=None):
     """Full comparison on a workload the oracle finishes in seconds.
 
     selection: "score" (GPU scores and selects; the oracle does the same),
@@ -100,6 +125,7 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
                ("sinks", s) (both keep s attention sinks + the most recent tokens) or
                "acumul" (both score by the full-prompt cumulated attention).
     budgets: per-layer budgets to use instead of the spec's schedule.
+    layer_bits: per-layer storage precision (2, 4 or 16) of one mixed cache.
     """
     K = kvc()
     rep = Report()
@@ -109,7 +135,7 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
         budgets = K.kvc_plan_budgets(dims, spec.schedule, spec.avg_budget, spec.pyramid_depth)
     n, a = spec.prompt_len, spec.obs_window
     B, Hk, Hq, D = spec.batch, spec.n_kv_heads, spec.n_q_heads, spec.head_dim
-    cache = None
+    cache = None if layer_bits is None else K.kvc_cache_create_layers(dims, budgets, layer_bits)
     oracles = {}
     same = {}
     for layer in layers:
@@ -117,7 +143,11 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
         k_np, v_np = np64(x["k"]), np64(x["v"])
         q_np = np64(x["q_obs"]) if "q_obs" in x else None
         bud = budgets[layer]
-        oc = OracleCache(B, Hq, Hk, D, spec.bits, spec.group_size, spec.window_len)
+        if layer_bits is None:
+            oc = OracleCache(B, Hq, Hk, D, spec.bits, spec.group_size, spec.window_len)
+        else:
+            ring = K.kvc_layer_info_get(cache, layer)["window_capacity"]
+            oc = OracleCache(B, Hq, Hk, D, layer_bits[layer], spec.group_size, ring)
         scoring = bud < n - a
         sinks = selection[1] if isinstance(selection, tuple) else None
         if sinks is not None:
@@ -166,7 +196,8 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
             ok_heads = []
             for b in range(B):
                 for h in range(Hk):
-                    check_scores(sc[b, h].double().cpu().numpy(), oc.scores[b][h], rep)
+                    check_scores(sc[b, h].double().cpu().numpy(), oc.scores[b][h], rep,
+                                 planted_positions(x, b, h))
                     np.testing.assert_array_equal(
                         pl[b, h].double().cpu().numpy(),
                         _pool_of(sc[b, h].double().cpu().numpy(), spec.pool_kernel))
@@ -175,6 +206,15 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
                     if check_kept(gk, oc.heads[b][h].kept, oc.pooled[b][h], bud, rep):
                         ok_heads.append((b, h))
             assert info["n_kept"] == bud
+            if len(ok_heads) < B * Hk:
+                # an excused near-tie: store the GPU's selection in the oracle too and
+                # compare everything downstream of it
+                gk_all = [[ex["kept"][b, h].cpu().numpy().astype(np.int64) for h in range(Hk)]
+                          for b in range(B)]
+                rep.rebuilt_units += B * Hk - len(ok_heads)
+                oc = OracleCache(B, Hq, Hk, D, oc.bits, spec.group_size, oc.R)
+                oc.prefill(k_np, v_np, a, kept=gk_all)
+                ok_heads = [(b, h) for b in range(B) for h in range(Hk)]
         ex = K.kvc_export_layer(cache, layer)
         torch.cuda.synchronize()
         check_export(ex, oc, ok_heads, rep)
@@ -207,8 +247,12 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
     # final state matches after the flushes
     for layer in layers:
         info = K.kvc_layer_info_get(cache, layer)
-        assert info["window_tokens"] == oracles[layer].window_len()
-        assert info["packed_tokens"] == oracles[layer].n_packed()
+        if oracles[layer].bits == 16:
+            assert info["packed_tokens"] == 0
+            assert info["window_tokens"] == oracles[layer].n_packed() + oracles[layer].window_len()
+        else:
+            assert info["window_tokens"] == oracles[layer].window_len()
+            assert info["packed_tokens"] == oracles[layer].n_packed()
         ex = K.kvc_export_layer(cache, layer)
         torch.cuda.synchronize()
         check_export(ex, oracles[layer], same[layer], rep)

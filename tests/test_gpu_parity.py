@@ -61,3 +61,16 @@ def test_per_layer_calls_match():
                             prompt_len=600, obs_window=16, avg_budget=64, window_len=32)
     rep = run_small(spec, 12, selection="score", multi_layer_decode=False)
     assert rep.decode_err <= 2e-3
+
+
+def test_mixed_precision_layers():
+    """One cache whose layers differ in precision (MiniKV Figure 1: 16-bit top
+    layers, 2-bit lower ones; here also a 4-bit layer), every decode step one
+    launch over all four layers, each layer against the oracle at its own
+    precision, across window flushes."""
+    spec = synth.small_spec(2, n_layers=4, batch=2, n_q_heads=8, n_kv_heads=2,
+                            prompt_len=1000, obs_window=32, avg_budget=96, window_len=64)
+    rep = run_small(spec, 45, selection="score", layer_bits=[2, 2, 4, 16])
+    print(f"mixed: excused={rep.excused} codes={rep.codes_compared} "
+          f"decode_err={rep.decode_err:.2e}")
+    assert rep.decode_checked > 0

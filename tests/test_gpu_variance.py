@@ -8,7 +8,8 @@ import torch
 
 import synth
 from _parity import DECODE_RTOL, kvc, np64, run_small
-from oracle import OracleCache, plan_budgets_weighted, score_variance, variance_weights
+from oracle import (OracleCache, acumul_scores, layer_variance, plan_budgets_weighted,
+                    score_variance, variance_weights)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,7 +56,11 @@ def test_score_variance_matches_oracle():
                 worst_own = max(worst_own, abs(var[b, h] - own) / own)
                 worst_ora = max(worst_ora, abs(var[b, h] - ora) / ora)
     print(f"variance vs own scores {worst_own:.2e}, vs oracle {worst_ora:.2e}")
-    assert worst_own <= 1e-6        # the reduction (fp64, output rounded to fp32)
+    # the reduction: each thread's compensated (Kahan) fp32 sums of its elements and
+    # of their squared deviations (each square rounded once to fp32, 2^-24
+    # relative), the 256 partial sums added in fp64, the result rounded to fp32:
+    # a few fp32 ulps in all at these lengths, far below 1e-6
+    assert worst_own <= 1e-6
     assert worst_ora <= 1e-3        # plus the scores' own tolerance (1e-4 each)
 
 
@@ -88,3 +93,52 @@ def test_score_variance_needs_a_scored_layer():
         K.kvc_score_variance(cache, var)
     assert e.value.status == 5
     cache.close()
+
+
+ACUMUL_SPEC = synth.small_spec(2, n_layers=3, batch=1, n_q_heads=8, n_kv_heads=2,
+                               prompt_len=800, obs_window=32, avg_budget=96,
+                               schedule="uniform", window_len=64)
+
+
+def test_variance_of_cumulated_attention():
+    """MiniKV Figure 7's variance score is that of the cumulated attention: the
+    variance after kvc_prefill_acumul against the oracle's A_cumul of the same
+    inputs, per unit and per layer; then Var-prop budgets from it, and a cache
+    selected by A_cumul under those budgets against the oracle end to end."""
+    K = kvc()
+    spec = ACUMUL_SPEC
+    dims = K.dims_from_spec(spec, max_new_tokens=4)
+    budgets = K.kvc_plan_budgets(dims, "uniform", spec.avg_budget)
+    B, Hk, g = spec.batch, spec.n_kv_heads, spec.gqa
+    ns = spec.prompt_len - spec.obs_window
+    cache = K.kvc_cache_create(dims, budgets)
+    layer_var, worst = [], 0.0
+    for layer in range(spec.n_layers):
+        x = synth.layer_inputs(spec, layer, device="cuda")
+        qf = synth.prompt_queries(spec, layer, device="cuda")
+        K.kvc_prefill_acumul(cache, layer, qf, x["k"], x["v"])
+        var = torch.empty(B, Hk, device="cuda")
+        K.kvc_score_variance(cache, var)
+        torch.cuda.synchronize()
+        q_np, k_np = np64(qf), np64(x["k"])
+        ora = np.stack([[acumul_scores(q_np[b, h * g:(h + 1) * g], k_np[b, h])[:ns]
+                         for h in range(Hk)] for b in range(B)])
+        v = var.double().cpu().numpy()
+        for b in range(B):
+            for h in range(Hk):
+                ref = score_variance(ora[b, h])
+                worst = max(worst, abs(v[b, h] - ref) / ref)
+        layer_var.append(float(v.mean()))
+        assert abs(layer_var[-1] - layer_variance(ora)) <= 1e-3 * layer_variance(ora)
+    K.kvc_check_device(cache)
+    cache.close()
+    print(f"Var(A_cumul) vs oracle: worst relative error {worst:.2e}; layers "
+          f"{[f'{x:.4g}' for x in layer_var]}")
+    assert worst <= 1e-3          # the scores' own tolerance carried into the variance
+    w = variance_weights(layer_var, "var-prop")
+    avg = 160
+    budgets = K.kvc_plan_budgets_weighted(dims, avg, w)
+    assert budgets == plan_budgets_weighted(spec.n_layers, avg, w, spec.group_size,
+                                            max_budget=ns)
+    rep = run_small(spec, 20, selection="acumul", budgets=budgets)
+    assert rep.decode_checked > 0 and rep.decode_err <= DECODE_RTOL

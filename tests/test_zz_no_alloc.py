@@ -5,8 +5,10 @@ kvc_select_noalloc exists for callers that cannot allocate device memory (they
 own all of it through their own arena, or cannot afford a cudaMalloc in the
 loop); its intermediates live in a static device array shared by every call.
 The test makes two calls in a row on different inputs, so stale contents left
-by the first call in that shared array would show up in the second. It runs
-last (file name) so that a failure here leaves every other test already run.
+by the first call in that shared array would show up in the second, and checks
+the defining property: after a first call on the device, further calls leave
+the device's free memory unchanged. It runs last (file name) so that a failure
+here leaves every other test already run.
 """
 import pytest
 import torch
@@ -18,15 +20,22 @@ pytestmark = pytest.mark.gpu
 SCORE_RTOL = 1e-4
 
 
-def _spec():
-    return synth.small_spec(2, n_layers=2, batch=2, n_q_heads=8, n_kv_heads=2,
-                            prompt_len=3000, obs_window=32, avg_budget=256,
-                            schedule="uniform", window_len=64)
+SPECS = {
+    # GQA 4, head_dim 128
+    "gqa4_d128": synth.small_spec(2, n_layers=2, batch=2, n_q_heads=8, n_kv_heads=2,
+                                  prompt_len=3000, obs_window=32, avg_budget=256,
+                                  schedule="uniform", window_len=64),
+    # MHA (g = 1), head_dim 64
+    "mha_d64": synth.small_spec(2, n_layers=2, batch=1, n_q_heads=4, n_kv_heads=4, head_dim=64,
+                                prompt_len=1500, obs_window=16, avg_budget=128,
+                                schedule="uniform", window_len=64),
+}
 
 
-def test_select_noalloc_matches_prefill_two_calls():
+@pytest.mark.parametrize("name", list(SPECS))
+def test_select_noalloc_matches_prefill_two_calls(name):
     import kv_cache_compression_snapkv_gb300 as K
-    spec = _spec()
+    spec = SPECS[name]
     dims = K.dims_from_spec(spec, max_new_tokens=4)
     budgets = K.kvc_plan_budgets(dims, spec.schedule, spec.avg_budget, spec.pyramid_depth)
     B, H, ns = spec.batch, spec.n_kv_heads, spec.prompt_len - spec.obs_window
@@ -46,11 +55,16 @@ def test_select_noalloc_matches_prefill_two_calls():
         assert torch.equal(kept, ref_kept), f"layer {layer}: kept positions differ"
         torch.testing.assert_close(scores, ref_scores, rtol=SCORE_RTOL, atol=0.0)
 
-        # without the optional scores output (the scores then live in the scratch too)
+        # without the optional scores output (the scores then live in the scratch
+        # too); the device's free memory does not move across the call
         kept2 = torch.full_like(kept, -1)
+        free0, _ = torch.cuda.mem_get_info()
         K.kvc_select_noalloc(dims, budgets[layer], x["q_obs"], x["k"], kept2)
         torch.cuda.synchronize()
+        free1, _ = torch.cuda.mem_get_info()
+        assert free1 == free0, f"free device memory moved by {free0 - free1} bytes"
         assert torch.equal(kept2, ref_kept)
+    K.kvc_select_noalloc_check()          # no bounded wait gave up
     cache.close()
 
 
