@@ -139,52 +139,76 @@ __device__ __forceinline__ uint32_t split_bf16(float v) {
   return *reinterpret_cast<const uint32_t*>(&p);
 }
 
-// Exact fp16 pair of the two codes in pair slot P of word w. The field of slot P
-// is masked in place under the fp16 exponent of 2^e, e = 10 - BITS*j (j = field
-// index inside its byte), so each half reads 2^e + code; one subtraction leaves
-// the code.
+// The masks of the code fields inside a byte of each 16-bit half, held in
+// registers: with the mask a register operand, the field and the fp16 exponent
+// bits are merged by one three-input logic instruction with the exponent as its
+// immediate (a mask and an exponent both as immediates take two).
+template <int BITS>
+struct CodeMasks { uint32_t m[8 / BITS]; };
+
+template <int BITS>
+__device__ __forceinline__ CodeMasks<BITS> code_masks() {
+  CodeMasks<BITS> cm;
+  static_for<8 / BITS>([&](auto J_) {
+    constexpr int J = decltype(J_)::value;
+    constexpr uint32_t v = (((1u << BITS) - 1u) * 0x00010001u) << (BITS * J);
+    asm volatile("mov.b32 %0, %1;" : "=r"(cm.m[J]) : "n"(v));
+  });
+  return cm;
+}
+
+// Exact fp16 pair of the two codes in pair slot P of word w (w8 = w >> 8). The
+// field of slot P is masked in place under the fp16 exponent of 2^e, e = 10 -
+// BITS*j (j = field index inside its byte), so each half reads 2^e + code; one
+// subtraction leaves the code.
 template <int BITS, int P>
-__device__ __forceinline__ uint32_t unpack_pair(uint32_t w) {
+__device__ __forceinline__ uint32_t unpack_pair(uint32_t w, uint32_t w8, const CodeMasks<BITS>& cm) {
   constexpr int CPB = 8 / BITS, SB = P / CPB, J = P % CPB;
-  constexpr uint32_t mask = (((1u << BITS) - 1u) * 0x00010001u) << (BITS * J);
   constexpr uint32_t mag = ((uint32_t)(25 - BITS * J) << 10) * 0x00010001u;
-  const uint32_t v = ((SB ? (w >> 8) : w) & mask) | mag;
+  uint32_t v;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(SB ? w8 : w), "r"(cm.m[J]), "n"(mag));
   return h2u(__hsub2(u2h(v), u2h(mag)));
 }
 
 // A operand of key product (MT, KS) (rows = tokens, k = channels) from the lane's
 // key code words.
 template <int D, int BITS, int MT, int KS>
-__device__ __forceinline__ void key_afrag(const uint32_t* kw, uint32_t (&a)[4]) {
+__device__ __forceinline__ void key_afrag(const uint32_t* kw, const CodeMasks<BITS>& cm,
+                                          uint32_t (&a)[4]) {
   if constexpr (BITS == 2) {
     constexpr int wi = MT * (D / 32) + KS / 2, b = 2 * (KS & 1);
-    a[0] = unpack_pair<2, b>(kw[wi]);
-    a[1] = unpack_pair<2, 4 + b>(kw[wi]);
-    a[2] = unpack_pair<2, b + 1>(kw[wi]);
-    a[3] = unpack_pair<2, 5 + b>(kw[wi]);
+    const uint32_t w = kw[wi], w8 = w >> 8;
+    a[0] = unpack_pair<2, b>(w, w8, cm);
+    a[1] = unpack_pair<2, 4 + b>(w, w8, cm);
+    a[2] = unpack_pair<2, b + 1>(w, w8, cm);
+    a[3] = unpack_pair<2, 5 + b>(w, w8, cm);
   } else {
     constexpr int wi = MT * (D / 16) + KS;
-    a[0] = unpack_pair<4, 0>(kw[wi]);
-    a[1] = unpack_pair<4, 2>(kw[wi]);
-    a[2] = unpack_pair<4, 1>(kw[wi]);
-    a[3] = unpack_pair<4, 3>(kw[wi]);
+    const uint32_t w = kw[wi], w8 = w >> 8;
+    a[0] = unpack_pair<4, 0>(w, w8, cm);
+    a[1] = unpack_pair<4, 2>(w, w8, cm);
+    a[2] = unpack_pair<4, 1>(w, w8, cm);
+    a[3] = unpack_pair<4, 3>(w, w8, cm);
   }
 }
 // A operand of value product (MT, KS) (rows = channels, k = tokens).
 template <int BITS, int MT, int KS>
-__device__ __forceinline__ void value_afrag(const uint32_t* vw, uint32_t (&a)[4]) {
+__device__ __forceinline__ void value_afrag(const uint32_t* vw, const CodeMasks<BITS>& cm,
+                                            uint32_t (&a)[4]) {
   if constexpr (BITS == 2) {
     constexpr int b = 2 * KS;
-    a[0] = unpack_pair<2, b>(vw[MT]);
-    a[1] = unpack_pair<2, 4 + b>(vw[MT]);
-    a[2] = unpack_pair<2, b + 1>(vw[MT]);
-    a[3] = unpack_pair<2, 5 + b>(vw[MT]);
+    const uint32_t w = vw[MT], w8 = w >> 8;
+    a[0] = unpack_pair<2, b>(w, w8, cm);
+    a[1] = unpack_pair<2, 4 + b>(w, w8, cm);
+    a[2] = unpack_pair<2, b + 1>(w, w8, cm);
+    a[3] = unpack_pair<2, 5 + b>(w, w8, cm);
   } else {
     constexpr int wi = 2 * MT + KS;
-    a[0] = unpack_pair<4, 0>(vw[wi]);
-    a[1] = unpack_pair<4, 2>(vw[wi]);
-    a[2] = unpack_pair<4, 1>(vw[wi]);
-    a[3] = unpack_pair<4, 3>(vw[wi]);
+    const uint32_t w = vw[wi], w8 = w >> 8;
+    a[0] = unpack_pair<4, 0>(w, w8, cm);
+    a[1] = unpack_pair<4, 2>(w, w8, cm);
+    a[2] = unpack_pair<4, 1>(w, w8, cm);
+    a[3] = unpack_pair<4, 3>(w, w8, cm);
   }
 }
 
@@ -296,8 +320,10 @@ __device__ void packed_warp(WarpState<D, GQ>& st, const QRegs<D, GQ>& qr, const 
   constexpr int NH = n_tiles<GQ>();
   const int lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
 
+  const CodeMasks<BITS> cm = code_masks<BITS>();
   // key zero-point sums of every group of the chunk: C[group][n] = Z_group . q_n
-  // (A rows = groups, B = the queries in the "hi" columns)
+  // (A rows = groups; rows past the chunk's groups repeat group 0 and are not
+  // read; B = the queries, whose "hi" column is read)
   float zb[NH];
   {
     uint32_t za[KS][2];
@@ -307,22 +333,18 @@ __device__ void packed_warp(WarpState<D, GQ>& st, const QRegs<D, GQ>& qr, const 
 #pragma unroll
     for (int i = 0; i < KS / 2; ++i) {
       const uint4 z = zp[i];
-      const bool live = gid < n_grp;
-      za[2 * i][0] = live ? z.x : 0u;
-      za[2 * i][1] = live ? z.y : 0u;
-      za[2 * i + 1][0] = live ? z.z : 0u;
-      za[2 * i + 1][1] = live ? z.w : 0u;
+      za[2 * i][0] = z.x;
+      za[2 * i][1] = z.y;
+      za[2 * i + 1][0] = z.z;
+      za[2 * i + 1][1] = z.w;
     }
 #pragma unroll
     for (int u = 0; u < NH; ++u) {
       float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const uint32_t b0 = (gid & 1) ? 0u : qr.qh[u][ks][0];
-        const uint32_t b1 = (gid & 1) ? 0u : qr.qh[u][ks][1];
-        mma_f16(c, za[ks][0], 0u, za[ks][1], 0u, b0, b1);
-      }
-      zb[u] = c[0];   // group gid, head 4u + tid
+      for (int ks = 0; ks < KS; ++ks)
+        mma_f16(c, za[ks][0], 0u, za[ks][1], 0u, qr.qh[u][ks][0], qr.qh[u][ks][1]);
+      zb[u] = c[0];   // group gid, head 4u + tid ("hi" column)
     }
   }
 
@@ -374,7 +396,7 @@ __device__ void packed_warp(WarpState<D, GQ>& st, const QRegs<D, GQ>& qr, const 
         static_for<KS>([&](auto KS_) {
           constexpr int K = decltype(KS_)::value;
           uint32_t a[4];
-          key_afrag<D, BITS, MT, K>(kw, a);
+          key_afrag<D, BITS, MT, K>(kw, cm, a);
 #pragma unroll
           for (int u = 0; u < NH; ++u)
             mma_f16(acc[u][MT][K & 1], a[0], a[1], a[2], a[3], bq[u][K][0], bq[u][K][1]);
@@ -437,7 +459,7 @@ __device__ void packed_warp(WarpState<D, GQ>& st, const QRegs<D, GQ>& qr, const 
           static_for<2>([&](auto H_) {
             constexpr int MV = 2 * GC + decltype(H_)::value;
             uint32_t a[4];
-            value_afrag<BITS, MV, K>(vw, a);
+            value_afrag<BITS, MV, K>(vw, cm, a);
             mma_f16(st.o[u][MV], z0, z0, z1, z1, bz0, bz1);
             mma_f16(st.o[u][MV], a[0], a[1], a[2], a[3], b0, b1);
           });
@@ -570,10 +592,10 @@ struct DecCfg {
   static constexpr int QB = GQ * D * 2;              // one unit's queries (bf16)
   static constexpr int DEPW = dep_floats(D, GQ);     // floats of one partial state
   static constexpr int per_warp = 2 * SLOT + 2 * QB + 2 * DEPW * 4 + 2 * 8 + 4;
-  // warps per CTA: as many as shared memory holds, at most 12 (8 with eight query
-  // heads, whose state needs more registers per thread)
+  // warps per CTA: as many as shared memory holds, at most 12 (8 with four or more
+  // query heads, whose state needs more registers per thread than 12 warps leave)
   static constexpr int pick(int nw) { return nw * per_warp <= 227 * 1024 ? nw : pick(nw - 1); }
-  static constexpr int NW = pick(GQ > 4 ? 8 : 12);
+  static constexpr int NW = pick(GQ > 2 ? 8 : 12);
   static constexpr int kThreads = NW * 32;
   static constexpr int oRing = 0;                    // [NW][2][SLOT]
   static constexpr int oDep = oRing + NW * 2 * SLOT; // [NW][2][DEPW] fp32 partial states
@@ -749,12 +771,21 @@ __device__ __forceinline__ void mbar_expect(uint64_t* bar, uint32_t bytes) {
                :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-// An even split of [0, T) into N contiguous ranges: range i is [first(i), first(i+1)),
-// and owner(c) is the range holding c.
+// An even split of [base, base + T) into N contiguous ranges: range i is
+// [first(i), first(i+1)), and owner(c) is the range holding c. When T * N < 2^32
+// (every launch of ordinary size) all products fit 32 bits: 32-bit divisions.
 struct Split {
   long long T, N, base;
-  __device__ long long first(long long i) const { return base + i * T / N; }
-  __device__ long long owner(long long c) const { return ((c - base + 1) * N - 1) / T; }
+  __device__ long long first(long long i) const {
+    if (T * N < (1LL << 32)) return base + (long long)((unsigned)i * (unsigned)T / (unsigned)N);
+    return base + i * T / N;
+  }
+  __device__ long long owner(long long c) const {
+    const long long x = c - base;
+    if (T * N < (1LL << 32))
+      return (long long)((((unsigned)x + 1u) * (unsigned)N - 1u) / (unsigned)T);
+    return ((x + 1) * N - 1) / T;
+  }
 };
 
 template <int D, int GQ, int BMASK>

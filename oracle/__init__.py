@@ -28,7 +28,7 @@ CPU-baseline leg of `bench.py` may import it; the product path never routes here
 from .budgets import plan_budgets
 from .snapkv import window_scores, max_pool, select_topk, snapkv_select
 from .sinks import sinks_window_select
-from .acumul import acumul_scores, acumul_select, acumul_columns
+from .acumul import acumul_scores, acumul_select, acumul_columns, prefill_attention
 from .variance import (score_variance, layer_variance, variance_weights,
                        plan_budgets_weighted)
 from .quant import (quantize_group, quantize_keys, quantize_values, dequantize_keys,

@@ -107,3 +107,25 @@ def acumul_columns(q_group: np.ndarray, k: np.ndarray, cols, key_block: int = KE
             total += float(np.exp(s[:, j] - m).sum())
         out.append(total)
     return np.array(out)
+
+
+def prefill_attention(q_group: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """X_O of one kv head: the causal softmax attention output of every prompt query
+    (MiniKV §4.3, Figure 9: the selective flash-attention kernel returns it beside
+    A_cumul). Each row is normalised over its own visible keys:
+
+        X_O[h, i] = sum over j <= i of softmax_j(q_hi . k_j / sqrt(d)) v_j.
+
+    q_group: [g][n][d], k and v: [n][d] (float64). Returns [g][n][d]."""
+    q_group = np.asarray(q_group, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    g, n, d = q_group.shape
+    scale = 1.0 / math.sqrt(d)
+    out = np.empty((g, n, d))
+    visible = np.tril(np.ones((n, n), dtype=bool))
+    for h in range(g):
+        s = np.where(visible, (q_group[h] @ k.T) * scale, -np.inf)
+        w = np.exp(s - s.max(axis=1, keepdims=True))
+        out[h] = (w / w.sum(axis=1, keepdims=True)) @ v
+    return out

@@ -145,3 +145,75 @@ def test_sampled_columns_match_the_full_computation(n, g, block):
     cols = sorted(set([0, 1, block - 1, block, n // 2, n - 2, n - 1]) & set(range(n)))
     np.testing.assert_allclose(acumul_columns(q, k, cols, block),
                                acumul_scores(q, k, block)[cols], rtol=1e-12)
+
+
+# ---------------------------------------------------------------- X_O
+from oracle.acumul import prefill_attention  # noqa: E402
+
+
+def test_prefill_attention_identical_keys_is_running_mean():
+    """Equal logits in every row: row i averages v_0 .. v_i (a closed form)."""
+    rng = np.random.default_rng(5)
+    n, d = 40, 8
+    q = rng.standard_normal((2, n, d))
+    k = np.tile(rng.standard_normal(d), (n, 1))
+    v = rng.standard_normal((n, d))
+    want = np.cumsum(v, axis=0) / np.arange(1, n + 1)[:, None]
+    got = prefill_attention(q, k, v)
+    for h in range(2):
+        np.testing.assert_allclose(got[h], want, rtol=1e-13, atol=1e-13)
+
+
+def test_prefill_attention_two_keys_logistic():
+    """Row 1 sees keys 0 and 1 only: its weight on key 1 is the logistic function of
+    the logit difference (q.k1 - q.k0)/sqrt(d); row 0 returns v_0 exactly."""
+    d = 4
+    q = np.zeros((1, 2, d))
+    q[0, 1] = [1.0, 2.0, 0.0, 0.0]
+    k = np.array([[0.5, 0.0, 0.0, 0.0], [0.0, 1.0, 0.0, 0.0]])
+    v = np.array([[1.0, 0.0, 3.0, 0.0], [0.0, 2.0, 0.0, -1.0]])
+    got = prefill_attention(q, k, v)
+    np.testing.assert_array_equal(got[0, 0], v[0])
+    t = (2.0 - 0.5) / math.sqrt(d)
+    w1 = 1.0 / (1.0 + math.exp(-t))
+    np.testing.assert_allclose(got[0, 1], (1 - w1) * v[0] + w1 * v[1], rtol=1e-14)
+
+
+def test_prefill_attention_dominant_key_selects_its_value():
+    """A key far more aligned with every query than the rest takes (almost) all the
+    weight of every row that sees it; rows before it keep their own softmax."""
+    rng = np.random.default_rng(6)
+    n, d, j = 30, 16, 7
+    q = np.abs(rng.standard_normal((1, n, d))) + 1.0
+    k = 0.01 * rng.standard_normal((n, d))
+    k[j] = 100.0
+    v = rng.standard_normal((n, d))
+    got = prefill_attention(q, k, v)
+    np.testing.assert_allclose(got[0, j:], np.tile(v[j], (n - j, 1)), atol=1e-12)
+
+
+def test_prefill_attention_is_shift_invariant_per_row():
+    """Adding a key-independent vector to every key shifts row i's logits by a
+    constant (q_i . c): the output does not change."""
+    rng = np.random.default_rng(7)
+    n, d = 25, 8
+    q = rng.standard_normal((3, n, d))
+    k = rng.standard_normal((n, d))
+    v = rng.standard_normal((n, d))
+    c = rng.standard_normal(d)
+    np.testing.assert_allclose(prefill_attention(q, k + c, v), prefill_attention(q, k, v),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_attention_last_row_is_dense_decode():
+    """The last prompt row attends to every prompt key: it equals one step of plain
+    dense attention computed directly (the special case the cache must reach with
+    the full budget and 16-bit storage)."""
+    rng = np.random.default_rng(8)
+    n, d = 33, 8
+    q = rng.standard_normal((1, n, d))
+    k = rng.standard_normal((n, d))
+    v = rng.standard_normal((n, d))
+    s = k @ q[0, -1] / math.sqrt(d)
+    w = np.exp(s - s.max())
+    np.testing.assert_allclose(prefill_attention(q, k, v)[0, -1], (w / w.sum()) @ v, rtol=1e-13)
