@@ -394,7 +394,7 @@ def run_gpu(args):
 
     # selection by the full-prompt cumulated attention (every prompt query, un-normalised
     # column sums): the first two layers compressed with it, outside the timed steps
-    acumul = None
+    acumul = attention = None
     if not args.no_acumul:
         LA = min(2, L)
         qfull = [synth.prompt_queries(spec, l, device=dev) for l in range(LA)]
@@ -418,7 +418,30 @@ def run_gpu(args):
                   "note": "selection by MiniKV's full-prompt cumulated attention (key blocks of "
                           "128, running row maxima); two MMAs per tile (S and S^T) on the "
                           "tensor cores"}
-        del qfull
+        # the selective flash-attention: the same selection plus the prefill attention
+        # output X_O of every query (one pass, three products per key tile)
+        xo = torch.empty(B, Hq, spec.prompt_len, D, dtype=torch.bfloat16, device=dev)
+        axs = []
+        for i in range(4):
+            K.kvc_cache_reset(cache)
+            ca0.record(stream)
+            for l in range(LA):
+                x = prompt[l]
+                K.kvc_prefill_attention(cache, l, qfull[l], x["k"], x["v"], xo)
+            ca1.record(stream)
+            torch.cuda.synchronize()
+            if i > 0:
+                axs.append(ca0.elapsed_time(ca1))
+        x_ms = statistics.mean(axs) / LA
+        # dense causal attention: q.k and p.v over every causal (query, key) pair
+        x_flops = 4 * D * B * Hq * spec.prompt_len * (spec.prompt_len + 1) // 2
+        attention = {"ms_per_layer": x_ms, "flops": x_flops, "layers": LA,
+                     "tflops": x_flops / (x_ms / 1e3) / 1e12,
+                     "note": "MiniKV's selective flash-attention: X_O (bf16) of every prompt "
+                             "query plus the cumulated-attention selection and packing; flops "
+                             "are those of dense causal attention (q.k and p.v); the kernel also "
+                             "forms S^T for the fp32 column sums"}
+        del qfull, xo
 
     # 16-bit storage (every kept token exact in the bf16 window), same selection and
     # budgets: decode launches over the exact cache, outside the timed steps
@@ -508,6 +531,8 @@ def run_gpu(args):
         "score_variance": variance,
         "compress_acumul": None if acumul is None else dict(
             acumul, frac=acumul["tflops"] / tc),
+        "prefill_attention": None if attention is None else dict(
+            attention, frac=attention["tflops"] / tc),
         "compress_sinks": None if sink_ms is None else {
             "ms_per_layer": sink_ms, "bytes": sink_bytes,
             "frac": sink_bytes / (hbm * 1e9) / (sink_ms * L / 1e3),

@@ -196,6 +196,25 @@ kvc_status kvc_prefill_acumul(kvc_cache* cache, int32_t layer, const void* q_ful
                               const void* v, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * kvc_prefill_attention -- the selective flash-attention of MiniKV §4.3 and
+ *   Figure 9: one pass over the layer's prompt that returns the causal attention
+ *   output X_O of every prompt query and, from the same tiles, the cumulated
+ *   attention A_cumul by which the layer is then compressed exactly as
+ *   kvc_prefill_acumul compresses it (same scores, kept sets and packing).
+ *   x_out: device bf16 [batch][n_q_heads][prompt_len][head_dim], 16-byte aligned
+ *          (written): X_O[i] = sum over keys j <= i of softmax(q_i . k_j /
+ *          sqrt(head_dim)) v_j, accumulated in fp32 on the tensor cores with the
+ *          weights rounded to bf16 (|error| <= 2^-8 of the largest |v| of the
+ *          row's keys, plus the bf16 rounding of the output).
+ *   q_full, k, v as for kvc_prefill_acumul (v is read by the attention too).
+ *   With a budget that keeps every token no scores are formed; X_O still is.
+ *   Errors: KVC_E_ARG (null pointer, misaligned x_out), KVC_E_SHAPE, KVC_E_STATE,
+ *   KVC_E_CUDA, KVC_E_TIMEOUT (a wait of an earlier call on the cache gave up).
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_prefill_attention(kvc_cache* cache, int32_t layer, const void* q_full,
+                                 const void* k, const void* v, void* x_out, void* stream);
+
+/* ---------------------------------------------------------------------------
  * kvc_prefill_sinks -- like kvc_prefill_compress with the attention-sink +
  *   recent-token selection in place of the scored one (blog "KV Cache
  *   Compression: Eviction and Quantization", "Measured on a real model": the first

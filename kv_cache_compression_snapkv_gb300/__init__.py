@@ -67,6 +67,7 @@ _SIGS = {
     "kvc_prefill_selected": [_P, _I, _P, _I, _P, _P, _P],
     "kvc_prefill_sinks": [_P, _I, _I, _P, _P, _P],
     "kvc_prefill_acumul": [_P, _I, _P, _P, _P, _P],
+    "kvc_prefill_attention": [_P, _I, _P, _P, _P, _P, _P],
     "kvc_cache_create": [ctypes.POINTER(KvcDims), _P, ctypes.POINTER(ctypes.c_void_p)],
     "kvc_cache_create_layers": [ctypes.POINTER(KvcDims), _P, _P, ctypes.POINTER(ctypes.c_void_p)],
     "kvc_append": [_P, _I, _P, _P, _P],
@@ -222,6 +223,14 @@ def kvc_prefill_acumul(cache: Cache, layer: int, q_full, k, v, stream=None):
                                    _stream(stream)), "kvc_prefill_acumul")
 
 
+def kvc_prefill_attention(cache: Cache, layer: int, q_full, k, v, x_out, stream=None):
+    """MiniKV's selective flash-attention of `layer`: the causal attention output of
+    every prompt query into x_out (bf16 [B][Hq][n][d]) and, from the same tiles, the
+    selection by the cumulated attention, then packing."""
+    _check(_lib.kvc_prefill_attention(cache.handle, layer, _ptr(q_full), _ptr(k), _ptr(v),
+                                      _ptr(x_out), _stream(stream)), "kvc_prefill_attention")
+
+
 def kvc_append(cache: Cache, layer: int, k_new, v_new, stream=None):
     _check(_lib.kvc_append(cache.handle, layer, _ptr(k_new), _ptr(v_new), _stream(stream)),
            "kvc_append")
@@ -334,6 +343,7 @@ __all__ = ["KvcDims", "KvcError", "Cache", "make_dims", "dims_from_spec", "kvc_p
            "kvc_append_layers", "kvc_decode_attn", "kvc_decode_step", "kvc_free",
            "kvc_layer_info_get", "kvc_export_layer", "kvc_scores_layer", "kvc_cache_reset",
            "kvc_plan_budgets_weighted", "kvc_score_variance", "kvc_prefill_acumul",
+           "kvc_prefill_attention",
            "kvc_launch_count", "kvc_check_device", "kvc_select_noalloc",
            "kvc_select_noalloc_check", "kvc_set_wait_limit", "LIB_PATH",
            "exported_symbols"]

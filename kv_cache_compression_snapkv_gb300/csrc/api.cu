@@ -497,6 +497,41 @@ kvc_status kvc_prefill_acumul(kvc_cache* c, int32_t layer, const void* q_full, c
   return finish_prefill(c, layer, n_kept, kp, k, v, s);
 }
 
+kvc_status kvc_prefill_attention(kvc_cache* c, int32_t layer, const void* q_full, const void* k,
+                                 const void* v, void* x_out, void* stream) {
+  if (!c || !k || !v || !q_full || !x_out) return KVC_E_ARG;
+  if (reinterpret_cast<uintptr_t>(x_out) % 16) return KVC_E_ARG;
+  if (kvc_status pe = pending_error(c)) return pe;
+  if (layer < 0 || layer >= c->dims.n_layers) return KVC_E_ARG;
+  LayerState& ls = c->L[layer];
+  if (ls.prefilled) return KVC_E_STATE;
+  const int ns = c->dims.prompt_len - c->dims.obs_window;
+  const int n_kept = ls.budget < ns ? ls.budget : ns;
+  if (!window_fits(c->dims, ls.bits, ls.R, n_kept)) return KVC_E_SHAPE;
+  const int g = c->dims.n_q_heads / c->dims.n_kv_heads;
+  if (g > 16 || 128 % g != 0) return KVC_E_SHAPE;
+  DeviceGuard dg(c->device);
+  if (!dg.ok) return KVC_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool scoring = n_kept < ns;
+  cudaError_t e = kvc::launch_acumul_xo(c->dims, static_cast<const __nv_bfloat16*>(q_full),
+                                        static_cast<const __nv_bfloat16*>(k),
+                                        static_cast<const __nv_bfloat16*>(v),
+                                        scoring ? c->scores : nullptr,
+                                        static_cast<__nv_bfloat16*>(x_out), c->err, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (!scoring) {                     // the budget keeps every token
+    ls.scored = 0;
+    return finish_prefill(c, layer, n_kept, nullptr, k, v, s);
+  }
+  int32_t* kp = ls.kept_ptr;
+  e = kvc::launch_pool_topk(c, layer, kp, n_kept, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  ls.scored = 1;
+  c->last_scored_layer = layer;
+  return finish_prefill(c, layer, n_kept, kp, k, v, s);
+}
+
 kvc_status kvc_prefill_sinks(kvc_cache* c, int32_t layer, int32_t n_sinks, const void* k,
                              const void* v, void* stream) {
   if (!c || !k || !v || n_sinks < 0) return KVC_E_ARG;

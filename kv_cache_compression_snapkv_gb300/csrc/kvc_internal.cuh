@@ -278,6 +278,12 @@ cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
 // [B][Hq][n][d]. Zeroes the scores first (stream-ordered); err may be NULL.
 cudaError_t launch_acumul(const kvc_dims& d, const __nv_bfloat16* q_full, const __nv_bfloat16* k,
                           float* scores, unsigned* err, cudaStream_t stream);
+// The same scores (skipped when scores is NULL) and, from the same tiles, the
+// causal attention output of every prompt query x_out [B][Hq][n][d] (bf16); v is
+// [B][Hkv][n][d].
+cudaError_t launch_acumul_xo(const kvc_dims& d, const __nv_bfloat16* q_full,
+                             const __nv_bfloat16* k, const __nv_bfloat16* v, float* scores,
+                             __nv_bfloat16* x_out, unsigned* err, cudaStream_t stream);
 // Population variance of each of `units` rows of m scores (fp32 out, one per row).
 cudaError_t launch_score_variance(const float* scores, int units, int m, float* var,
                                   cudaStream_t stream);

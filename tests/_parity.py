@@ -25,7 +25,7 @@ import numpy as np
 import torch
 
 import synth
-from oracle import OracleCache, sinks_window_select, snapkv_select
+from oracle import OracleCache, prefill_attention, sinks_window_select, snapkv_select
 
 DECODE_RTOL = 2e-3
 TIE_RTOL = 1e-5
@@ -46,6 +46,8 @@ class Report:
     decode_checked: int = 0
     score_err: float = 0.0
     rebuilt_units: int = 0
+    xo_err: float = 0.0
+    xo_checked: int = 0
     notes: list = field(default_factory=list)
 
 
@@ -109,6 +111,20 @@ def check_export(ex: dict, oc: OracleCache, heads, rep: Report):
         rep.codes_compared += T
 
 
+def check_prefill_attention(x_gpu, q_group, k, v, rep: Report):
+    """The GPU's X_O of one kv head ([g][n][d], bf16) against the oracle's. The GPU
+    rounds the attention weights to bf16 (relative 2^-9) before the product with
+    V, and the output to bf16 (relative 2^-9): element by element
+    |x - x*| <= 2^-9 (max |v| over the row's keys) + 2^-9 |x*|; tested with 2^-8."""
+    ref = prefill_attention(q_group, k, v)
+    vmax = np.maximum.accumulate(np.abs(v).max(axis=1))       # max |v| over keys <= i
+    bound = 2.0 ** -8 * (vmax[None, :, None] + np.abs(ref))
+    err = np.abs(x_gpu - ref)
+    rep.xo_err = max(rep.xo_err, float((err / np.maximum(vmax[None, :, None], 1e-30)).max()))
+    rep.xo_checked += ref.size
+    assert np.all(err <= bound), f"X_O off by {float((err - bound).max()):.3g} over the bound"
+
+
 def decode_error(o_gpu, o_ora):
     """max over (b, head) of ||o - o*||_inf / ||o*||_inf."""
     diff = np.abs(o_gpu - o_ora).max(axis=-1)
@@ -123,7 +139,9 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
     selection: "score" (GPU scores and selects; the oracle does the same),
                "oracle" (the GPU is given the oracle's kept positions) or
                ("sinks", s) (both keep s attention sinks + the most recent tokens) or
-               "acumul" (both score by the full-prompt cumulated attention).
+               "acumul" (both score by the full-prompt cumulated attention) or
+               "attention" (as "acumul", through the selective flash-attention that
+               also returns the prefill attention output, checked against the oracle).
     budgets: per-layer budgets to use instead of the spec's schedule.
     layer_bits: per-layer storage precision (2, 4 or 16) of one mixed cache.
     """
@@ -154,7 +172,8 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
             sel = sinks_window_select(n - a, bud, sinks)
             oc.prefill(k_np, v_np, a, kept=[[sel] * Hk for _ in range(B)])
         else:
-            qf = synth.prompt_queries(spec, layer, device="cpu") if selection == "acumul" else None
+            qf = (synth.prompt_queries(spec, layer, device="cpu")
+                  if selection in ("acumul", "attention") else None)
             oc.prefill(k_np, v_np, a, budget=bud if scoring else None, q_obs=q_np,
                        pool_kernel=spec.pool_kernel, q_full=None if qf is None else np64(qf))
         kd, vd = x["k"].to(dev), x["v"].to(dev)
@@ -185,6 +204,19 @@ def run_small(spec, steps, selection="score", layers=None, multi_layer_decode=Tr
                 if cache is None:
                     cache = K.kvc_cache_create(dims, budgets)
                 K.kvc_prefill_acumul(cache, layer, qf.to(dev), kd, vd)
+            elif selection == "attention":
+                if cache is None:
+                    cache = K.kvc_cache_create(dims, budgets)
+                xo = torch.empty(B, Hq, n, D, dtype=torch.bfloat16, device=dev)
+                K.kvc_prefill_attention(cache, layer, qf.to(dev), kd, vd, xo)
+                torch.cuda.synchronize()
+                g = Hq // Hk
+                qf64 = np64(qf)
+                for b in range(B):
+                    for h in range(Hk):
+                        check_prefill_attention(np64(xo[b, h * g:(h + 1) * g]),
+                                                qf64[b, h * g:(h + 1) * g], k_np[b, h],
+                                                v_np[b, h], rep)
             else:
                 cache = K.kvc_prefill_compress(dims, budgets, layer, qd, kd, vd, cache=cache)
             sc = torch.empty(B, Hk, n - a, device=dev)

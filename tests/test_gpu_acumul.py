@@ -35,6 +35,18 @@ CASES = {
 
 
 @pytest.mark.parametrize("name", list(CASES))
+def test_prefill_attention_parity(name):
+    """The selective flash-attention (MiniKV §4.3, Figure 9): the prefill attention
+    output X_O of every query against the oracle, and the selection, store and
+    decode it feeds exactly as for kvc_prefill_acumul."""
+    spec, steps = CASES[name]
+    rep = run_small(spec, steps, selection="attention")
+    print(f"{name}: X_O elements={rep.xo_checked} worst |err|/max|v|={rep.xo_err:.2e} "
+          f"excused={rep.excused} score_err={rep.score_err:.2e} decode_err={rep.decode_err:.2e}")
+    assert rep.xo_checked > 0 and rep.kept_compared > 0 and rep.decode_checked > 0
+
+
+@pytest.mark.parametrize("name", list(CASES))
 def test_acumul_parity(name):
     spec, steps = CASES[name]
     rep = run_small(spec, steps, selection="acumul")
@@ -90,3 +102,55 @@ def test_acumul_keep_all_needs_no_queries():
     assert info["n_kept"] == 300 - 16 and info["packed_tokens"] == 256
     K.kvc_check_device(cache)
     cache.close()
+
+
+def test_prefill_attention_full_prompt_length_sampled_rows():
+    """Llama-3-8B prompt (32,768 tokens, GQA 4): X_O of sampled rows of one unit
+    (the first key block, the middle, the observation window) against the oracle's
+    definition evaluated for those rows only, and the scores equal to those of
+    kvc_prefill_acumul on the same inputs."""
+    K = kvc()
+    spec = synth.workload(2)
+    n, a, g, D = spec.prompt_len, spec.obs_window, spec.gqa, spec.head_dim
+    ns = n - a
+    dims = K.dims_from_spec(spec, max_new_tokens=4)
+    budgets = K.kvc_plan_budgets(dims, spec.schedule, spec.avg_budget, spec.pyramid_depth)
+    x = synth.layer_inputs(spec, 0, device="cuda")
+    qf = synth.prompt_queries(spec, 0, device="cuda")
+    cache = K.kvc_cache_create(dims, budgets)
+    xo = torch.empty(spec.batch, spec.n_q_heads, n, D, dtype=torch.bfloat16, device="cuda")
+    K.kvc_prefill_attention(cache, 0, qf, x["k"], x["v"], xo)
+    sc = torch.empty(spec.batch, spec.n_kv_heads, ns, device="cuda")
+    K.kvc_scores_layer(cache, sc)
+    kept = K.kvc_export_layer(cache, 0)["kept"]
+    K.kvc_check_device(cache)
+    cache.close()
+    ref_cache = K.kvc_cache_create(dims, budgets)
+    K.kvc_prefill_acumul(ref_cache, 0, qf, x["k"], x["v"])
+    sc_ref = torch.empty_like(sc)
+    K.kvc_scores_layer(ref_cache, sc_ref)
+    kept_ref = K.kvc_export_layer(ref_cache, 0)["kept"]
+    ref_cache.close()
+    rel = ((sc - sc_ref).abs() / sc_ref.abs().clamp_min(1e-30)).max().item()
+    assert rel <= 1e-5, rel
+    diff = (kept != kept_ref).sum().item()
+    print(f"scores vs kvc_prefill_acumul: {rel:.2e}; kept indices differing: {diff}")
+    assert diff <= 8            # summation order of the atomics: near-ties only
+    rng = np.random.default_rng(1)
+    rows = np.concatenate([[0, 1, 127, 128], rng.choice(np.arange(129, ns), 6, replace=False),
+                           [ns, n - 1]])
+    h = 3
+    k64, v64 = np64(x["k"][0, h]), np64(x["v"][0, h])
+    worst = 0.0
+    for hh in range(g):
+        q = np64(qf[0, h * g + hh])
+        for i in rows:
+            s_ = k64[:i + 1] @ q[i] / np.sqrt(D)
+            w = np.exp(s_ - s_.max())
+            ref = (w / w.sum()) @ v64[:i + 1]
+            got = np64(xo[0, h * g + hh, i])
+            vmax = np.abs(v64[:i + 1]).max()
+            err = np.abs(got - ref)
+            assert np.all(err <= 2.0 ** -8 * (vmax + np.abs(ref))), (hh, i, err.max())
+            worst = max(worst, float(err.max() / vmax))
+    print(f"sampled rows {rows.tolist()}: worst |err|/max|v| {worst:.2e}")
