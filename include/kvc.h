@@ -187,8 +187,9 @@ kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets,
  *   k, v:   device bf16 [batch][n_kv_heads][prompt_len][head_dim].
  *   Needs 128 % (n_q_heads / n_kv_heads) == 0 and n_q_heads / n_kv_heads <= 16.
  *   The scores stay readable through kvc_scores_layer / kvc_score_variance until
- *   the next scoring call. Atomic additions make the scores' last bits depend on
- *   timing.
+ *   the next scoring call. The row blocks' contributions are added as 64-bit
+ *   fixed-point integers (units of 2^-40), so the scores and kept sets are the
+ *   same on every run. Allocates, on first use, 8 bytes per score for them.
  *   Errors: KVC_E_ARG, KVC_E_SHAPE (group size, or initial window not shorter
  *   than R), KVC_E_STATE (layer already compressed), KVC_E_CUDA.
  * ------------------------------------------------------------------------- */

@@ -82,7 +82,7 @@ struct AcArgs {
   int rblocks;     // row blocks per unit
   long long items; // units * rblocks
   float sl2;       // log2(e) / sqrt(d)
-  float* scores;   // [unit][ns], zero before the launch
+  unsigned long long* fx;   // [unit][ns] fixed-point column sums, zero before the launch
   unsigned* err;
 };
 
@@ -125,6 +125,28 @@ __device__ __forceinline__ void cursor_next_item(Cursor& c, int cta, int G, cons
   if (c.live) c.it = item_of(i, a);
   c.t = 0;
   c.jn += 2;
+}
+
+// The items' contributions to a score are added as 64-bit fixed-point integers
+// (units of 2^-40): integer addition does not depend on the order the items
+// arrive in, so the scores (and the kept sets) are the same on every run. A
+// score is at most g * n <= 16 * 2^19 (2^23), far inside the 2^63 / 2^40 range.
+constexpr float kFixScale = 1099511627776.f;   // 2^40
+__device__ __forceinline__ void add_fixed(unsigned long long* dst, float v) {
+  atomicAdd(dst, __float2ull_rn(v * kFixScale));
+}
+__global__ void fixed_to_float_kernel(const unsigned long long* __restrict__ fx, float* __restrict__ out,
+                                      long long count) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < count;
+       i += (long long)gridDim.x * blockDim.x)
+    out[i] = __ull2float_rn(fx[i]) * (1.f / kFixScale);
+}
+cudaError_t fixed_to_float(const unsigned long long* fx, float* out, long long count,
+                           cudaStream_t stream) {
+  fixed_to_float_kernel<<<(int)std::min<long long>(1024, (count + 255) / 256), 256, 0, stream>>>(
+      fx, out, count);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -383,7 +405,7 @@ acumul_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         // the halves meet in shared memory; one atomic add per key
         if (half == 1) gpart[r] = acc;
         named_bar(1 + x, ET);
-        if (half == 0 && ok && key < a.ns) atomicAdd(a.scores + (size_t)it.unit * a.ns + key,
+        if (half == 0 && ok && key < a.ns) add_fixed(a.fx + (size_t)it.unit * a.ns + key,
                                                     acc + gpart[r]);
       }
     }
@@ -636,8 +658,17 @@ acumul_xo_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         for (int c0 = 0; c0 < 64; c0 += 32) {
           float v[32];
           tc::tmem_ld32(c1 + (uint32_t)c0, v);
+          if (masked) {
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) pm = jj + c0 <= lim0 ? fmaxf(pm, v[jj]) : pm;
+            for (int jj = 0; jj < 32; ++jj) v[jj] = jj + c0 <= lim0 ? v[jj] : -INFINITY;
+          }
+          float ma = v[0], mb = v[16];
+#pragma unroll
+          for (int jj = 1; jj < 15; jj += 2) {
+            ma = max3(ma, v[jj], v[jj + 1]);
+            mb = max3(mb, v[jj + 16], v[jj + 17]);
+          }
+          pm = max3(pm, max3(ma, v[15], v[31]), mb);
         }
         gmax[half * 128 + r] = pm;
         named_bar(1, ET);
@@ -677,15 +708,29 @@ acumul_xo_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
           for (int c0 = 0; c0 < 64; c0 += 32) {
             float v[32];
             tc::tmem_ld32(c1 + (uint32_t)c0, v);
-            uint32_t pk[16];
+            // paired fp32 arithmetic; a hidden key's logit becomes -inf (weight 0)
+            const float2 s2 = make_float2(a.sl2, a.sl2), n2 = make_float2(nref, nref);
 #pragma unroll
             for (int jj = 0; jj < 32; jj += 2) {
-              const float p0 = jj + c0 <= lim0 ? exp2f(fmaf(v[jj], a.sl2, nref)) : 0.f;
-              const float p1 = jj + 1 + c0 <= lim0 ? exp2f(fmaf(v[jj + 1], a.sl2, nref)) : 0.f;
-              lsum += p0 + p1;
-              const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+              const float2 e = __ffma2_rn(make_float2(v[jj], v[jj + 1]), s2, n2);
+              v[jj] = e.x;
+              v[jj + 1] = e.y;
+            }
+            if (masked) {
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) v[jj] = jj + c0 <= lim0 ? v[jj] : -INFINITY;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(v[jj]) : "f"(v[jj]));
+            uint32_t pk[16];
+            float2 ls = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 2) {
+              ls = __fadd2_rn(ls, make_float2(v[jj], v[jj + 1]));
+              const __nv_bfloat162 h = __floats2bfloat162_rn(v[jj], v[jj + 1]);
               pk[jj / 2] = *reinterpret_cast<const uint32_t*>(&h);
             }
+            lsum += ls.x + ls.y;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               const int chunk = c0 / 8 + q4;      // 16-byte chunk of the 128-byte row
@@ -704,20 +749,43 @@ acumul_xo_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         const float* nm = gnegm + half * 64;
         const int key = key0 + r;
         float acc = 0.f;
-        if (key0 < a.ns && a.scores) {
+        if (key0 < a.ns && a.fx) {
 #pragma unroll 1
           for (int c0 = 0; c0 < 64; c0 += 32) {
             float v[32];
             tc::tmem_ld32(c2 + (uint32_t)c0, v);
+            if (!masked) {
+              const float4* nm4 = reinterpret_cast<const float4*>(nm + c0);
+              const float2 s2 = make_float2(a.sl2, a.sl2);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const int row = half * 64 + c0 + jj;
-              const int pos = it.p0 + row % a.P;
-              const bool vis = !masked || (pos < a.n && key <= pos);
-              v[jj] = vis ? exp2f(fmaf(v[jj], a.sl2, nm[c0 + jj])) : 0.f;
+              for (int jj = 0; jj < 32; jj += 4) {
+                const float4 b4 = nm4[jj / 4];
+                const float2 lo = __ffma2_rn(make_float2(v[jj], v[jj + 1]), s2,
+                                             make_float2(b4.x, b4.y));
+                const float2 hi = __ffma2_rn(make_float2(v[jj + 2], v[jj + 3]), s2,
+                                             make_float2(b4.z, b4.w));
+                v[jj] = lo.x; v[jj + 1] = lo.y; v[jj + 2] = hi.x; v[jj + 3] = hi.y;
+              }
+            } else {
+              // rows are head-major: row = head * P + (position - p0), P a power of two
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const int pos = it.p0 + ((half * 64 + c0 + jj) & (a.P - 1));
+                v[jj] = (pos < a.n && key <= pos) ? fmaf(v[jj], a.sl2, nm[c0 + jj]) : -INFINITY;
+              }
             }
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) acc += v[jj];
+            for (int jj = 0; jj < 32; ++jj) asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(v[jj]) : "f"(v[jj]));
+            float2 sum[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              sum[q] = __fadd2_rn(make_float2(v[2 * q], v[2 * q + 1]),
+                                  make_float2(v[2 * q + 16], v[2 * q + 17]));
+#pragma unroll
+            for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+              for (int q = 0; q < w; ++q) sum[q] = __fadd2_rn(sum[q], sum[q + w]);
+            acc += sum[0].x + sum[0].y;
           }
         }
         tc::fence_before_sync();
@@ -725,8 +793,8 @@ acumul_xo_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         if (lane == 0) tc::mbar_arrive(sfree);
         if (half == 1) gpart[r] = acc;
         named_bar(1, ET);
-        if (half == 0 && ok && key < a.ns && a.scores)
-          atomicAdd(a.scores + (size_t)it.unit * a.ns + key, acc + gpart[r]);
+        if (half == 0 && ok && key < a.ns && a.fx)
+          add_fixed(a.fx + (size_t)it.unit * a.ns + key, acc + gpart[r]);
       }
       // --- the item's attention output: O / l of row r, this half's d columns
       if (ok) ok = tc::mbar_wait(pvdone, (uint32_t)((k - 1) & 1), a.err, kErrAcEpilogue);
@@ -809,7 +877,7 @@ cudaError_t ac_make_map(CUtensorMap* m, const void* base, long long rows, int d,
 
 template <int D>
 cudaError_t run_acumul(const kvc_dims& d, const __nv_bfloat16* q_full, const __nv_bfloat16* k,
-                       float* scores, unsigned* err, cudaStream_t stream) {
+                       float* scores, unsigned long long* fx, unsigned* err, cudaStream_t stream) {
   using C = AcCfg<D>;
   const int g = d.n_q_heads / d.n_kv_heads;
   AcArgs a{};
@@ -823,9 +891,9 @@ cudaError_t run_acumul(const kvc_dims& d, const __nv_bfloat16* q_full, const __n
   a.rblocks = (a.n + a.P - 1) / a.P;
   a.items = (long long)a.units * a.rblocks;
   a.sl2 = 1.4426950408889634f / sqrtf((float)D);
-  a.scores = scores;
+  a.fx = fx;
   a.err = err;
-  cudaError_t e = cudaMemsetAsync(scores, 0, (size_t)a.units * a.ns * 4, stream);
+  cudaError_t e = cudaMemsetAsync(fx, 0, (size_t)a.units * a.ns * 8, stream);
   if (e != cudaSuccess) return e;
   CUtensorMap mk, mq;
   if ((e = ac_make_map(&mk, k, (long long)a.units * a.n, D, 128)) != cudaSuccess) return e;
@@ -842,13 +910,13 @@ cudaError_t run_acumul(const kvc_dims& d, const __nv_bfloat16* q_full, const __n
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   count_launches(1);
-  return cudaSuccess;
+  return fixed_to_float(fx, scores, (long long)a.units * a.ns, stream);
 }
 
 template <int D>
 cudaError_t run_acumul_xo(const kvc_dims& d, const __nv_bfloat16* q_full, const __nv_bfloat16* k,
-                          const __nv_bfloat16* v, float* scores, __nv_bfloat16* x_out,
-                          unsigned* err, cudaStream_t stream) {
+                          const __nv_bfloat16* v, float* scores, unsigned long long* fx,
+                          __nv_bfloat16* x_out, unsigned* err, cudaStream_t stream) {
   using C = XoCfg<D>;
   const int g = d.n_q_heads / d.n_kv_heads;
   XoArgs xa{};
@@ -863,11 +931,11 @@ cudaError_t run_acumul_xo(const kvc_dims& d, const __nv_bfloat16* q_full, const 
   a.rblocks = (a.n + a.P - 1) / a.P;
   a.items = (long long)a.units * a.rblocks;
   a.sl2 = 1.4426950408889634f / sqrtf((float)D);
-  a.scores = scores;
+  a.fx = scores ? fx : nullptr;
   a.err = err;
   xa.x_out = x_out;
   xa.d = D;
-  cudaError_t e = scores ? cudaMemsetAsync(scores, 0, (size_t)a.units * a.ns * 4, stream)
+  cudaError_t e = scores ? cudaMemsetAsync(fx, 0, (size_t)a.units * a.ns * 8, stream)
                          : cudaSuccess;
   if (e != cudaSuccess) return e;
   CUtensorMap mk, mv, mq;
@@ -886,29 +954,31 @@ cudaError_t run_acumul_xo(const kvc_dims& d, const __nv_bfloat16* q_full, const 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   count_launches(1);
-  return cudaSuccess;
+  return scores ? fixed_to_float(fx, scores, (long long)a.units * a.ns, stream) : cudaSuccess;
 }
 
 }  // namespace
 
 cudaError_t launch_acumul_xo(const kvc_dims& d, const __nv_bfloat16* q_full,
                              const __nv_bfloat16* k, const __nv_bfloat16* v, float* scores,
-                             __nv_bfloat16* x_out, unsigned* err, cudaStream_t stream) {
+                             unsigned long long* fx, __nv_bfloat16* x_out, unsigned* err,
+                             cudaStream_t stream) {
   const int g = d.n_q_heads / d.n_kv_heads;
   if (g < 1 || g > 16 || 128 % g != 0) return cudaErrorInvalidValue;
   if (d.prompt_len - d.obs_window < 1) return cudaErrorInvalidValue;
-  if (d.head_dim == 128) return run_acumul_xo<128>(d, q_full, k, v, scores, x_out, err, stream);
-  if (d.head_dim == 64) return run_acumul_xo<64>(d, q_full, k, v, scores, x_out, err, stream);
+  if (d.head_dim == 128) return run_acumul_xo<128>(d, q_full, k, v, scores, fx, x_out, err, stream);
+  if (d.head_dim == 64) return run_acumul_xo<64>(d, q_full, k, v, scores, fx, x_out, err, stream);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_acumul(const kvc_dims& d, const __nv_bfloat16* q_full, const __nv_bfloat16* k,
-                          float* scores, unsigned* err, cudaStream_t stream) {
+                          float* scores, unsigned long long* fx, unsigned* err,
+                          cudaStream_t stream) {
   const int g = d.n_q_heads / d.n_kv_heads;
   if (g < 1 || g > 16 || 128 % g != 0) return cudaErrorInvalidValue;
   if (d.prompt_len - d.obs_window < 1) return cudaErrorInvalidValue;
-  if (d.head_dim == 128) return run_acumul<128>(d, q_full, k, scores, err, stream);
-  if (d.head_dim == 64) return run_acumul<64>(d, q_full, k, scores, err, stream);
+  if (d.head_dim == 128) return run_acumul<128>(d, q_full, k, scores, fx, err, stream);
+  if (d.head_dim == 64) return run_acumul<64>(d, q_full, k, scores, fx, err, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -488,8 +488,13 @@ kvc_status kvc_prefill_acumul(kvc_cache* c, int32_t layer, const void* q_full, c
   }
   if (!q_full) return KVC_E_ARG;
   int32_t* kp = ls.kept_ptr;
+  if (!c->score_fx) {
+    c->score_fx = static_cast<unsigned long long*>(dev_alloc(c, c->score_elems * 8));
+    if (!c->score_fx) return KVC_E_OOM;
+  }
   cudaError_t e = kvc::launch_acumul(c->dims, static_cast<const __nv_bfloat16*>(q_full),
-                                     static_cast<const __nv_bfloat16*>(k), c->scores, c->err, s);
+                                     static_cast<const __nv_bfloat16*>(k), c->scores,
+                                     c->score_fx, c->err, s);
   if (e == cudaSuccess) e = kvc::launch_pool_topk(c, layer, kp, n_kept, s);
   if (e != cudaSuccess) return from_cuda(e);
   ls.scored = 1;
@@ -514,10 +519,14 @@ kvc_status kvc_prefill_attention(kvc_cache* c, int32_t layer, const void* q_full
   if (!dg.ok) return KVC_E_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool scoring = n_kept < ns;
+  if (scoring && !c->score_fx) {
+    c->score_fx = static_cast<unsigned long long*>(dev_alloc(c, c->score_elems * 8));
+    if (!c->score_fx) return KVC_E_OOM;
+  }
   cudaError_t e = kvc::launch_acumul_xo(c->dims, static_cast<const __nv_bfloat16*>(q_full),
                                         static_cast<const __nv_bfloat16*>(k),
                                         static_cast<const __nv_bfloat16*>(v),
-                                        scoring ? c->scores : nullptr,
+                                        scoring ? c->scores : nullptr, c->score_fx,
                                         static_cast<__nv_bfloat16*>(x_out), c->err, s);
   if (e != cudaSuccess) return from_cuda(e);
   if (!scoring) {                     // the budget keeps every token

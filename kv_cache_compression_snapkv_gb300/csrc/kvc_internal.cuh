@@ -197,6 +197,7 @@ struct kvc_cache {
   unsigned* gsync = nullptr;  // scoring counters, 1 + B*H words (zero between launches)
   float* scores = nullptr;
   float* pooled = nullptr;    size_t score_elems = 0;
+  unsigned long long* score_fx = nullptr;  // fixed-point sums of the cumulated attention
   float* dec_ws = nullptr;    size_t dec_ws_floats = 0;  // decode partial states
   unsigned* dec_cnt = nullptr; // decode arrival tickets, n_layers * B*H words (zero between launches)
   // error word set by bounded device waits that gave up: mapped pinned host memory
@@ -275,15 +276,19 @@ cudaError_t launch_score_into(const kvc_dims& d, const __nv_bfloat16* q_obs,
                               float* scores, unsigned* err, cudaStream_t stream);
 // Full-prompt cumulated attention (un-normalised column sums, key blocks of 128 with
 // running row maxima) of every unit into scores [unit][n - alpha]; q_full is
-// [B][Hq][n][d]. Zeroes the scores first (stream-ordered); err may be NULL.
+// [B][Hq][n][d]. The sums are accumulated in fx (64-bit fixed point, [unit][n -
+// alpha], zeroed first) and then converted: the same scores on every run. err may
+// be NULL.
 cudaError_t launch_acumul(const kvc_dims& d, const __nv_bfloat16* q_full, const __nv_bfloat16* k,
-                          float* scores, unsigned* err, cudaStream_t stream);
+                          float* scores, unsigned long long* fx, unsigned* err,
+                          cudaStream_t stream);
 // The same scores (skipped when scores is NULL) and, from the same tiles, the
 // causal attention output of every prompt query x_out [B][Hq][n][d] (bf16); v is
 // [B][Hkv][n][d].
 cudaError_t launch_acumul_xo(const kvc_dims& d, const __nv_bfloat16* q_full,
                              const __nv_bfloat16* k, const __nv_bfloat16* v, float* scores,
-                             __nv_bfloat16* x_out, unsigned* err, cudaStream_t stream);
+                             unsigned long long* fx, __nv_bfloat16* x_out, unsigned* err,
+                             cudaStream_t stream);
 // Population variance of each of `units` rows of m scores (fp32 out, one per row).
 cudaError_t launch_score_variance(const float* scores, int units, int m, float* var,
                                   cudaStream_t stream);

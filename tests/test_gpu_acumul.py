@@ -154,3 +154,36 @@ def test_prefill_attention_full_prompt_length_sampled_rows():
             assert np.all(err <= 2.0 ** -8 * (vmax + np.abs(ref))), (hh, i, err.max())
             worst = max(worst, float(err.max() / vmax))
     print(f"sampled rows {rows.tolist()}: worst |err|/max|v| {worst:.2e}")
+
+
+def test_acumul_scores_are_deterministic():
+    """The row blocks' contributions are added as fixed-point integers: three runs
+    on the same inputs give bit-identical scores and kept sets (for both the
+    selection-only kernel and the one that also forms X_O)."""
+    K = kvc()
+    spec = CASES["gqa4"][0]
+    n, a = spec.prompt_len, spec.obs_window
+    dims = K.dims_from_spec(spec, max_new_tokens=4)
+    budgets = K.kvc_plan_budgets(dims, spec.schedule, spec.avg_budget, spec.pyramid_depth)
+    x = synth.layer_inputs(spec, 0, device="cuda")
+    qf = synth.prompt_queries(spec, 0, device="cuda")
+    xo = torch.empty(spec.batch, spec.n_q_heads, n, spec.head_dim, dtype=torch.bfloat16,
+                     device="cuda")
+    cache = K.kvc_cache_create(dims, budgets)
+    for call in ("acumul", "attention"):
+        runs = []
+        for _ in range(3):
+            K.kvc_cache_reset(cache)
+            if call == "acumul":
+                K.kvc_prefill_acumul(cache, 0, qf, x["k"], x["v"])
+            else:
+                K.kvc_prefill_attention(cache, 0, qf, x["k"], x["v"], xo)
+            sc = torch.empty(spec.batch, spec.n_kv_heads, n - a, device="cuda")
+            K.kvc_scores_layer(cache, sc)
+            runs.append((sc, K.kvc_export_layer(cache, 0)["kept"]))
+        torch.cuda.synchronize()
+        for sc, kept in runs[1:]:
+            assert torch.equal(sc, runs[0][0]), f"{call}: scores differ between runs"
+            assert torch.equal(kept, runs[0][1]), f"{call}: kept sets differ between runs"
+    K.kvc_check_device(cache)
+    cache.close()
