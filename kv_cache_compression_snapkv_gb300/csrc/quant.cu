@@ -17,64 +17,118 @@ namespace {
 
 constexpr int kThreads = 256;
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+               :: "r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_one() {   // all but the latest group complete
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- kernels
-// grid.x = group index j within the unit (j < n_pack), then one CTA per 32 rows of
-// the initial window (j >= n_pack); grid.y = unit (b * H + h). n_pack is the number
-// of whole groups of kept tokens (0 with 16-bit storage: every kept token then
-// starts in the window). Kept position p of the unit is kept[p] when `kept` is
-// given; else, with sinks >= 0, the sink + recent-window position (p < sinks: p;
-// else n - alpha - (n_kept - sinks) + (p - sinks)), also stored to kept_out; else p.
+// Persistent: CTA b takes the contiguous range [G b / grid, G (b + 1) / grid) of
+// the G = units * n_pack packed groups (unit-major; n_pack is the number of whole
+// groups of kept tokens per unit, 0 with 16-bit storage where every kept token
+// starts in the window), its rows staged by cp.async two groups ahead of the group
+// being quantized (three stages), then, grid-strided, the units' initial windows (32
+// rows per item). Kept position p of the unit is kept[p] when `kept` is given;
+// else, with sinks >= 0, the sink + recent-window position (p < sinks: p; else n -
+// alpha - (n_kept - sinks) + (p - sinks)), also stored to kept_out; else p.
 template <int D, int BITS>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                     const int32_t* __restrict__ kept, int n_kept, int n, int alpha,
                     uint8_t* __restrict__ packed, int cap_groups, int block_bytes, int R,
                     __nv_bfloat16* __restrict__ win_k, __nv_bfloat16* __restrict__ win_v,
-                    int sinks, int32_t* __restrict__ kept_out, int n_pack) {
+                    int sinks, int32_t* __restrict__ kept_out, int n_pack, int units,
+                    int win_items) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  GroupStage<D>* stage = reinterpret_cast<GroupStage<D>*>(smem_raw);
+  QuantScratch<D>& qs = *reinterpret_cast<QuantScratch<D>*>(smem_raw + 3 * sizeof(GroupStage<D>));
   pdl_wait();      // the selection is complete
   pdl_release();
-  const int j = blockIdx.x, unit = blockIdx.y;
-  const int n_groups = n_pack;
-  const __nv_bfloat16* K = k + (size_t)unit * n * D;
-  const __nv_bfloat16* V = v + (size_t)unit * n * D;
-  const int32_t* kp = kept ? kept + (size_t)unit * n_kept : nullptr;
-  int32_t* ko = kept_out ? kept_out + (size_t)unit * n_kept : nullptr;
   const int recent0 = n - alpha - (n_kept - sinks);
-  auto index_of = [&](int p) -> int {
-    if (kp) return kp[p];
+  auto index_of = [&](int unit, int p) -> int {
+    if (kept) return __ldg(kept + (size_t)unit * n_kept + p);
     if (sinks >= 0) return p < sinks ? p : recent0 + (p - sinks);
     return p;
   };
-  if (j >= n_groups) {
-    // initial window: the kept tokens past the last whole group, then the
-    // alpha observation tokens, in ring slots 0 .. W-1 (rows [32 wj, 32 wj + 32) here)
-    const int n_full = n_groups * KVC_GROUP, tail = n_kept - n_full, W = tail + alpha;
-    const int wj = j - n_groups, w0 = wj * KVC_GROUP, w1 = min(W, w0 + KVC_GROUP);
+  constexpr int CH = D / 8;                      // 16-byte chunks per row
+  constexpr int TPR = kThreads / KVC_GROUP;      // threads per staged row
+  static_assert(CH % TPR == 0, "row chunks");
+  const int row = threadIdx.x / TPR, c0 = threadIdx.x % TPR;
+  const int G = units * n_pack;
+  const int g0 = (int)((long long)G * blockIdx.x / gridDim.x);
+  const int g1 = (int)((long long)G * (blockIdx.x + 1) / gridDim.x);
+  // cursors (unit, group) of the group being quantized and of the next one to stage
+  int cu = 0, cj = 0;
+  if (g0 < g1) { cu = g0 / n_pack; cj = g0 - cu * n_pack; }
+  int nu = cu, nj = cj;
+  auto advance = [&](int& u, int& j) { if (++j == n_pack) { j = 0; ++u; } };
+  auto issue = [&](GroupStage<D>& st, int u, int j, int idx) {
+    const __nv_bfloat16* ks = k + ((size_t)u * n + idx) * D;
+    const __nv_bfloat16* vs = v + ((size_t)u * n + idx) * D;
+#pragma unroll
+    for (int ch = c0; ch < CH; ch += TPR) {
+      cp_async16(&st.k[row][ch * 8], ks + ch * 8);
+      cp_async16(&st.v[row][ch * 8], vs + ch * 8);
+    }
+    if (kept_out && c0 == 0) kept_out[(size_t)u * n_kept + j * KVC_GROUP + row] = idx;
+  };
+  // three stages: groups g + 1 and g + 2 are in flight while g is quantized
+  int sidx = 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (g0 + i < g1) {
+      issue(stage[i], nu, nj, index_of(nu, nj * KVC_GROUP + row));
+      advance(nu, nj);
+    }
+    cp_async_commit();
+  }
+  if (g0 + 2 < g1) sidx = index_of(nu, nj * KVC_GROUP + row);
+  int st = 0;
+  for (int g = g0; g < g1; ++g) {
+    cp_async_wait_one();
+    __syncthreads();   // stage st is complete; every thread is done with the group before
+    const int s2 = st == 0 ? 2 : st - 1;   // (st + 2) % 3: the stage read one group ago
+    if (g + 2 < g1) {
+      issue(stage[s2], nu, nj, sidx);
+      advance(nu, nj);
+      if (g + 3 < g1) sidx = index_of(nu, nj * KVC_GROUP + row);
+    }
+    cp_async_commit();
+    uint8_t* blk = packed + ((size_t)cu * cap_groups + cj) * block_bytes;
+    quantize_block<D, BITS>(stage[st], qs, blk);
+    advance(cu, cj);
+    st = st == 2 ? 0 : st + 1;
+  }
+  cp_async_wait_all();
+  if (win_items == 0) return;
+  // initial windows: the kept tokens past the last whole group, then the alpha
+  // observation tokens, in ring slots 0 .. W-1 (item = (unit, 32-row slice))
+  const int n_full = n_pack * KVC_GROUP, tail = n_kept - n_full, W = tail + alpha;
+  const int per_unit = win_items / units;
+  for (int it = blockIdx.x; it < win_items; it += gridDim.x) {
+    const int unit = it / per_unit, wj = it - unit * per_unit;
+    const int w0 = wj * KVC_GROUP, w1 = min(W, w0 + KVC_GROUP);
+    const __nv_bfloat16* K = k + (size_t)unit * n * D;
+    const __nv_bfloat16* V = v + (size_t)unit * n * D;
+    int32_t* ko = kept_out ? kept_out + (size_t)unit * n_kept : nullptr;
     __nv_bfloat16* wk = win_k + (size_t)unit * R * D;
     __nv_bfloat16* wv = win_v + (size_t)unit * R * D;
     for (int i = w0 * D + threadIdx.x; i < w1 * D; i += kThreads) {
       const int w = i / D, c = i % D;
-      const int idx = w < tail ? index_of(n_full + w) : n - alpha + (w - tail);
+      const int idx = w < tail ? index_of(unit, n_full + w) : n - alpha + (w - tail);
       if (ko && c == 0 && w < tail) ko[n_full + w] = idx;
       window_store(wk, wv, w, c, D, K[(size_t)idx * D + c], V[(size_t)idx * D + c]);
     }
-    return;
   }
-  GroupSmem<D, kThreads>& s = *reinterpret_cast<GroupSmem<D, kThreads>*>(smem_raw);
-  constexpr int CH = D / 8;   // 16-byte chunks per row
-  for (int i = threadIdx.x; i < KVC_GROUP * CH; i += kThreads) {
-    const int t = i / CH, ch = i % CH;
-    const int idx = index_of(j * KVC_GROUP + t);
-    if (ko && ch == 0) ko[j * KVC_GROUP + t] = idx;
-    *reinterpret_cast<uint4*>(&s.k[t][ch * 8]) =
-        __ldg(reinterpret_cast<const uint4*>(K + (size_t)idx * D) + ch);
-    *reinterpret_cast<uint4*>(&s.v[t][ch * 8]) =
-        __ldg(reinterpret_cast<const uint4*>(V + (size_t)idx * D) + ch);
-  }
-  __syncthreads();
-  uint8_t* blk = packed + ((size_t)unit * cap_groups + j) * block_bytes;
-  quantize_block<D, BITS, kThreads>(s, blk);
 }
 
 struct AppendParams {
@@ -108,7 +162,8 @@ append_kernel(AppendParams P, int units, const __nv_bfloat16* __restrict__ k_new
   const int fs = P.flush_start[lrel];
   if (fs < 0) return;
   __syncthreads();   // the new token may belong to the flushed group (R == 32)
-  GroupSmem<D, kThreads>& s = *reinterpret_cast<GroupSmem<D, kThreads>*>(smem_raw);
+  GroupStage<D>& s = *reinterpret_cast<GroupStage<D>*>(smem_raw);
+  QuantScratch<D>& qs = *reinterpret_cast<QuantScratch<D>*>(smem_raw + sizeof(GroupStage<D>));
   for (int i = threadIdx.x; i < KVC_GROUP * D; i += kThreads) {
     const int t = i / D, c = i % D;
     const int sl = fs + t;
@@ -119,8 +174,8 @@ append_kernel(AppendParams P, int units, const __nv_bfloat16* __restrict__ k_new
   const int bits = P.bits[lrel];
   uint8_t* blk = packed + P.packed_off[lrel] +
                  ((size_t)unit * P.cap_groups[lrel] + P.flush_group[lrel]) * block_bytes(D, bits);
-  if (bits == 2) quantize_block<D, 2, kThreads>(s, blk);
-  else quantize_block<D, 4, kThreads>(s, blk);
+  if (bits == 2) quantize_block<D, 2>(s, qs, blk);
+  else quantize_block<D, 4>(s, qs, blk);
 }
 
 // Export: grid.x = group j (or window when j == n_groups), grid.y = unit
@@ -184,7 +239,9 @@ __global__ void export_kept_kernel(const int32_t* __restrict__ kept, int n_kept,
 }
 
 template <int D>
-constexpr size_t group_smem() { return sizeof(GroupSmem<D, kThreads>); }
+constexpr size_t group_smem() { return sizeof(GroupStage<D>) + sizeof(QuantScratch<D>); }
+template <int D>
+constexpr size_t gather_smem() { return 3 * sizeof(GroupStage<D>) + sizeof(QuantScratch<D>); }
 
 }  // namespace
 
@@ -215,12 +272,23 @@ cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* ke
   const int win_ctas = (win_rows + KVC_GROUP - 1) / KVC_GROUP;
   const int units = d.batch * d.n_kv_heads;
   const size_t woff = ls.win_off;
+  if ((long long)units * groups >= (1ll << 31)) return cudaErrorInvalidValue;
+  const int win_items = units * win_ctas;
   KVC_DISPATCH_DB(d.head_dim, exact ? 2 : ls.bits, {
-    const size_t sm = group_smem<D>();
+    const size_t sm = gather_smem<D>();
     cudaError_t e = set_smem(gather_quant_kernel<D, BITS>, sm);
     if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_quant_kernel<D, BITS>,
+                                                      kThreads, sm);
+    if (e != cudaSuccess) return e;
+    const long long want = (long long)units * groups > win_items ? (long long)units * groups
+                                                                 : win_items;
+    long long grid = (long long)c->n_sm * (per_sm > 0 ? per_sm : 1);
+    if (grid > want) grid = want;
+    if (grid < 1) grid = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(groups + (win_ctas > 0 ? win_ctas : 1), units);
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = sm;
     cfg.stream = stream;
@@ -230,7 +298,7 @@ cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* ke
     e = cudaLaunchKernelEx(&cfg, gather_quant_kernel<D, BITS>, k, v, kept, n_kept, d.prompt_len,
                            d.obs_window, c->packed + ls.packed_off, ls.cap_groups,
                            ls.block_bytes, ls.R, c->win_k + woff, c->win_v + woff,
-                           sinks, kept_out, groups);
+                           sinks, kept_out, groups, units, win_items);
     if (e != cudaSuccess) return e;
   });
   count_launches(1);
