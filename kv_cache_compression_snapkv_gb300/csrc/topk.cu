@@ -222,9 +222,9 @@ pool_topk_kernel(const float* __restrict__ scores, float* __restrict__ pooled, i
 // above the selected one): the ordered compaction needs no further exchange. The
 // passes stop early once the selected bin is kept whole.
 constexpr int kCluster = 8;
-constexpr int kCThreads = 256;
+constexpr int kCThreads = 1024;   // threads 0..255 also own one histogram bin each
 constexpr int kCWarps = kCThreads / 32;
-constexpr int kMaxSeg = 24 * 1024;   // elements per CTA (two fp32 copies in shared memory)
+constexpr int kMaxSeg = 22 * 1024;   // elements per CTA (two fp32 copies in shared memory)
 constexpr size_t kOnePerSm = 120 * 1024;   // dynamic shared memory that leaves room for one CTA
 
 struct ClusterSmem {
@@ -329,22 +329,21 @@ __device__ void cluster_pool_select(ClusterSmem& s, float* dyn, const float* __r
   int shift = 24;
   for (int pass = 0; pass < 4; ++pass, shift -= 8) {
     unsigned* h = s.hist[pass & 1];
-#pragma unroll
-    for (int ww = 0; ww < kCWarps; ++ww) s.whist[ww][threadIdx.x] = 0u;   // 256 bins
+    for (int t = threadIdx.x; t < kCWarps * 256; t += kCThreads) (&s.whist[0][0])[t] = 0u;
     __syncthreads();
     for (int t = threadIdx.x; t < n_loc; t += kCThreads) {
       const unsigned u = __float_as_uint(pl[t]);
       if ((u & mask) == prefix) atomicAdd(&s.whist[warp][(u >> shift) & 255u], 1u);
     }
     __syncthreads();
-    {
+    if (threadIdx.x < 256) {
       unsigned hb = 0;
 #pragma unroll
       for (int ww = 0; ww < kCWarps; ++ww) hb += s.whist[ww][threadIdx.x];
       h[threadIdx.x] = hb;
     }
     cluster_sync_all();   // every CTA's histogram of this pass is complete
-    {
+    if (threadIdx.x < 256) {
       const int b = threadIdx.x;
 #pragma unroll
       for (int r = 0; r < kCluster; ++r) v[r] = ld_cluster_u32(&h[b], (unsigned)r);
@@ -384,7 +383,7 @@ __device__ void cluster_pool_select(ClusterSmem& s, float* dyn, const float* __r
     }
     __syncthreads();
     const unsigned sel = s.sel_bin;
-    if ((unsigned)threadIdx.x > sel) {
+    if (threadIdx.x < 256 && (unsigned)threadIdx.x > sel) {
 #pragma unroll
       for (int r = 0; r < kCluster; ++r) gacc[r] += v[r];
     }
