@@ -758,9 +758,13 @@ kvc_status kvc_score_variance(kvc_cache* c, float* var_out, void* stream) {
   DeviceGuard dg(c->device);
   if (!dg.ok) return KVC_E_CUDA;
   const kvc_dims& d = c->dims;
-  return from_cuda(kvc::launch_score_variance(c->scores, d.batch * d.n_kv_heads,
-                                              d.prompt_len - d.obs_window, var_out,
-                                              static_cast<cudaStream_t>(stream)));
+  // the slices' partials go to the scoring launch's statistics scratch and the units'
+  // tickets to its arrival counters (both idle between launches; the tickets return
+  // to zero)
+  return from_cuda(kvc::launch_score_variance(
+      c->scores, d.batch * d.n_kv_heads, d.prompt_len - d.obs_window, var_out,
+      reinterpret_cast<double*>(c->stats), c->stats_elems, c->gsync + 1,
+      static_cast<cudaStream_t>(stream)));
 }
 
 kvc_status kvc_scores_layer(kvc_cache* c, float* scores, float* pooled, void* stream) {

@@ -291,6 +291,7 @@ cudaError_t launch_acumul_xo(const kvc_dims& d, const __nv_bfloat16* q_full,
                              cudaStream_t stream);
 // Population variance of each of `units` rows of m scores (fp32 out, one per row).
 cudaError_t launch_score_variance(const float* scores, int units, int m, float* var,
+                                  double* ws, size_t ws_doubles, unsigned* cnt,
                                   cudaStream_t stream);
 // abort_flag (may be NULL): when it is non-zero at launch time every kept index is
 // written as -1.
