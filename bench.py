@@ -497,7 +497,8 @@ def run_gpu(args):
     dec_gbs = mean_bytes / (att_ms / 1e3) / 1e9
     # compression: algorithmic bytes and flops per layer
     ns = spec.prompt_len - spec.obs_window
-    comp_bytes, comp_flops, t_roof = compress_roofline(spec, budgets, hbm, tc)
+    comp_bytes, comp_flops, comp_exps, t_roof, comp_bound = compress_roofline(spec, budgets,
+                                                                              hbm, tc)
     comp_frac = t_roof / (comp_ms / 1e3)
     # sink + recent selection: kept rows read, packed groups and window rows written
     sink_bytes = 0
@@ -540,7 +541,8 @@ def run_gpu(args):
             "ms_per_layer": sink_ms, "bytes": sink_bytes,
             "frac": sink_bytes / (hbm * 1e9) / (sink_ms * L / 1e3),
             "note": "4 attention sinks + the most recent tokens within each layer's budget"},
-        "compress_roofline": {"bytes": comp_bytes, "flops": comp_flops, "t_roof_ms": t_roof * 1e3,
+        "compress_roofline": {"bytes": comp_bytes, "flops": comp_flops, "exps": comp_exps,
+                              "bound": comp_bound, "t_roof_ms": t_roof * 1e3,
                               "frac": comp_frac},
         "wall_ms_per_step": wall * 1e3,
         "roofline": roofline,
@@ -584,12 +586,31 @@ def decode_bytes(K, cache, spec):
     return tot + L * B * Hq * D * (2 + 4) + L * B * Hk * D * 2 * 2
 
 
+MUFU_PER_CLK_SM = 16   # exp2 results per clock per SM (special-function units, sm_100 family)
+
+
+def mufu_peak():
+    """exp2 results per second: the SFU rate per SM x SMs x the maximum SM clock."""
+    import torch
+    n_sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        mhz = 2070.0
+    return MUFU_PER_CLK_SM * n_sm * mhz * 1e6
+
+
 def compress_roofline(spec, budgets, hbm, tc):
-    """Algorithmic bytes and flops of compressing every layer, and the roofline time."""
+    """Algorithmic bytes, flops and exponentials of compressing every layer, and the
+    roofline time: the slowest of the three at its peak (HBM copy, bf16 tensor, SFU
+    exp2). The scoring evaluates one exp2 per (observation row, key) in each of its two
+    passes (row normalisers over all n keys, then the column sums over the n - alpha
+    scored ones); the normalisers must be complete before any column sum."""
     B, Hk, Hq, D, L = spec.batch, spec.n_kv_heads, spec.n_q_heads, spec.head_dim, spec.n_layers
     block_bytes = 8 * D * (spec.bits + 1)
     ns = spec.prompt_len - spec.obs_window
-    comp_bytes = comp_flops = 0
+    comp_bytes = comp_flops = comp_exps = 0
     for l in range(L):
         kept = min(budgets[l], ns)
         scored = kept < ns
@@ -598,8 +619,12 @@ def compress_roofline(spec, budgets, hbm, tc):
                        + B * Hk * (kept // 32) * block_bytes
                        + (B * Hq * spec.obs_window * D * 2 if scored else 0))
         comp_flops += 2 * B * Hq * spec.obs_window * spec.prompt_len * D if scored else 0
-    t_roof = max(comp_bytes / (hbm * 1e9), comp_flops / (tc * 1e12))
-    return comp_bytes, comp_flops, t_roof
+        comp_exps += B * Hq * spec.obs_window * (spec.prompt_len + ns) if scored else 0
+    terms = {"hbm": comp_bytes / (hbm * 1e9), "tensor": comp_flops / (tc * 1e12)}
+    if comp_exps:
+        terms["sfu"] = comp_exps / mufu_peak()
+    bound = max(terms, key=terms.get)
+    return comp_bytes, comp_flops, comp_exps, terms[bound], bound
 
 
 def run_leg(K, wid, hbm, tc, dev, flush):
@@ -653,13 +678,14 @@ def run_leg(K, wid, hbm, tc, dev, flush):
     att_ms = statistics.mean(att[warm:])
     mean_bytes = statistics.mean(nbytes[warm:])
     gbs = mean_bytes / (att_ms / 1e3) / 1e9
-    cb, cf, t_roof = compress_roofline(spec, budgets, hbm, tc)
+    cb, cf, ce, t_roof, cbound = compress_roofline(spec, budgets, hbm, tc)
     return {"workload": workload_desc(spec, S),
             "decode_tokens_per_s": B * S / (sum(att) / 1e3),
             "decode_attn_us_per_launch": att_ms * 1e3,
             "bytes_per_launch": mean_bytes, "cache_gbs": gbs, "cache_frac_of_hbm": gbs / hbm,
             "compress_ms_per_layer": comp_ms / L,
-            "compress_roofline": {"bytes": cb, "flops": cf, "t_roof_ms": t_roof * 1e3,
+            "compress_roofline": {"bytes": cb, "flops": cf, "exps": ce, "bound": cbound,
+                                  "t_roof_ms": t_roof * 1e3,
                                   "frac": t_roof / (comp_ms / 1e3)},
             "note": "decode: one launch per token over all layers (append + split-K attention), "
                     "L2 flushed before each; compression: each layer's call timed alone, its "
