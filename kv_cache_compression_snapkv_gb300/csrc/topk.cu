@@ -510,9 +510,25 @@ cudaError_t launch_topk_cluster(const float* scores, float* pooled, int units, i
   return cudaGetLastError();
 }
 
+// The cluster kernel spreads a long row over 8 SMs, for few units; with many units,
+// or rows short enough that a cluster's barriers would outweigh its work, one CTA per
+// unit (the row staged in shared memory) fills the GPU by itself.
+static bool use_cluster(int units, int ns, int w) {
+  if ((ns + kCluster - 1) / kCluster > kMaxSeg || w > 129) return false;
+  if (ns > kSmemMax) return true;
+  static int n_sm = 0;
+  if (!n_sm) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n_sm = 148;
+  }
+  return ns > 8192 && units * 2 <= n_sm;
+}
+
 cudaError_t launch_topk(const float* scores, float* pooled, int units, int ns, int w, int k_sel,
                         int32_t* kept, const unsigned* abort_flag, cudaStream_t stream) {
-  if ((ns + kCluster - 1) / kCluster <= kMaxSeg && w <= 129)
+  if (use_cluster(units, ns, w))
     return launch_topk_cluster(scores, pooled, units, ns, w, k_sel, kept, abort_flag, stream);
   if (ns <= kSmemMax) {
     const size_t sm = (size_t)ns * sizeof(float);
