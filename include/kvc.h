@@ -244,7 +244,9 @@ kvc_status kvc_prefill_sinks(kvc_cache* cache, int32_t layer, int32_t n_sinks, c
  *   observation window is kept); n_kept <= the layer's budget. The cache must
  *   exist (created by kvc_prefill_compress or kvc_cache_create).
  *   Errors: as kvc_prefill_compress; KVC_E_CAPACITY if n_kept > budget. Index
- *   order/range is the caller's contract (not checked on the device).
+ *   order/range is the caller's contract; the checked build (kvc_build_checked)
+ *   tests the range on the device, skips an index outside it (position 0 is read
+ *   instead) and the next call on the cache returns KVC_E_DEVICE_CHECK.
  * ------------------------------------------------------------------------- */
 kvc_status kvc_prefill_selected(kvc_cache* cache, int32_t layer, const int32_t* kept,
                                 int32_t n_kept, const void* k, const void* v,
@@ -320,10 +322,19 @@ kvc_status kvc_decode_step(kvc_cache* cache, int32_t layer_begin, int32_t layer_
                            float* out, void* stream);
 
 /* kvc_check_device -- synchronize `stream` and report device-side failures
- * recorded since the last check: KVC_E_TIMEOUT if a bounded wait inside a
- * kernel gave up (that kernel then skipped the affected work), KVC_OK otherwise.
+ * recorded since the last check: KVC_E_DEVICE_CHECK if a check of the checked
+ * build found an index out of range, else KVC_E_TIMEOUT if a bounded wait inside
+ * a kernel gave up (that kernel then skipped the affected work), KVC_OK otherwise.
  * The error word is cleared. */
 kvc_status kvc_check_device(kvc_cache* cache, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * kvc_build_checked -- 1 if this library was compiled with device-side checks
+ *   (KVC_CHECKED=1 at build time: caller-supplied indices are range-checked on the
+ *   device and reported as KVC_E_DEVICE_CHECK by the next call on the cache, in
+ *   place of an out-of-range access), else 0.
+ * ------------------------------------------------------------------------- */
+int32_t kvc_build_checked(void);
 
 /* kvc_set_wait_limit -- bound every staging wait of this cache's decode launches
  * to `polls` polls of its mbarrier (0: each wait gives up at once); a negative

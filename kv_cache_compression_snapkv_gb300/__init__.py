@@ -12,7 +12,9 @@ import os
 from typing import Optional, Sequence
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkvc.so")
+# KVC_LIB selects another build of the library (e.g. libkvc_checked.so, with
+# device-side index checks); by default the one built next to this file.
+LIB_PATH = os.environ.get("KVC_LIB") or os.path.join(_HERE, "libkvc.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -89,6 +91,8 @@ for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
     _f.restype = ctypes.c_int
+_lib.kvc_build_checked.argtypes = []
+_lib.kvc_build_checked.restype = ctypes.c_int32
 _lib.kvc_launch_count.argtypes = []
 _lib.kvc_launch_count.restype = ctypes.c_uint64
 _lib.kvc_status_string.argtypes = [ctypes.c_int]
@@ -319,7 +323,9 @@ def kvc_select_noalloc_check(stream=None):
 
 
 def kvc_check_device(cache: Cache, stream=None):
-    """Synchronize and raise KvcError(KVC_E_TIMEOUT) if a bounded device wait gave up."""
+    """Synchronize and raise KvcError(KVC_E_DEVICE_CHECK) if a check of the checked
+    build found an index out of range, KvcError(KVC_E_TIMEOUT) if a bounded device wait
+    gave up."""
     _check(_lib.kvc_check_device(cache.handle, _stream(stream)), "kvc_check_device")
 
 
@@ -332,9 +338,14 @@ def kvc_launch_count() -> int:
     return int(_lib.kvc_launch_count())
 
 
+def kvc_build_checked() -> bool:
+    """True if the loaded library was built with device-side index checks."""
+    return bool(_lib.kvc_build_checked())
+
+
 def exported_symbols() -> list:
     """Names of the C entry points this binding resolved."""
-    return sorted(list(_SIGS) + ["kvc_status_string", "kvc_launch_count"])
+    return sorted(list(_SIGS) + ["kvc_status_string", "kvc_launch_count", "kvc_build_checked"])
 
 
 __all__ = ["KvcDims", "KvcError", "Cache", "make_dims", "dims_from_spec", "kvc_plan_budgets",
@@ -344,6 +355,6 @@ __all__ = ["KvcDims", "KvcError", "Cache", "make_dims", "dims_from_spec", "kvc_p
            "kvc_layer_info_get", "kvc_export_layer", "kvc_scores_layer", "kvc_cache_reset",
            "kvc_plan_budgets_weighted", "kvc_score_variance", "kvc_prefill_acumul",
            "kvc_prefill_attention",
-           "kvc_launch_count", "kvc_check_device", "kvc_select_noalloc",
+           "kvc_launch_count", "kvc_check_device", "kvc_build_checked", "kvc_select_noalloc",
            "kvc_select_noalloc_check", "kvc_set_wait_limit", "LIB_PATH",
            "exported_symbols"]

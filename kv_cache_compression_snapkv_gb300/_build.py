@@ -17,6 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvc.so")
+LIB_CHECKED = os.path.join(PKG, "libkvc_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -32,8 +33,8 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, extra, obj_dir: str = OBJ) -> str:
+    obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -41,20 +42,25 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra=()) -> str:
-    """Compile every CUDA source and link libkvc.so; returns the library path."""
-    os.makedirs(OBJ, exist_ok=True)
+def build(verbose: bool = False, extra=(), checked: bool = False) -> str:
+    """Compile every CUDA source and link libkvc.so (libkvc_checked.so with
+    checked=True: device-side index checks, KVC_CHECKED=1); returns the library path."""
+    obj_dir = OBJ + ("_checked" if checked else "")
+    lib = LIB_CHECKED if checked else LIB
+    flags = list(extra) + (["-DKVC_CHECKED=1"] if checked else [])
+    os.makedirs(obj_dir, exist_ok=True)
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, list(extra)), SOURCES))
-    cmd = [nvcc(), *ARCH, "-shared", "-o", LIB + ".tmp", *objs, "-lcudart_static"]
+        objs = list(ex.map(lambda s: _compile(s, flags, obj_dir), SOURCES))
+    cmd = [nvcc(), *ARCH, "-shared", "-o", lib + ".tmp", *objs, "-lcudart_static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(LIB + ".tmp", LIB)
+    os.replace(lib + ".tmp", lib)
     if verbose:
-        print(f"built {LIB}")
-    return LIB
+        print(f"built {lib}")
+    return lib
 
 
 if __name__ == "__main__":
-    build(verbose=True, extra=sys.argv[1:])
+    args = [a for a in sys.argv[1:] if a != "--checked"]
+    build(verbose=True, extra=args, checked="--checked" in sys.argv[1:])

@@ -121,10 +121,16 @@ bool make_error_word(kvc_cache* c) {
 
 // A bounded device wait of earlier work on the cache gave up (seen without a
 // synchronisation where the error word is host-visible): report it once.
+kvc_status word_status(unsigned word) {
+  if (word == 0u) return KVC_OK;
+  return (word & kvc::kErrDeviceCheck) ? KVC_E_DEVICE_CHECK : KVC_E_TIMEOUT;
+}
+
 kvc_status pending_error(kvc_cache* c) {
   if (c->err_host && *c->err_host != 0u) {
+    const unsigned word = *c->err_host;
     *c->err_host = 0u;
-    return KVC_E_TIMEOUT;
+    return word_status(word);
   }
   return KVC_OK;
 }
@@ -704,14 +710,16 @@ kvc_status kvc_check_device(kvc_cache* c, void* stream) {
   if (c->err_host) {
     word = *c->err_host;
     *c->err_host = 0u;
-    return word == 0 ? KVC_OK : KVC_E_TIMEOUT;
+    return word_status(word);
   }
   if (cudaMemcpy(&word, c->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
     return KVC_E_CUDA;
   if (word == 0) return KVC_OK;
   if (cudaMemset(c->err, 0, sizeof(word)) != cudaSuccess) return KVC_E_CUDA;
-  return KVC_E_TIMEOUT;
+  return word_status(word);
 }
+
+int32_t kvc_build_checked(void) { return kvc::kChecked ? 1 : 0; }
 
 kvc_status kvc_set_wait_limit(kvc_cache* c, int64_t polls) {
   if (!c) return KVC_E_ARG;

@@ -159,6 +159,17 @@ __host__ __device__ constexpr int off_kzero(int D, int bits) { return 2 * code_b
 __host__ __device__ constexpr int off_vscale(int D, int bits) { return 2 * code_bytes(D, bits) + 4 * D; }
 __host__ __device__ constexpr int off_vzero(int D, int bits) { return 2 * code_bytes(D, bits) + 6 * D; }
 
+// A device-side check of the checked build (compiled with -DKVC_CHECKED=1) that
+// found a caller-supplied index out of range sets this bit of the cache's error word
+// (the access is skipped); the next call on the cache returns KVC_E_DEVICE_CHECK.
+// Waits that give up set other bits (KVC_E_TIMEOUT).
+constexpr unsigned kErrDeviceCheck = 1u << 31;
+#if defined(KVC_CHECKED) && KVC_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
 // ------------------------------------------------------------------ cache state
 struct LayerState {
   int prefilled = 0;

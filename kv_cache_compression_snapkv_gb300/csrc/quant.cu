@@ -47,7 +47,7 @@ gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
                     uint8_t* __restrict__ packed, int cap_groups, int block_bytes, int R,
                     __nv_bfloat16* __restrict__ win_k, __nv_bfloat16* __restrict__ win_v,
                     int sinks, int32_t* __restrict__ kept_out, int n_pack, int units,
-                    int win_items) {
+                    int win_items, unsigned* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   GroupStage<D>* stage = reinterpret_cast<GroupStage<D>*>(smem_raw);
   QuantScratch<D>& qs = *reinterpret_cast<QuantScratch<D>*>(smem_raw + 3 * sizeof(GroupStage<D>));
@@ -55,7 +55,14 @@ gather_quant_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
   pdl_release();
   const int recent0 = n - alpha - (n_kept - sinks);
   auto index_of = [&](int unit, int p) -> int {
-    if (kept) return __ldg(kept + (size_t)unit * n_kept + p);
+    if (kept) {
+      int idx = __ldg(kept + (size_t)unit * n_kept + p);
+      if (kChecked && (idx < 0 || idx >= n - alpha)) {   // outside the scored range
+        if (err) atomicOr(err, kErrDeviceCheck);
+        idx = 0;
+      }
+      return idx;
+    }
     if (sinks >= 0) return p < sinks ? p : recent0 + (p - sinks);
     return p;
   };
@@ -298,7 +305,7 @@ cudaError_t launch_gather_quant(const kvc_cache* c, int layer, const int32_t* ke
     e = cudaLaunchKernelEx(&cfg, gather_quant_kernel<D, BITS>, k, v, kept, n_kept, d.prompt_len,
                            d.obs_window, c->packed + ls.packed_off, ls.cap_groups,
                            ls.block_bytes, ls.R, c->win_k + woff, c->win_v + woff,
-                           sinks, kept_out, groups, units, win_items);
+                           sinks, kept_out, groups, units, win_items, c->err);
     if (e != cudaSuccess) return e;
   });
   count_launches(1);
