@@ -712,13 +712,18 @@ def e2e_measure(K, spec, dims, budgets, cache, prompt, qs, kns, vns, S, dev, ste
          hv.numel() * hv.element_size())
     d2h = hout.numel() * 4
 
-    def step():
+    def step(parts=None):
         K.kvc_cache_reset(cache)
+        ta = time.perf_counter()
         for l in range(L):
             for k in dp:
                 dp[k].copy_(hp[l][k], non_blocking=True)
             K.kvc_prefill_compress(dims, budgets, l, dp.get("q_obs"), dp["k"], dp["v"],
                                    cache=cache)
+        if parts is not None:
+            torch.cuda.synchronize()
+            parts["prompt_copy_and_compress_ms"] = (time.perf_counter() - ta) * 1e3
+        tb = time.perf_counter()
         for t in range(S):
             dq.copy_(hq[t], non_blocking=True)
             dk.copy_(hk[t], non_blocking=True)
@@ -726,14 +731,18 @@ def e2e_measure(K, spec, dims, budgets, cache, prompt, qs, kns, vns, S, dev, ste
             K.kvc_decode_step(cache, 0, L, dq, dk, dv, dout)
             hout[t].copy_(dout, non_blocking=True)
         torch.cuda.synchronize()
+        if parts is not None:
+            parts["decode_steps_ms"] = (time.perf_counter() - tb) * 1e3
 
     step()
     t0 = time.perf_counter()
     for _ in range(steps):
         step()
     dt = (time.perf_counter() - t0) / steps
+    parts = {}
+    step(parts)     # one more step, synchronised between its two phases, for the split
     return {"value": spec.batch * S / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "parts": parts,
             "note": "includes the prompt's host->device copy and prefill compression"}
 
 
