@@ -34,6 +34,14 @@ CASES = {
                                       head_dim=64, prompt_len=32800, obs_window=32,
                                       avg_budget=4096, schedule="uniform", bits=4,
                                       window_len=64), 12, "score"),
+    # scoring rows not a multiple of 32: M = 2 x 20 = 40 (one partial 32-row chunk of
+    # the column sums) and M = 8 x 25 = 200 (two row halves, the second partial)
+    "obs20_m40": (synth.small_spec(2, n_layers=2, batch=2, n_q_heads=4, n_kv_heads=2,
+                                   prompt_len=900, obs_window=20, avg_budget=128,
+                                   window_len=64), 30, "score"),
+    "obs25_m200": (synth.small_spec(2, n_layers=1, batch=1, n_q_heads=16, n_kv_heads=2,
+                                    prompt_len=1100, obs_window=25, avg_budget=160,
+                                    window_len=64), 30, "score"),
     # attention sinks + recent tokens (no scoring), pyramid budgets over 3 layers
     "sinks_window": (synth.small_spec(2, n_layers=3, batch=2, n_q_heads=8, n_kv_heads=2,
                                       prompt_len=1000, obs_window=32, avg_budget=96,
