@@ -692,24 +692,44 @@ def run_leg(K, wid, hbm, tc, dev, flush):
                     "inputs generated outside the timed interval"}
 
 
-def e2e_measure(K, spec, dims, budgets, cache, prompt, qs, kns, vns, S, dev, steps=2):
+def e2e_measure(K, spec, dims, budgets, cache, prompt, qs, kns, vns, S, dev, steps=2,
+                warmup=3):
     """Same metric through the C ABI with host buffers: every step copies the
-    prompt (pinned host -> device) before compressing it, and each decode step's
-    inputs in and its output back."""
+    prompt (pinned host -> device) before compressing it, waits for the prefill,
+    then copies each decode step's inputs in and its output back."""
     import torch
     L = spec.n_layers
-    hp = [{k: v.cpu().pin_memory() for k, v in x.items()
-           if isinstance(v, torch.Tensor) and k in ("q_obs", "k", "v")} for x in prompt]
-    hq = torch.stack(qs).cpu().pin_memory()
-    hk = torch.stack(kns).cpu().pin_memory()
-    hv = torch.stack(vns).cpu().pin_memory()
+    # the whole prompt (every layer's q_obs, k, v) as views of one pinned buffer:
+    # measured ~6 % faster to copy in than the same bytes as separate pinned tensors
+    names = ("q_obs", "k", "v")
+    sizes = [[x[k].numel() * x[k].element_size() for k in names if k in x] for x in prompt]
+    pool = torch.empty(sum(map(sum, sizes)), dtype=torch.uint8, pin_memory=True)
+    hp, off = [], 0
+    for x in prompt:
+        d = {}
+        for k in names:
+            if k not in x:
+                continue
+            nb = x[k].numel() * x[k].element_size()
+            d[k] = pool[off:off + nb].view(x[k].dtype).view(x[k].shape)
+            d[k].copy_(x[k])
+            off += nb
+        hp.append(d)
+    # each decode step's q, k_new and v_new side by side in one pinned row (one
+    # host -> device copy per step), landing in one device buffer they are views of
+    nq, nk, nv = qs[0].numel(), kns[0].numel(), vns[0].numel()
+    assert qs[0].dtype == kns[0].dtype == vns[0].dtype
+    hin = torch.empty(S, nq + nk + nv, dtype=qs[0].dtype, pin_memory=True)
+    hin.copy_(torch.cat([torch.stack(x).reshape(S, -1) for x in (qs, kns, vns)], dim=1))
     hout = torch.empty(S, *qs[0].shape, dtype=torch.float32).pin_memory()
     dp = {k: torch.empty_like(v, device=dev) for k, v in hp[0].items()}
-    dq, dk, dv = (torch.empty_like(qs[0]), torch.empty_like(kns[0]), torch.empty_like(vns[0]))
+    din = torch.empty(nq + nk + nv, dtype=qs[0].dtype, device=dev)
+    dq = din[:nq].view(qs[0].shape)
+    dk = din[nq:nq + nk].view(kns[0].shape)
+    dv = din[nq + nk:].view(vns[0].shape)
     dout = torch.empty(qs[0].shape, dtype=torch.float32, device=dev)
     h2d = sum(v.numel() * v.element_size() for x in hp for v in x.values()) + \
-        (hq.numel() * hq.element_size() + hk.numel() * hk.element_size() +
-         hv.numel() * hv.element_size())
+        hin.numel() * hin.element_size()
     d2h = hout.numel() * 4
 
     def step(parts=None):
@@ -720,30 +740,37 @@ def e2e_measure(K, spec, dims, budgets, cache, prompt, qs, kns, vns, S, dev, ste
                 dp[k].copy_(hp[l][k], non_blocking=True)
             K.kvc_prefill_compress(dims, budgets, l, dp.get("q_obs"), dp["k"], dp["v"],
                                    cache=cache)
+        # the prefill is waited for before the first decode step, as a server does
+        # before it emits its first token
+        torch.cuda.synchronize()
         if parts is not None:
-            torch.cuda.synchronize()
             parts["prompt_copy_and_compress_ms"] = (time.perf_counter() - ta) * 1e3
         tb = time.perf_counter()
         for t in range(S):
-            dq.copy_(hq[t], non_blocking=True)
-            dk.copy_(hk[t], non_blocking=True)
-            dv.copy_(hv[t], non_blocking=True)
+            din.copy_(hin[t], non_blocking=True)
             K.kvc_decode_step(cache, 0, L, dq, dk, dv, dout)
             hout[t].copy_(dout, non_blocking=True)
         torch.cuda.synchronize()
         if parts is not None:
             parts["decode_steps_ms"] = (time.perf_counter() - tb) * 1e3
 
-    step()
+    for _ in range(warmup):     # as before the device-timed steps; the first pass
+        step()                  # over the pinned prompt is the slowest
+    step_ms = []
     t0 = time.perf_counter()
     for _ in range(steps):
+        ts = time.perf_counter()
         step()
+        step_ms.append((time.perf_counter() - ts) * 1e3)
     dt = (time.perf_counter() - t0) / steps
     parts = {}
-    step(parts)     # one more step, synchronised between its two phases, for the split
+    step(parts)     # one more step, each phase's wall time recorded
     return {"value": spec.batch * S / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "parts": parts,
-            "note": "includes the prompt's host->device copy and prefill compression"}
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "step_ms": step_ms,
+            "parts": parts,
+            "note": "includes the prompt's host->device copy and prefill compression (waited "
+                    "for before decoding), one host->device copy of each decode step's "
+                    "q|k_new|v_new and the device->host copy of its output"}
 
 
 def main():
