@@ -56,10 +56,13 @@ def test_score_variance_matches_oracle():
                 worst_own = max(worst_own, abs(var[b, h] - own) / own)
                 worst_ora = max(worst_ora, abs(var[b, h] - ora) / ora)
     print(f"variance vs own scores {worst_own:.2e}, vs oracle {worst_ora:.2e}")
-    # the reduction: each thread's compensated (Kahan) fp32 sums of its elements and
-    # of their squared deviations (each square rounded once to fp32, 2^-24
-    # relative), the 256 partial sums added in fp64, the result rounded to fp32:
-    # a few fp32 ulps in all at these lengths, far below 1e-6
+    # the reduction: the scores cut into slices, one CTA each; each thread's
+    # compensated (Kahan) fp32 sums of its elements and of their squared deviations
+    # about the slice's fp32-rounded mean (each square rounded once to fp32, 2^-24
+    # relative; the mean's rounding corrected in fp64), added across a warp in
+    # double-float and across warps in fp64; the slices' (count, sum, M2) merged
+    # pairwise in fp64; the result rounded to fp32: a few fp32 ulps in all at these
+    # lengths, far below 1e-6
     assert worst_own <= 1e-6
     assert worst_ora <= 1e-3        # plus the scores' own tolerance (1e-4 each)
 
