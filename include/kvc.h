@@ -395,12 +395,17 @@ kvc_status kvc_export_layer(kvc_cache* cache, int32_t layer, const kvc_export* d
 /* kvc_score_variance -- the variance score of the last scored layer (MiniKV
  * §4.2, Figure 7: the variance of cumulated attention), per (sequence, kv head):
  * the population variance, over the prompt_len - obs_window selectable
- * positions, of the selection scores (before pooling), accumulated in fp64 and
- * written as fp32 to var_out (device, [B][H]). The mean over (B, H) is the
- * layer's weight for Var-prop / Var-inv budgets. One launch on `stream`. Only
- * valid right after kvc_prefill_compress of a scoring layer (the scratch is
- * reused by the next one). Errors: KVC_E_ARG (null pointer), KVC_E_STATE (no
- * layer scored yet), KVC_E_CUDA. */
+ * positions, of the selection scores (before pooling): the observation-window
+ * scores after kvc_prefill_compress, the cumulated attention A_cumul after
+ * kvc_prefill_acumul or kvc_prefill_attention. Compensated fp32 sums per thread,
+ * the block's and the slices' partials combined in double-float and fp64 in a
+ * fixed order (the result does not depend on timing), written as fp32 to
+ * var_out (device, [B][H]). The mean over (B, H) is the layer's weight for
+ * Var-prop / Var-inv budgets. One launch on `stream`. Only valid right after the
+ * scoring call (the scratch is reused by the next one); kvc_prefill_compress does
+ * not score a layer kept whole (budget >= prompt_len - obs_window). Errors:
+ * KVC_E_ARG (null pointer), KVC_E_STATE (no layer scored since create or reset),
+ * KVC_E_CUDA. */
 kvc_status kvc_score_variance(kvc_cache* cache, float* var_out, void* stream);
 
 /* kvc_scores_layer -- copy the last scored layer's selection scores (fp32,
