@@ -79,16 +79,23 @@ typedef enum kvc_schedule {
 typedef void* (*kvc_alloc_fn)(size_t bytes, void* stream, void* ctx);
 typedef void (*kvc_free_fn)(void* ptr, void* stream, void* ctx);
 
+/* Size limits of kvc_dims (KVC_E_SHAPE beyond them): every token count and
+ * per-head capacity the library forms on the host then stays inside int32. */
+#define KVC_MAX_PROMPT_LEN (1 << 30)     /* prompt_len                          */
+#define KVC_MAX_NEW_TOKENS (1 << 24)     /* max_new_tokens                      */
+#define KVC_MAX_QUERY_HEADS (1 << 24)    /* batch * n_q_heads                   */
+
 /* The problem statement (MiniKV Definition 2.1 plus the selection and window
  * parameters of PyramidKV §4.2.2 and MiniKV §4.4). */
 typedef struct kvc_dims {
   int32_t n_layers;       /* transformer layers (1..256)                           */
-  int32_t batch;          /* independent sequences                                 */
+  int32_t batch;          /* independent sequences (batch * n_q_heads at most      */
+                          /*   KVC_MAX_QUERY_HEADS)                                */
   int32_t n_q_heads;      /* query heads; a multiple of n_kv_heads                 */
   int32_t n_kv_heads;     /* key/value heads (GQA group g = n_q_heads/n_kv_heads,  */
                           /*   g in {1, 2, 4, 8})                                  */
   int32_t head_dim;       /* 64 or 128                                             */
-  int32_t prompt_len;     /* n, tokens in the prompt                               */
+  int32_t prompt_len;     /* n, tokens in the prompt (1..KVC_MAX_PROMPT_LEN)       */
   int32_t obs_window;     /* alpha, trailing observation/instruction tokens;       */
                           /*   0 only with KVC_SCHED_NONE budgets (no scoring)     */
   int32_t pool_kernel;    /* w, odd max-pool width (1 = no pooling)                */
@@ -101,6 +108,7 @@ typedef struct kvc_dims {
   int32_t window_len;     /* R, bf16 recent window; a multiple of G, 32..1024      */
                           /*   (up to 65536 with bits == 16)                       */
   int32_t max_new_tokens; /* decode steps the cache is sized for                   */
+                          /*   (0..KVC_MAX_NEW_TOKENS)                             */
   kvc_alloc_fn alloc;     /* optional; NULL = cudaMalloc                           */
   kvc_free_fn free;       /* optional; must be set when alloc is                   */
   void* alloc_ctx;        /* passed to alloc/free                                  */

@@ -41,11 +41,12 @@ kvc_status check_dims(const kvc_dims* d) {
   if (!d) return KVC_E_ARG;
   if (d->n_layers < 1 || d->n_layers > 256) return KVC_E_SHAPE;
   if (d->batch < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1) return KVC_E_SHAPE;
+  if ((int64_t)d->batch * d->n_q_heads > KVC_MAX_QUERY_HEADS) return KVC_E_SHAPE;
   if (d->n_q_heads % d->n_kv_heads) return KVC_E_SHAPE;
   const int g = d->n_q_heads / d->n_kv_heads;
   if (g != 1 && g != 2 && g != 4 && g != 8) return KVC_E_SHAPE;
   if (d->head_dim != 64 && d->head_dim != 128) return KVC_E_SHAPE;
-  if (d->prompt_len < 1) return KVC_E_SHAPE;
+  if (d->prompt_len < 1 || d->prompt_len > KVC_MAX_PROMPT_LEN) return KVC_E_SHAPE;
   if (d->obs_window < 0 || d->obs_window >= d->prompt_len) return KVC_E_SHAPE;
   if (d->pool_kernel < 1 || d->pool_kernel % 2 == 0) return KVC_E_ARG;
   if (d->bits != 2 && d->bits != 4 && d->bits != 16) return KVC_E_ARG;
@@ -55,6 +56,7 @@ kvc_status check_dims(const kvc_dims* d) {
       d->window_len % KVC_GROUP)
     return KVC_E_SHAPE;
   if (d->max_new_tokens < 0) return KVC_E_ARG;
+  if (d->max_new_tokens > KVC_MAX_NEW_TOKENS) return KVC_E_SHAPE;
   if (d->obs_window >= d->window_len) return KVC_E_SHAPE;
   if ((d->alloc == nullptr) != (d->free == nullptr)) return KVC_E_ARG;
   return KVC_OK;
@@ -145,7 +147,7 @@ int kept_cap(const kvc_dims& d, int budget) {
 // 16-bit storage (no packed store, no flush), every kept, observation and appended
 // token.
 bool window_fits(const kvc_dims& d, int bits, int R, int n_kept) {
-  if (bits == 16) return n_kept + d.obs_window + d.max_new_tokens <= R;
+  if (bits == 16) return (int64_t)n_kept + d.obs_window + d.max_new_tokens <= R;
   return n_kept % KVC_GROUP + d.obs_window < R;
 }
 
@@ -154,8 +156,9 @@ bool window_fits(const kvc_dims& d, int bits, int R, int n_kept) {
 // hold every token it will store.
 int ring_len(const kvc_dims& d, int bits, int n_kept) {
   if (bits != 16 || d.bits == 16) return d.window_len;
-  const int need = n_kept + d.obs_window + d.max_new_tokens;
-  return std::max(KVC_GROUP, (need + KVC_GROUP - 1) / KVC_GROUP * KVC_GROUP);
+  const int64_t need = (int64_t)n_kept + d.obs_window + d.max_new_tokens;
+  const int64_t R = (need + KVC_GROUP - 1) / KVC_GROUP * KVC_GROUP;
+  return (int)std::min<int64_t>(std::max<int64_t>(KVC_GROUP, R), INT32_MAX / 2);
 }
 
 kvc_status create(const kvc_dims* dims, const int32_t* budgets, const int32_t* layer_bits,
