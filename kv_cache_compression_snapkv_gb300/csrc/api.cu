@@ -594,9 +594,12 @@ kvc_status kvc_prefill_selected(kvc_cache* c, int32_t layer, const int32_t* kept
   const int units = c->dims.batch * c->dims.n_kv_heads;
   ls.scored = 0;
   if (n_kept > 0) {
-    // keep a copy of the selection (row stride n_kept) for export
+    // keep a copy of the selection (row stride n_kept) for export; a keep-all layer
+    // has no stored selection from creation: it gets one sized for the largest
+    // selection the layer allows (its budget, clipped to prompt_len - obs_window),
+    // so that a later call (after kvc_cache_reset) with more kept positions fits
     if (!ls.kept_ptr) {
-      ls.kept_ptr = static_cast<int32_t*>(dev_alloc(c, (size_t)units * n_kept * 4));
+      ls.kept_ptr = static_cast<int32_t*>(dev_alloc(c, (size_t)units * ls.budget * 4));
       if (!ls.kept_ptr) return KVC_E_OOM;
     }
     cudaError_t e = cudaMemcpyAsync(ls.kept_ptr, kept, (size_t)units * n_kept * 4,

@@ -82,3 +82,45 @@ def test_mixed_precision_layers():
     print(f"mixed: excused={rep.excused} codes={rep.codes_compared} "
           f"decode_err={rep.decode_err:.2e}")
     assert rep.decode_checked > 0
+
+
+def test_selected_after_reset_on_a_keep_all_layer():
+    """A keep-all layer (budget >= prompt_len - obs_window) has no stored selection
+    from creation; kvc_prefill_selected gives it one. After kvc_cache_reset a second
+    call with more kept positions must still fit, and its store is compared with
+    the oracle's on the same selection (kept set, codes, scales, zero-points and
+    window, bit for bit)."""
+    import numpy as np
+    import torch
+    from _parity import Report, check_export, kvc, np64
+    from oracle import OracleCache
+
+    K = kvc()
+    B, Hq, Hk, D, n, a = 1, 4, 2, 128, 512, 16
+    dims = K.make_dims(1, B, Hq, Hk, D, n, a, 7, 2, 32, 64, 4)
+    budgets = K.kvc_plan_budgets(dims, "none", 0)
+    assert budgets[0] >= n - a
+    gen = torch.Generator().manual_seed(91)
+    k = torch.randn(B, Hk, n, D, generator=gen).to(torch.bfloat16)
+    v = torch.randn(B, Hk, n, D, generator=gen).to(torch.bfloat16)
+    rng = np.random.default_rng(91)
+    cache = K.kvc_cache_create(dims, budgets)
+    try:
+        for nk in (64, 200):
+            sel = [[np.sort(rng.choice(n - a, nk, replace=False)) for _ in range(Hk)]
+                   for _ in range(B)]
+            kept = torch.tensor(np.array(sel), dtype=torch.int32, device="cuda")
+            K.kvc_cache_reset(cache)
+            K.kvc_prefill_selected(cache, 0, kept, nk, k.cuda(), v.cuda())
+            ex = K.kvc_export_layer(cache, 0)
+            torch.cuda.synchronize()
+            oc = OracleCache(B, Hq, Hk, D, 2, 32, 64)
+            oc.prefill(np64(k), np64(v), a, kept=sel)
+            for b in range(B):
+                for h in range(Hk):
+                    np.testing.assert_array_equal(ex["kept"][b, h].cpu().numpy(), sel[b][h])
+            rep = Report()
+            check_export(ex, oc, [(b, h) for b in range(B) for h in range(Hk)], rep)
+            assert rep.codes_compared == B * Hk * (nk // 32 * 32)
+    finally:
+        cache.close()
