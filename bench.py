@@ -16,7 +16,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -154,7 +153,6 @@ def oracle_sample(spec, n_layers_sample=2, n_steps=8):
 
     Returns (compress seconds per layer, decode seconds per token per layer, text).
     """
-    import numpy as np
     import synth
     from oracle import OracleCache
     budgets = _budgets_host(spec)

@@ -18,14 +18,13 @@ Acceptance rules (compressed-KV parity):
 """
 from __future__ import annotations
 
-import math
 from dataclasses import dataclass, field
 
 import numpy as np
 import torch
 
 import synth
-from oracle import OracleCache, prefill_attention, sinks_window_select, snapkv_select
+from oracle import OracleCache, prefill_attention, sinks_window_select
 
 DECODE_RTOL = 2e-3
 TIE_RTOL = 1e-5

@@ -3,7 +3,6 @@ order, capacity, argument checks, and the bounded-wait timeout path of the decod
 kernel (driven by a zero wait limit: every staging wait gives up at once, so no
 GPU ever hangs or faults), after which the cache is reset and must give exactly
 the outputs of a fresh cache."""
-import ctypes
 
 import pytest
 import torch
