@@ -128,11 +128,7 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   return y;
 }
 
-// v as an fp16 pair (hi, lo) with hi = fp16(v), lo = fp16(v - hi): hi in the low half.
-__device__ __forceinline__ uint32_t split_f16(float v) {
-  const float hi = __half2float(__float2half_rn(v));
-  return h2u(__floats2half2_rn(v, v - hi));
-}
+// v as a bf16 pair (hi, lo) with hi = bf16(v), lo = bf16(v - hi): hi in the low half.
 __device__ __forceinline__ uint32_t split_bf16(float v) {
   const float hi = __bfloat162float(__float2bfloat16_rn(v));
   const __nv_bfloat162 p = __floats2bfloat162_rn(v, v - hi);

@@ -74,9 +74,6 @@ struct CodePos {
   int bit;    // bit offset of the code inside the word
 };
 
-// Words of one section a lane owns (D*BITS/32) and pairs per word (16/BITS).
-__host__ __device__ constexpr int words_per_lane(int D, int bits) { return D * bits / 32; }
-
 // Bit of pair slot P inside each 16-bit half of a word: slot P sits in byte
 // P / (8/bits) at field P % (8/bits).
 __host__ __device__ constexpr int pair_bit(int P, int bits) {
@@ -92,23 +89,7 @@ __host__ __device__ constexpr int pair_bit(int P, int bits) {
 //   values 2-bit: word mt,               slot 4rl + 2ks + rh
 //          4-bit: word 2mt + ks,         slot 2rl + rh
 // so the field of a code (slot % (8/bits)) depends only on its k index.
-struct FragPos { int mt, ks, rl, rh; };
-
-__host__ __device__ inline FragPos key_frag(int wi, int P, int D, int bits) {
-  const int KS = D >> 4;
-  FragPos f;
-  if (bits == 2) { f.mt = wi / (KS >> 1); f.ks = 2 * (wi % (KS >> 1)) + ((P >> 1) & 1); f.rl = P >> 2; }
-  else { f.mt = wi / KS; f.ks = wi % KS; f.rl = P >> 1; }
-  f.rh = P & 1;
-  return f;
-}
-__host__ __device__ inline FragPos value_frag(int wi, int P, int bits) {
-  FragPos f;
-  if (bits == 2) { f.mt = wi; f.ks = (P >> 1) & 1; f.rl = P >> 2; }
-  else { f.mt = wi >> 1; f.ks = wi & 1; f.rl = P >> 1; }
-  f.rh = P & 1;
-  return f;
-}
+// kcode_pos / vcode_pos below give the word and bit of each (token, channel).
 
 __host__ __device__ inline int word_addr(int lane, int wi) { return (wi >> 2) * 128 + lane * 4 + (wi & 3); }
 
