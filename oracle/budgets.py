@@ -24,6 +24,11 @@ Readings taken where the pages are silent or disagree:
     fractional parts, an integer) go one each to the layers with the largest
     remainders, ties to the lower layer. All integer arithmetic.
   * Budgets are finally clipped to the number of selectable prompt tokens.
+
+Parity unpinned as to the reading: which endpoints the pages mean (MiniKV's x/d
+form rather than PyramidKV's beta form) is a reading, not a pinned fact. The
+schedule it gives is pinned (exact sums, the long-context workload's 1,920 / 128
+endpoints, one group from the exact line).
 """
 from __future__ import annotations
 

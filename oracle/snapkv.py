@@ -21,6 +21,11 @@ Readings (the score and pooling equations are lost on the PyramidKV page):
   * Pooling is a stride-1 max over [i - (w-1)/2, i + (w-1)/2] clipped to the
     scored range [0, n - alpha), applied after the window/group sum.
   * Top-k ties go to the lower index; the kept indices are returned ascending.
+
+Parity unpinned as to the reading: no page prints a worked selection, so the
+order of the GQA sum and the pool (sum first, then pool) is a reading, not a
+pinned fact. The arithmetic of that reading is pinned (closed forms, brute force,
+scipy's maximum filter).
 """
 from __future__ import annotations
 
