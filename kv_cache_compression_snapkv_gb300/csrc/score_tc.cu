@@ -85,7 +85,9 @@ struct TcArgs {
   int M;          // rows per unit (g * alpha)
   int MP;         // M rounded up to 16 (N of the column-phase MMA)
   int units;
-  int ubatch;     // units per batch
+  int ubatch;     // units per batch; every batch must give each CTA a row-stats tile
+                  // (a unit's wait counts the CTAs over its tiles, and a CTA
+                  // without a tile of the batch would never arrive)
   int tiles0;     // 256-key tiles per unit, row-stats phase (all n keys)
   int tiles1;     // 256-key tiles per unit, column phase (the ns scored keys)
   int smax;       // partial slots per (unit, row)
