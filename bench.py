@@ -196,6 +196,29 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it: its model name, else (Arm) the
+    implementer and part codes; with the machine architecture."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k, v = k.strip().lower(), v.strip()
+                if k in ("model name", "cpu implementer", "cpu part") and k not in fields:
+                    fields[k] = v
+    except Exception:
+        pass
+    if "model name" in fields:
+        name = fields["model name"]
+    elif "cpu part" in fields:
+        name = f"implementer {fields.get('cpu implementer', '?')} part {fields['cpu part']}"
+    else:
+        name = "unknown"
+    return f"{name} ({platform.machine()})"
+
+
 def run_reference(args):
     rank, world, _ = rank_info()
     if rank != 0:
@@ -222,7 +245,7 @@ def run_reference(args):
         "config": {"workload": workload_desc(spec, S)},
         "compress_ms_per_layer": statistics.mean(comp),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                         "sample": text},
+                         "sample": text, "cpu": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -556,7 +579,7 @@ def run_gpu(args):
         c, d, text = oracle_sample(spec)
         per_token = d * L
         line["cpu_baseline"] = {"value": B / per_token, "unit": UNIT, "cores": cpu_cores(),
-                                "kind": "oracle", "sample": text,
+                                "kind": "oracle", "sample": text, "cpu": cpu_model(),
                                 "compress_ms_per_layer": c * 1e3}
     cache.close()
     legs = [int(w) for w in args.legs.split(",") if w.strip()] if args.legs else []
