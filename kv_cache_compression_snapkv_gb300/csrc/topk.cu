@@ -63,6 +63,12 @@ __device__ __forceinline__ void block_scan2(TopkSmem& s, unsigned a, unsigned b,
 
 // When the scoring launch before this one gave up a wait (*abort_flag != 0; the
 // flag may be NULL), its scores are incomplete: every kept index is written as -1.
+// Every thread of every CTA must read the same value (a CTA of a cluster that left
+// early would strand its peers at a cluster barrier), so the flag is final when it
+// is read: only the scoring launch writes it, the plain launch starts after that
+// launch and the cluster launch reads it after griddepcontrol.wait, and the host
+// clears it only after synchronising the stream. The cache's own selections pass
+// no flag (their error word is host-visible and cleared by the next call).
 __device__ __forceinline__ bool selection_aborted(const unsigned* abort_flag, int32_t* out,
                                                   int k_sel, bool writer) {
   if (!abort_flag || *reinterpret_cast<const volatile unsigned*>(abort_flag) == 0u) return false;
