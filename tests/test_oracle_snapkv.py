@@ -59,6 +59,13 @@ def test_pool_matches_library_filter():
         s = rng.random(97)
         np.testing.assert_array_equal(max_pool(s, w),
                                       maximum_filter1d(s, size=w, mode="nearest"))
+    # windows as wide as or wider than the row (short prompts): every position
+    # sees the whole row, or all of it within reach
+    for n, w in ((1, 7), (3, 7), (5, 11), (6, 7), (7, 25)):
+        s = rng.random(n)
+        np.testing.assert_array_equal(max_pool(s, w),
+                                      maximum_filter1d(s, size=w, mode="nearest"))
+    np.testing.assert_array_equal(max_pool(np.array([0.2, 0.9, 0.1]), 25), [0.9, 0.9, 0.9])
 
 
 def test_pool_rejects_even_kernel():
