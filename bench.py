@@ -576,7 +576,8 @@ def run_gpu(args):
     if not args.no_e2e:
         line["e2e"] = e2e_measure(K, spec, dims, budgets, cache, prompt, qs, kns, vns, S, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        c, d, text = oracle_sample(spec)
+        # ~10 s of oracle work on the box's 16 host cores (2.7 s per long-context layer)
+        c, d, text = oracle_sample(spec, n_layers_sample=4)
         per_token = d * L
         line["cpu_baseline"] = {"value": B / per_token, "unit": UNIT, "cores": cpu_cores(),
                                 "kind": "oracle", "sample": text, "cpu": cpu_model(),
