@@ -35,9 +35,11 @@ def nvcc() -> str:
 
 def _compile(src: str, extra, obj_dir: str = OBJ) -> str:
     obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
+    if os.path.exists(obj):
+        os.remove(obj)   # never link an object left from an earlier build
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
+    if r.returncode != 0 or not os.path.exists(obj):
         raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
     return obj
 
@@ -62,5 +64,10 @@ def build(verbose: bool = False, extra=(), checked: bool = False) -> str:
 
 
 if __name__ == "__main__":
+    if any(a in ("-h", "--help") for a in sys.argv[1:]):
+        print("usage: python -m kv_cache_compression_snapkv_gb300._build [--checked] "
+              "[extra nvcc flags ...]\n  --checked  build libkvc_checked.so (KVC_CHECKED=1: "
+              "device-side checks of caller-given indices)")
+        sys.exit(0)
     args = [a for a in sys.argv[1:] if a != "--checked"]
     build(verbose=True, extra=args, checked="--checked" in sys.argv[1:])
