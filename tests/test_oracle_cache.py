@@ -102,3 +102,43 @@ def test_selected_tail_goes_to_window():
     assert st.n_packed == 32
     np.testing.assert_array_equal(st.win_k[:8], k[0, 0, kept[0][0][32:]])
     np.testing.assert_array_equal(st.win_k[8:], k[0, 0, n - a:])
+
+
+def test_flush_all_agrees_when_window_equals_group():
+    """MiniKV (Algorithm 1, decoding) keeps new tokens in a 16-bit buffer and, when
+    it holds n_r tokens, quantizes all of them and empties it; the cache here flushes
+    its oldest group whenever the window reaches R. With R = G = n_r the two are the
+    same schedule: restated independently below (a list that is quantized whole and
+    cleared), the packed store and the window agree after every step."""
+    G = R = 32
+    d, n, a = 32, 200, 16
+    rng = np.random.default_rng(3)
+    k = rng.normal(size=(1, 1, n, d)).astype(np.float32).astype(np.float64)
+    v = rng.normal(size=(1, 1, n, d)).astype(np.float32).astype(np.float64)
+    cache = OracleCache(1, 1, 1, d, 2, G, R)
+    kept = [[np.arange(0, 2 * G)]]                 # two whole groups, no tail
+    cache.prefill(k, v, a, kept=kept)
+    st = cache.heads[0][0]
+    # flush-all model: the buffer starts with the observation tokens
+    buf_k, buf_v = list(k[0, 0, n - a:]), list(v[0, 0, n - a:])
+    packed_k = [st.kcodes.copy()]
+    for t in range(100):
+        nk = rng.normal(size=(1, 1, d)).astype(np.float32).astype(np.float64)
+        nv = rng.normal(size=(1, 1, d)).astype(np.float32).astype(np.float64)
+        cache.append(nk, nv)
+        buf_k.append(nk[0, 0])
+        buf_v.append(nv[0, 0])
+        if len(buf_k) == R:                        # n_r tokens: quantize all, empty
+            kc, kS, kZ = quantize_keys(np.array(buf_k), 2, G)
+            vc, vS, vZ = quantize_values(np.array(buf_v), 2, G)
+            packed_k.append(kc)
+            np.testing.assert_array_equal(st.kcodes[-G:], kc)
+            np.testing.assert_array_equal(st.vcodes[-G:], vc)
+            np.testing.assert_array_equal(st.kS[-1:], kS)
+            np.testing.assert_array_equal(st.vS[-G:], vS)
+            buf_k, buf_v = [], []
+        np.testing.assert_array_equal(st.kcodes, np.vstack(packed_k))
+        assert len(st.win_k) == len(buf_k)
+        if buf_k:
+            np.testing.assert_array_equal(st.win_k, np.array(buf_k))
+            np.testing.assert_array_equal(st.win_v, np.array(buf_v))
