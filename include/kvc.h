@@ -40,7 +40,8 @@
  *     error word and its kernel winds down (its output is then undefined).
  *     Where the device has native atomics on host memory (e.g. a Grace-hosted
  *     GPU) the word lives in mapped pinned host memory, and the next call on the
- *     cache made after the word was set returns KVC_E_TIMEOUT, enqueues nothing
+ *     cache made after the word was set returns KVC_E_TIMEOUT (KVC_E_DEVICE_CHECK
+ *     when a device-side check of the checked build set it), enqueues nothing
  *     and clears it; elsewhere kvc_check_device reports it. After KVC_E_TIMEOUT
  *     the cache's contents are undefined: kvc_cache_reset and prefill again.
  *   - Tensors are dense, row-major, bf16 unless stated; outputs are fp32.
@@ -261,7 +262,11 @@ kvc_status kvc_prefill_selected(kvc_cache* cache, int32_t layer, const int32_t* 
                                 void* stream);
 
 /* kvc_cache_create -- create an empty cache for dims/budgets (what
- * kvc_prefill_compress does when *cache is NULL). */
+ * kvc_prefill_compress does when *cache is NULL); budgets: host int32
+ * [n_layers], each clipped to prompt_len - obs_window. Errors: KVC_E_ARG (null
+ * pointer, a negative budget, invalid argument values of dims), KVC_E_SHAPE
+ * (unsupported dims or beyond the size limits, an initial window that does not
+ * fit its ring, g * obs_window > 256 for a scoring layer), KVC_E_OOM, KVC_E_CUDA. */
 kvc_status kvc_cache_create(const kvc_dims* dims, const int32_t* budgets,
                             kvc_cache** cache);
 
@@ -324,7 +329,9 @@ kvc_status kvc_decode_attn(kvc_cache* cache, int32_t layer_begin, int32_t layer_
  * when the window reaches R) and attend q (as kvc_decode_attn); the results equal
  * those two calls made in sequence. One launch, or two in the steps where some
  * layer's window fills (the append with its group flush runs first). Shapes as in
- * those calls. */
+ * those calls. Errors: KVC_E_STATE (a layer not prefilled), KVC_E_CAPACITY (more
+ * than max_new_tokens appends), KVC_E_ARG (null pointer, q or out not 16-byte
+ * aligned, layers out of range), KVC_E_CUDA. */
 kvc_status kvc_decode_step(kvc_cache* cache, int32_t layer_begin, int32_t layer_count,
                            const void* q, const void* k_new, const void* v_new,
                            float* out, void* stream);
