@@ -172,8 +172,10 @@ kvc_status kvc_plan_budgets_weighted(const kvc_dims* dims, int32_t avg_budget,
  *   whole groups of 32 kept tokens (ascending position) are quantized into the
  *   packed store; the remaining kept tokens and then the alpha observation
  *   tokens start the bf16 window.
- *   Errors: KVC_E_ARG, KVC_E_SHAPE (e.g. initial window not shorter than R),
- *   KVC_E_STATE (layer already compressed), KVC_E_OOM, KVC_E_CUDA.
+ *   Errors: KVC_E_ARG (null k, v or cache; q_obs NULL for a scoring layer;
+ *   layer out of range), KVC_E_SHAPE (dims unlike the cache's, or as
+ *   kvc_cache_create), KVC_E_STATE (layer already compressed), KVC_E_OOM,
+ *   KVC_E_CUDA.
  * ------------------------------------------------------------------------- */
 kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets,
                                 int32_t layer, const void* q_obs, const void* k,
