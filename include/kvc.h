@@ -159,8 +159,9 @@ kvc_status kvc_plan_budgets_weighted(const kvc_dims* dims, int32_t avg_budget,
  * kvc_prefill_compress -- compress one layer's prompt into the cache.
  *   PyramidKV §4.2.2; MiniKV §4.1, §4.4 and Algorithm 1 (prefill part).
  *   If *cache is NULL a cache is created for `dims` and `budgets` (host,
- *   n_layers int32, as from kvc_plan_budgets) and returned in *cache; later
- *   calls must pass the same dims. Each layer is compressed once.
+ *   n_layers int32, as from kvc_plan_budgets) and returned in *cache (the
+ *   call's arguments are checked first: a call rejected by them creates
+ *   nothing); later calls must pass the same dims. Each layer is compressed once.
  *   q_obs: device bf16 [batch][n_q_heads][obs_window][head_dim], the queries of
  *          the last obs_window prompt positions (may be NULL when the layer's
  *          budget keeps every token).

@@ -203,9 +203,12 @@ def kvc_cache_create_layers(dims: KvcDims, budgets: Sequence[int],
 def kvc_prefill_compress(dims: KvcDims, budgets: Sequence[int], layer: int, q_obs, k, v,
                          cache: Optional[Cache] = None, stream=None) -> Cache:
     h = ctypes.c_void_p(cache.handle if cache is not None else None)
-    _check(_lib.kvc_prefill_compress(ctypes.byref(dims), _budget_array(budgets), layer,
-                                     _ptr(q_obs), _ptr(k), _ptr(v), ctypes.byref(h),
-                                     _stream(stream)), "kvc_prefill_compress")
+    st = _lib.kvc_prefill_compress(ctypes.byref(dims), _budget_array(budgets), layer,
+                                   _ptr(q_obs), _ptr(k), _ptr(v), ctypes.byref(h),
+                                   _stream(stream))
+    if st != KVC_OK and cache is None and h.value:
+        _lib.kvc_free(h.value)    # created by this call, which then failed
+    _check(st, "kvc_prefill_compress")
     return cache if cache is not None else Cache(h.value, dims, budgets)
 
 

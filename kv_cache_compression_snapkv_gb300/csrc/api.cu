@@ -443,7 +443,13 @@ kvc_status kvc_prefill_compress(const kvc_dims* dims, const int32_t* budgets, in
                                 kvc_cache** cache, void* stream) {
   if (!cache || !dims) return KVC_E_ARG;
   if (*cache == nullptr) {
-    kvc_status st = create(dims, budgets, nullptr, cache);
+    // the call's own arguments first: a call that fails creates nothing
+    kvc_status st = check_dims(dims);
+    if (st != KVC_OK) return st;
+    if (!budgets || !k || !v || layer < 0 || layer >= dims->n_layers) return KVC_E_ARG;
+    if (budgets[layer] >= 0 && budgets[layer] < dims->prompt_len - dims->obs_window && !q_obs)
+      return KVC_E_ARG;
+    st = create(dims, budgets, nullptr, cache);
     if (st != KVC_OK) return st;
   } else if (!same_dims((*cache)->dims, *dims)) {
     return KVC_E_SHAPE;

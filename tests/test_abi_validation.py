@@ -187,3 +187,25 @@ def test_select_noalloc_without_a_device():
     P = ctypes.c_void_p(256)
     dims = _dims()
     assert K._lib.kvc_select_noalloc(ctypes.byref(dims), 64, P, P, P, None, None) == E_CUDA
+
+
+@host_only
+def test_prefill_compress_checks_its_arguments_before_creating_a_cache():
+    """With *cache NULL, a call whose own arguments are invalid returns KVC_E_ARG
+    and creates nothing (on a machine without a GPU, creation would fail with
+    KVC_E_CUDA, so KVC_E_ARG shows the check came first)."""
+    P = ctypes.c_void_p(256)   # made-up addresses: every case returns before a launch
+    dims = _dims()
+    f = K._lib.kvc_prefill_compress
+    scoring = (ctypes.c_int32 * 4)(64, 64, 64, 64)
+    keep_all = (ctypes.c_int32 * 4)(*([4096 - 32] * 4))
+    for budgets, layer, q, k, v in ((scoring, 0, P, None, P), (scoring, 0, P, P, None),
+                                    (scoring, 4, P, P, P), (scoring, -1, P, P, P),
+                                    (scoring, 0, None, P, P), (None, 0, P, P, P)):
+        h = ctypes.c_void_p()
+        assert f(ctypes.byref(dims), budgets, layer, q, k, v, ctypes.byref(h), None) == E_ARG
+        assert h.value is None, "nothing created"
+    # a keep-all layer needs no observation queries: creation is reached
+    h = ctypes.c_void_p()
+    assert f(ctypes.byref(dims), keep_all, 0, None, P, P, ctypes.byref(h), None) == E_CUDA
+    assert h.value is None
