@@ -714,7 +714,7 @@ def run_leg(K, wid, hbm, tc, dev, flush):
                     "inputs generated outside the timed interval"}
 
 
-def e2e_measure(K, spec, dims, budgets, cache, prompt, qs, kns, vns, S, dev, steps=2,
+def e2e_measure(K, spec, dims, budgets, cache, prompt, qs, kns, vns, S, dev, steps=4,
                 warmup=3):
     """Same metric through the C ABI with host buffers: every step copies the
     prompt (pinned host -> device) before compressing it, waits for the prefill,
